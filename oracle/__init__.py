@@ -1,0 +1,152 @@
+"""CPU oracle for the attention forward -- TEST INFRASTRUCTURE ONLY.
+
+Only the tests, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The product path (the CUDA library and
+its Python binding) never imports, links or calls it, and it shares no code
+with that path: its arithmetic lives in ``attn_oracle.c`` (plain C, fp64),
+which is built with gcc into ``oracle/lib/liboracle_attn.so``.
+
+Every function takes Q, K, V as ``uint16`` arrays of bf16 bit patterns shaped
+[B, H, N, D] (the layout of the C ABI) and returns float64 results.
+
+Pins for every function here live in ``tests/oracle_pins.py`` (closed forms,
+invariants, an independent tiled online-softmax restatement, a library
+routine and a 50-digit brute force).  The one part left unpinned is the GPU's
+own fp32/bf16 rounding, which nothing fixes beyond the stated tolerance.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+SOURCE = os.path.join(_HERE, "attn_oracle.c")
+_LIBDIR = os.path.join(_HERE, "lib")
+_LIB = os.path.join(_LIBDIR, "liboracle_attn.so")
+_lock = threading.Lock()
+_default = None
+
+
+def compile_source(src: str, out: str) -> str:
+    """gcc the C oracle ``src`` into the shared library ``out`` (OpenMP when available)."""
+    os.makedirs(os.path.dirname(out), exist_ok=True)
+    tmp = out + f".tmp{os.getpid()}"
+    base = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fPIC", "-shared", "-o", tmp, src, "-lm"]
+    try:
+        subprocess.run(base[:1] + ["-fopenmp"] + base[1:], check=True, capture_output=True)
+    except subprocess.CalledProcessError:
+        subprocess.run(base, check=True, capture_output=True)
+    os.replace(tmp, out)
+    return out
+
+
+def build(force: bool = False) -> str:
+    """Build ``oracle/lib/liboracle_attn.so`` if it is missing or stale; returns its path."""
+    if not force and os.path.exists(_LIB) and os.path.getmtime(_LIB) >= os.path.getmtime(SOURCE):
+        return _LIB
+    return compile_source(SOURCE, _LIB)
+
+
+def _bits(a: np.ndarray) -> np.ndarray:
+    a = np.ascontiguousarray(a)
+    if a.dtype != np.uint16 or a.ndim != 4:
+        raise TypeError("expected uint16 bf16 bit patterns shaped [B, H, N, D]")
+    return a
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+class Oracle:
+    """ctypes view of one compiled copy of ``attn_oracle.c``."""
+
+    def __init__(self, libpath: str):
+        lib = ctypes.CDLL(libpath)
+        P, I64, I = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+        lib.oracle_attn_fwd.argtypes = [P, P, P, P, P, I64, I64, I64, I64, I, ctypes.c_double, I]
+        lib.oracle_attn_rows.argtypes = [P, P, P, I64, I64, I64, I, ctypes.c_double, P, P, I64, P, P, I]
+        lib.oracle_attn_probs.argtypes = [P, P, P, P, P, P, I64, I64, I64, I64, I, ctypes.c_double]
+        lib.oracle_threads.argtypes = [I]
+        for f in (lib.oracle_attn_fwd, lib.oracle_attn_rows, lib.oracle_attn_probs, lib.oracle_threads):
+            f.restype = I
+        self._lib = lib
+        self.path = libpath
+
+    def threads(self, nthreads: int = 0) -> int:
+        """OpenMP threads a call with ``nthreads`` uses (0 means all available)."""
+        return self._lib.oracle_threads(nthreads)
+
+    def attn_fwd(self, q, k, v, causal: bool, scale: float, nthreads: int = 0):
+        """(O [B,H,N,D] float64, LSE [B,H,N] float64) by the two-pass definition."""
+        q, k, v = _bits(q), _bits(k), _bits(v)
+        if not (q.shape == k.shape == v.shape):
+            raise ValueError("q, k, v must have one shape")
+        B, H, N, D = q.shape
+        o = np.empty((B, H, N, D), dtype=np.float64)
+        lse = np.empty((B, H, N), dtype=np.float64)
+        rc = self._lib.oracle_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, D,
+                                       int(bool(causal)), float(scale), int(nthreads))
+        if rc != 0:
+            raise RuntimeError("oracle_attn_fwd failed")
+        return o, lse
+
+    def attn_rows(self, q, k, v, causal: bool, scale: float, bh_idx, row_idx, nthreads: int = 0):
+        """O and LSE for the rows (bh_idx[r], row_idx[r]) only: shapes [R, D] and [R]."""
+        q, k, v = _bits(q), _bits(k), _bits(v)
+        B, H, N, D = q.shape
+        bh = np.ascontiguousarray(bh_idx, dtype=np.int64)
+        ri = np.ascontiguousarray(row_idx, dtype=np.int64)
+        if bh.shape != ri.shape or bh.ndim != 1:
+            raise ValueError("bh_idx and row_idx must be 1-D and of one length")
+        R = bh.shape[0]
+        o = np.empty((R, D), dtype=np.float64)
+        lse = np.empty((R,), dtype=np.float64)
+        rc = self._lib.oracle_attn_rows(_ptr(q), _ptr(k), _ptr(v), B * H, N, D, int(bool(causal)),
+                                        float(scale), _ptr(bh), _ptr(ri), R, _ptr(o), _ptr(lse),
+                                        int(nthreads))
+        if rc != 0:
+            raise RuntimeError("oracle_attn_rows failed (bad index?)")
+        return o, lse
+
+    def attn_probs(self, q, k, v, causal: bool, scale: float):
+        """(O, LSE, P [B,H,N,N]) for small problems; P is the softmax matrix."""
+        q, k, v = _bits(q), _bits(k), _bits(v)
+        B, H, N, D = q.shape
+        o = np.empty((B, H, N, D), dtype=np.float64)
+        lse = np.empty((B, H, N), dtype=np.float64)
+        p = np.empty((B, H, N, N), dtype=np.float64)
+        rc = self._lib.oracle_attn_probs(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(p),
+                                         B, H, N, D, int(bool(causal)), float(scale))
+        if rc != 0:
+            raise RuntimeError("oracle_attn_probs failed")
+        return o, lse, p
+
+
+def default() -> Oracle:
+    """The oracle built from ``attn_oracle.c`` (compiled on first use)."""
+    global _default
+    with _lock:
+        if _default is None:
+            _default = Oracle(build())
+    return _default
+
+
+def threads(nthreads: int = 0) -> int:
+    return default().threads(nthreads)
+
+
+def attn_fwd(q, k, v, causal: bool, scale: float, nthreads: int = 0):
+    return default().attn_fwd(q, k, v, causal, scale, nthreads)
+
+
+def attn_rows(q, k, v, causal: bool, scale: float, bh_idx, row_idx, nthreads: int = 0):
+    return default().attn_rows(q, k, v, causal, scale, bh_idx, row_idx, nthreads)
+
+
+def attn_probs(q, k, v, causal: bool, scale: float):
+    return default().attn_probs(q, k, v, causal, scale)
