@@ -1,0 +1,420 @@
+"""Benchmark of the GB300 fused attention forward: one JSON line on rank 0.
+
+A step is one attn_fwd call (the whole fused forward: Q/K/V tile loads, QK^T,
+online softmax, PV, epilogue) over one batch of seeded synthetic input.  The
+default workload is the long-sequence throughput shape B=4, H=16, N=4096,
+D=128, non-causal.  Value = algorithmic TFLOP/s (4*B*H*N^2*D, halved when
+causal) measured with CUDA events on the launching stream, inputs resident in
+device memory.  ``e2e`` repeats the measurement through the C ABI with pinned
+host buffers: each step copies Q, K, V in and O, LSE out.
+
+``--impl reference`` times the CPU oracle (plain C, fp64) on the host cores
+instead: each step is a bounded sample of rows of the same workload.
+
+Under torchrun every rank runs its own copy of the workload on its own GPU
+(independent problems, no collective on the data path: weak scaling); rank 0
+prints the line with value = total FLOPs of all ranks / max-over-ranks time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from tiled_attention_forward_fa2_gb300.inputs import WORKLOADS  # noqa: E402
+
+METRIC = "attention fwd TFLOP/s (bf16, 1×GB300) and % of dense BF16 tensor peak"
+DEFAULT_WORKLOAD = "b4h16n4096d128"
+L2_BYTES = 129 * 2**20
+FALLBACK_PEAK_TFLOPS = 1900.0
+KERNEL_SOURCES = ["tiled_attention_forward_fa2_gb300/csrc/attn_fwd_kernel.cuh",
+                  "tiled_attention_forward_fa2_gb300/csrc/sm103_ptx.cuh",
+                  "tiled_attention_forward_fa2_gb300/csrc/attn_fwd.cu"]
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return json.load(f), "measured"
+    return {"bf16_tflops": FALLBACK_PEAK_TFLOPS, "hbm_gbs": 6800.0}, "fallback"
+
+
+def ncu_traffic(workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if taken on this kernel source."""
+    path = os.path.join(ROOT, "profiles", f"attn_fwd_sm103_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m_src = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]{16})", text)
+    m_tr = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    if not m_src or not m_tr or m_src.group(1) != kernel_source_hash():
+        return None
+    return float(m_tr.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi samples (SM clock, throttle reasons) taken while the timed region runs."""
+
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.samples = []
+        self.proc = None
+        self.marks = []
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "50",
+                 "-i", str(device_index)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, ValueError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), line.strip()))
+
+    def mark(self):
+        self.marks.append(time.time())
+
+    def wait_first(self, timeout=5.0):
+        t0 = time.time()
+        while self.proc is not None and not self.samples and time.time() - t0 < timeout:
+            time.sleep(0.02)
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        t0, t1 = (self.marks[0], self.marks[-1]) if len(self.marks) >= 2 else (0, float("inf"))
+        rows = [s for (t, s) in self.samples if t0 <= t <= t1]
+        in_region = len(rows)
+        if not rows:
+            rows = [s for (_, s) in self.samples]
+        sm, smax, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            parts = [x.strip() for x in r.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(power) if power else None, "reasons": sorted(reasons),
+                "samples": in_region, "samples_total": len(self.samples)}
+
+
+def to_dev(bits, device):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(device)
+
+
+def cpu_oracle_rate(w, budget_s: float, rows_cap: int | None = None, seed: int = 0):
+    """Time the CPU oracle on sampled rows of workload ``w`` for about ``budget_s`` seconds.
+
+    Returns (TFLOP/s, seconds, rows, threads).  Row (b, h, i) costs 4*n_i*D FLOPs
+    (n_i visible keys), the same convention as the GPU metric.
+    """
+    import oracle
+
+    q, k, v = w.qkv()
+    rng = np.random.default_rng(seed)
+
+    def sample(n):
+        bh = rng.integers(0, w.B * w.H, n).astype(np.int64)
+        ri = rng.integers(0, w.N, n).astype(np.int64)
+        return bh, ri
+
+    def flops(ri):
+        vis = (ri + 1) if w.causal else np.full(ri.shape, w.N)
+        return float(4.0 * w.D * vis.sum())
+
+    bh, ri = sample(64)
+    t0 = time.perf_counter()
+    oracle.attn_rows(q, k, v, w.causal, w.scale, bh, ri)
+    dt = max(time.perf_counter() - t0, 1e-6)
+    n = max(16, int(64 * budget_s / dt))
+    if rows_cap:
+        n = min(n, rows_cap)
+    bh, ri = sample(n)
+    t0 = time.perf_counter()
+    oracle.attn_rows(q, k, v, w.causal, w.scale, bh, ri)
+    dt = time.perf_counter() - t0
+    return flops(ri) / dt / 1e12, dt, n, oracle.threads()
+
+
+def run_reference(args, w):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+
+    q, k, v = w.qkv()
+    rng = np.random.default_rng(1)
+    # Per step: a fixed sample of rows sized so that warm-up + timed steps take about a minute.
+    bh, ri = rng.integers(0, w.B * w.H, 32).astype(np.int64), rng.integers(0, w.N, 32).astype(np.int64)
+    t0 = time.perf_counter()
+    oracle.attn_rows(q, k, v, w.causal, w.scale, bh, ri)
+    per_row = max((time.perf_counter() - t0) / 32, 1e-7)
+    rows = int(max(8, min(4096, 60.0 / (args.steps + args.warmup) / per_row)))
+    bh = rng.integers(0, w.B * w.H, rows).astype(np.int64)
+    ri = rng.integers(0, w.N, rows).astype(np.int64)
+    vis = (ri + 1) if w.causal else np.full(ri.shape, w.N)
+    step_flops = float(4.0 * w.D * vis.sum())
+    for _ in range(args.warmup):
+        oracle.attn_rows(q, k, v, w.causal, w.scale, bh, ri)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.attn_rows(q, k, v, w.causal, w.scale, bh, ri)
+    dt = time.perf_counter() - t0
+    value = step_flops * args.steps / dt / 1e12
+    sample = f"{rows} sampled query rows (all keys each) of {w.name} per step"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": workload_config(w),
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": oracle.threads(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def workload_config(w, extra=None):
+    cfg = {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "D": w.D, "causal": w.causal, "seed": w.seed,
+           "q_std": w.q_std, "scale": w.scale, "layout": "[B,H,N,D] bf16, D innermost"}
+    if extra:
+        cfg.update(extra)
+    return cfg
+
+
+def run_ours(args, w):
+    import torch
+
+    import tiled_attention_forward_fa2_gb300 as pkg
+
+    world, rank, local = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device (the product path has no CPU fallback)")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+    pkg.library()
+
+    q, k, v = w.qkv()
+    qd, kd, vd = to_dev(q, dev), to_dev(k, dev), to_dev(v, dev)
+    o = torch.empty_like(qd)
+    lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    in_bytes = 3 * q.nbytes
+    flush = in_bytes + o.numel() * 2 < 2 * L2_BYTES
+    scratch = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev) if flush else None
+
+    def step():
+        st = pkg.attn_fwd(qd, kd, vd, o, lse, w.B, w.H, w.N, w.D, w.causal, w.scale, stream)
+        if st != pkg.ATTN_OK:
+            raise RuntimeError(pkg.attn_status_string(st))
+
+    for _ in range(args.warmup):
+        step()
+    st = pkg.attn_last_status(stream)
+    if st != pkg.ATTN_OK:
+        raise RuntimeError(pkg.attn_status_string(st))
+
+    sampler = ClockSampler(local) if rank == 0 else None
+    if sampler:
+        sampler.wait_first()
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize(dev)
+    if sampler:
+        sampler.mark()
+    if flush:
+        # Working set below 2x L2: rewrite a 2x-L2 buffer between steps, time each launch alone.
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        for i in range(args.steps):
+            scratch.fill_(float(i))
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        torch.cuda.synchronize(dev)
+        elapsed_ms = sum(s.elapsed_time(e) for s, e in zip(starts, ends))
+    else:
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        elapsed_ms = e0.elapsed_time(e1)
+    if sampler:
+        sampler.mark()
+    if pg:
+        pg.barrier()
+    st = pkg.attn_last_status(stream)
+    if st != pkg.ATTN_OK:
+        raise RuntimeError(pkg.attn_status_string(st))
+    t = torch.tensor([elapsed_ms], dtype=torch.float64, device=dev)
+    if pg:
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    elapsed_ms = float(t.item())
+    if sampler:
+        sampler.stop()
+
+    flops = pkg.attn_fwd_flops(w.B, w.H, w.N, w.D, w.causal)
+    ms_per_step = elapsed_ms / args.steps
+    value = world * flops / (ms_per_step * 1e-3) / 1e12
+
+    # End to end through the C ABI with pinned host buffers.
+    e2e_steps = max(3, min(args.steps, 50))
+    qh, kh, vh = (torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).pin_memory()
+                  for a in (q, k, v))
+    oh = torch.empty(o.shape, dtype=torch.bfloat16).pin_memory()
+    lh = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
+
+    def e2e_step():
+        qd.copy_(qh, non_blocking=True)
+        kd.copy_(kh, non_blocking=True)
+        vd.copy_(vh, non_blocking=True)
+        step()
+        oh.copy_(o, non_blocking=True)
+        lh.copy_(lse, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize(dev)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
+    if pg:
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    e2e_ms = float(t.item())
+
+    if rank != 0:
+        if pg:
+            pg.destroy_process_group()
+        return
+
+    peaks, peak_src = measured_peaks()
+    peak = float(peaks["bf16_tflops"])
+    achieved = flops / (ms_per_step * 1e-3) / 1e12
+    traffic = ncu_traffic(w.name)
+    cpu = None
+    if not args.no_cpu_baseline:
+        tf, secs, rows, cores = cpu_oracle_rate(w, args.cpu_seconds)
+        cpu = {"value": tf, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+               "sample": f"{rows} random query rows (all visible keys each) of {w.name}, {secs:.1f} s wall"}
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_per_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "pct_of_peak": 100.0 * achieved / peak,
+        "config": workload_config(w, {
+            "l2": ("working set < 2x L2: 2x-L2 buffer rewritten between steps, each launch timed alone"
+                   if flush else f"inputs {in_bytes / 2**20:.0f} MiB > 129 MiB L2, no flush"),
+            "parallelism": f"independent replicas x{world}" if world > 1 else "single GPU"}),
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "peak_source": f"bf16_tflops (burst) of {peak_src}",
+                     "kernel": f"attn_fwd_sm103<{w.D},{str(w.causal).lower()}>"},
+        "cpu_baseline": cpu,
+        "e2e": {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": int(in_bytes), "d2h_bytes_per_step": int(o.numel() * 2 + lse.numel() * 4),
+                "ms_per_step": e2e_ms, "steps": e2e_steps},
+        "gpu_launches": args.steps,
+        "clocks": sampler.summary() if sampler else None,
+        "kernel_source": kernel_source_hash(),
+    }
+    print(json.dumps(line), flush=True)
+    if pg:
+        pg.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU-oracle baseline budget")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    w = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_ours(args, w)
+
+
+if __name__ == "__main__":
+    main()

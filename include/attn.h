@@ -1,0 +1,92 @@
+/*
+ * attn.h -- C ABI of the GB300 (sm_103a) fused attention forward.
+ *
+ * The operation ("[GPU] Deep Learning for HPC", bkkhyunn.github.io
+ * hardware/pytorch_for_HPC, section "Flash Attention"): scores S = Q K^T,
+ * a softmax over each row of S, then O = softmax(S) V, computed as one fused,
+ * tiled kernel so the N x N score matrix never reaches device memory.  The
+ * argument list follows the FlashAttention-2 Triton forward shown on
+ * null-ptr.tistory.com (category "development", the `_fwd_kernel` post):
+ * Q, K, V, Out, Lse, softmax_scale, batch, nheads, IS_CAUSAL.  That kernel's
+ * TMP scratch has no counterpart: the running row statistics stay on chip.
+ *
+ * For every batch b, head h and query row i:
+ *   s_ij   = scale * sum_d Q[b,h,i,d] K[b,h,j,d]       (j <= i when causal)
+ *   O[b,h,i,:] = sum_j softmax_j(s_ij) V[b,h,j,:]
+ *   LSE[b,h,i] = log(sum_j exp(s_ij))                  (natural log)
+ * The softmax is evaluated tile by tile with a running maximum and running
+ * sum (exp2-based on the device); accumulation is fp32, O is rounded once to
+ * bf16 (nearest even), LSE is fp32.
+ *
+ * All entry points are host functions.  They allocate no device memory per
+ * call, never synchronise the device except attn_last_status, and are safe
+ * to call from several host threads.
+ */
+#ifndef ATTN_FWD_GB300_ATTN_H
+#define ATTN_FWD_GB300_ATTN_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  ATTN_OK = 0,
+  ATTN_ERR_INVALID_ARG = 1, /* null/misaligned/overlapping pointer, bad size or scale */
+  ATTN_ERR_UNSUPPORTED = 2, /* valid request this build does not implement (head dim, device) */
+  ATTN_ERR_CUDA = 3,        /* a CUDA runtime or driver call failed (launch, tensor map, ...) */
+  ATTN_ERR_TIMEOUT = 4      /* a kernel pipeline wait exceeded its bound and the kernel gave up */
+} attn_status_t;
+
+/*
+ * attn_fwd -- enqueue the fused forward on `stream` and return.
+ *
+ * q, k, v : device pointers, bf16, [B, H, N, D] contiguous row-major (D
+ *           innermost), 16-byte aligned.  Read only.
+ * o       : device pointer, bf16, [B, H, N, D] contiguous, 16-byte aligned.
+ *           Written.  Must not overlap q, k, v or lse.
+ * lse     : device pointer, fp32, [B, H, N] contiguous, 4-byte aligned.
+ *           Written.  Must not overlap q, k, v or o.
+ * B, H, N : batch, heads, sequence length (queries = keys = N).  Any N >= 1
+ *           (a ragged last tile is masked).  B, H or N equal to 0 is an empty
+ *           problem: ATTN_OK, nothing launched.
+ * D       : head dimension, 64 or 128 (others: ATTN_ERR_UNSUPPORTED).
+ * causal  : nonzero -> key j is visible to query i only when j <= i.
+ * scale   : softmax scale applied to the logits, finite and > 0 (usually
+ *           1/sqrt(D)).
+ * stream  : a cudaStream_t (0 = legacy default stream).
+ *
+ * The caller owns every buffer.  Argument errors return synchronously with
+ * nothing launched: ATTN_ERR_INVALID_ARG, or ATTN_ERR_UNSUPPORTED for a head
+ * dimension other than 64/128 or a device that is not sm_103.  A failed
+ * launch returns ATTN_ERR_CUDA.  A kernel that hits a pipeline timeout does
+ * not trap: it records ATTN_ERR_TIMEOUT in a device status word that
+ * attn_last_status reports; its outputs are then unspecified.
+ */
+attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                       int64_t B, int64_t H, int64_t N, int64_t D, int causal, float scale,
+                       void* stream);
+
+/*
+ * attn_last_status -- synchronise `stream`, then report and clear the device
+ * status word of the current device: ATTN_OK, or ATTN_ERR_TIMEOUT if a kernel
+ * gave up on a pipeline wait since the last call; ATTN_ERR_CUDA if the
+ * synchronisation itself failed.
+ */
+attn_status_t attn_last_status(void* stream);
+
+/* attn_status_string -- static, human-readable name of a status code. */
+const char* attn_status_string(attn_status_t status);
+
+/*
+ * attn_fwd_flops -- algorithmic FLOPs of one attn_fwd call:
+ * 4 * B * H * N^2 * D, halved when causal (exp and softmax not counted).
+ */
+double attn_fwd_flops(int64_t B, int64_t H, int64_t N, int64_t D, int causal);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_FWD_GB300_ATTN_H */

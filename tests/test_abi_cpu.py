@@ -1,0 +1,92 @@
+"""The C-ABI library loads and validates arguments without a GPU (no compute calls)."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+import tiled_attention_forward_fa2_gb300 as pkg
+from tiled_attention_forward_fa2_gb300 import build as cuda_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+A16 = 0x10000  # fake, 16-byte aligned addresses: every call below returns before touching them
+MB = 1 << 20
+
+
+@pytest.fixture(scope="module")
+def lib():
+    cuda_build.build()
+    return pkg.library()
+
+
+def declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
+        names |= set(re.findall(r"\b(attn_[a-z0-9_]+)\s*\(", text))
+    return sorted(names)
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert {"attn_fwd", "attn_last_status", "attn_status_string"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in include/ but not exported"
+
+
+def call(q=A16, k=A16 + 64 * MB, v=A16 + 128 * MB, o=A16 + 192 * MB, lse=A16 + 256 * MB,
+         B=1, H=2, N=256, D=64, causal=0, scale=0.125):
+    return pkg.attn_fwd(q, k, v, o, lse, B, H, N, D, causal, scale, None)
+
+
+def test_null_pointers(lib):
+    for kw in ("q", "k", "v", "o", "lse"):
+        assert call(**{kw: None}) == pkg.ATTN_ERR_INVALID_ARG
+
+
+def test_bad_sizes_and_scale(lib):
+    assert call(B=-1) == pkg.ATTN_ERR_INVALID_ARG
+    assert call(N=-5) == pkg.ATTN_ERR_INVALID_ARG
+    assert call(D=0) == pkg.ATTN_ERR_INVALID_ARG
+    for s in (0.0, -0.125, float("inf"), float("nan")):
+        assert call(scale=s) == pkg.ATTN_ERR_INVALID_ARG
+    assert call(N=2**31) == pkg.ATTN_ERR_INVALID_ARG
+    assert call(B=2**20, H=2**20) == pkg.ATTN_ERR_INVALID_ARG
+
+
+def test_unsupported_head_dims(lib):
+    for d in (16, 32, 96, 256):
+        assert call(D=d) == pkg.ATTN_ERR_UNSUPPORTED
+
+
+def test_empty_problem_is_a_no_op(lib):
+    for kw in ({"B": 0}, {"H": 0}, {"N": 0}):
+        assert call(**kw) == pkg.ATTN_OK
+
+
+def test_misaligned_pointers(lib):
+    assert call(q=A16 + 8) == pkg.ATTN_ERR_INVALID_ARG
+    assert call(o=A16 + 192 * MB + 2) == pkg.ATTN_ERR_INVALID_ARG
+    assert call(lse=A16 + 256 * MB + 2) == pkg.ATTN_ERR_INVALID_ARG
+
+
+def test_overlapping_outputs(lib):
+    assert call(o=A16) == pkg.ATTN_ERR_INVALID_ARG               # o over q
+    assert call(o=A16 + 64 * MB + 4096) == pkg.ATTN_ERR_INVALID_ARG  # o inside k
+    assert call(lse=A16 + 128 * MB + 16) == pkg.ATTN_ERR_INVALID_ARG  # lse inside v
+    assert call(lse=A16 + 192 * MB + 64) == pkg.ATTN_ERR_INVALID_ARG  # lse inside o
+
+
+def test_status_strings_and_flops(lib):
+    assert pkg.attn_status_string(pkg.ATTN_ERR_TIMEOUT) == "ATTN_ERR_TIMEOUT"
+    assert pkg.attn_status_string(99) == "ATTN_ERR_UNKNOWN"
+    assert pkg.attn_fwd_flops(4, 16, 4096, 128, False) == 4.0 * 4 * 16 * 4096 ** 2 * 128
+    assert pkg.attn_fwd_flops(1, 16, 16384, 128, True) == 2.0 * 16 * 16384 ** 2 * 128
+
+
+def test_no_gpu_means_cuda_error_not_a_crash(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert call() == pkg.ATTN_ERR_CUDA

@@ -1,0 +1,189 @@
+"""CUDA path against the CPU oracle, element by element, through the C ABI."""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+import tiled_attention_forward_fa2_gb300 as pkg
+from parity import assert_close, o_to_f64, to_dev
+from tiled_attention_forward_fa2_gb300.inputs import WORKLOADS, f64_to_bf16_bits, make_qkv
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    pkg.library()
+
+
+def run(q, k, v, causal, scale, poison=True):
+    """Call the C ABI on fresh device copies; outputs are poisoned first so an unwritten element shows."""
+    B, H, N, D = q.shape
+    qd, kd, vd = to_dev(q), to_dev(k), to_dev(v)
+    o = torch.full_like(qd, float("nan")) if poison else torch.empty_like(qd)
+    lse = torch.full((B, H, N), float("nan"), dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream()
+    st = pkg.attn_fwd(qd, kd, vd, o, lse, B, H, N, D, causal, scale, stream)
+    assert st == pkg.ATTN_OK, pkg.attn_status_string(st)
+    st = pkg.attn_last_status(stream)
+    assert st == pkg.ATTN_OK, pkg.attn_status_string(st)
+    return o_to_f64(o), lse.cpu().numpy().astype(np.float64)
+
+
+def full_check(q, k, v, causal, scale, what):
+    o, lse = run(q, k, v, causal, scale)
+    o_ref, lse_ref = oracle.attn_fwd(q, k, v, causal, scale)
+    return assert_close(o, lse, o_ref, lse_ref, what)
+
+
+SMALL = ["b1h1n256d64", "b2h8n1024d64", "b2h8n1024d64_causal", "b16h32n512d64_causal"]
+
+
+@pytest.mark.parametrize("name", SMALL)
+def test_workload_full(name):
+    w = WORKLOADS[name]
+    q, k, v = w.qkv()
+    full_check(q, k, v, w.causal, w.scale, name)
+
+
+def sampled_rows(BH, N, n_random, seed):
+    rng = np.random.default_rng(seed)
+    bh = [rng.integers(0, BH, n_random)]
+    ri = [rng.integers(0, N, n_random)]
+    for h in (0, BH - 1):  # whole first and last query tiles of two heads, and the last rows
+        for r0 in (0, N - 128):
+            bh.append(np.full(128, h))
+            ri.append(np.arange(r0, r0 + 128))
+    return np.concatenate(bh).astype(np.int64), np.concatenate(ri).astype(np.int64)
+
+
+@pytest.mark.parametrize("name", ["b4h16n4096d128", "b1h16n16384d128_causal_q4"])
+def test_workload_sampled(name):
+    """Full-size problems in the bench's launch configuration; the oracle checks sampled rows."""
+    w = WORKLOADS[name]
+    q, k, v = w.qkv()
+    o, lse = run(q, k, v, w.causal, w.scale)
+    assert np.all(np.isfinite(o)) and np.all(np.isfinite(lse)), "unwritten or non-finite output"
+    bh, ri = sampled_rows(w.B * w.H, w.N, 1024, w.seed)
+    o_ref, lse_ref = oracle.attn_rows(q, k, v, w.causal, w.scale, bh, ri)
+    of = o.reshape(w.B * w.H, w.N, w.D)[bh, ri]
+    lf = lse.reshape(w.B * w.H, w.N)[bh, ri]
+    assert_close(of, lf, o_ref, lse_ref, name)
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("N", [1, 2, 17, 127, 128, 129, 200, 383, 640])
+def test_ragged_and_tiny_lengths(N, D, causal):
+    q, k, v = make_qkv(2, 3, N, D, seed=500 + N + D)
+    full_check(q, k, v, causal, 1.0 / math.sqrt(D), f"N={N} D={D} causal={causal}")
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_large_logits_stress_rescaling(D):
+    # Q spread 8x: logits up to ~40 in magnitude; the running max moves often.
+    q, k, v = make_qkv(1, 4, 1000, D, seed=77, q_std=8.0)
+    for causal in (False, True):
+        full_check(q, k, v, causal, 1.0 / math.sqrt(D), f"q_std=8 D={D} causal={causal}")
+
+
+def test_identical_keys_give_mean_of_v():
+    B, H, N, D = 1, 2, 300, 128
+    q, k, v = make_qkv(B, H, N, D, seed=78)
+    k = np.broadcast_to(k[:, :, :1], k.shape).copy()
+    full_check(q, k, v, True, 0.1, "identical keys")
+
+
+def test_zero_queries_and_one_hot():
+    B, H, N, D = 1, 1, 256, 64
+    _, k, v = make_qkv(B, H, N, D, seed=79)
+    full_check(np.zeros_like(k), k, v, False, 0.125, "Q = 0")
+    sixteen = f64_to_bf16_bits(np.array([16.0]))[0]
+    q = np.zeros_like(k)
+    q[..., 0] = sixteen
+    k1 = np.zeros_like(k)
+    k1[0, 0, 100, 0] = sixteen
+    full_check(q, k1, v, False, 0.125, "one-hot logit")
+    full_check(q, k1, v, True, 0.125, "one-hot logit, causal")
+
+
+def test_scale_variants():
+    q, k, v = make_qkv(1, 2, 384, 64, seed=80)
+    for scale in (1e-3, 0.05, 0.5):
+        full_check(q, k, v, False, scale, f"scale={scale}")
+
+
+def test_deterministic():
+    q, k, v = make_qkv(2, 4, 1024, 128, seed=81)
+    o1, l1 = run(q, k, v, True, 0.088)
+    o2, l2 = run(q, k, v, True, 0.088)
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+
+
+def test_many_heads_beyond_int32_offsets():
+    # 270000 (batch, head) slices of one 128-row tile: a grid of 270000 CTAs and
+    # 2.2e9 elements per tensor, so element offsets pass 2^31.  The inputs are 16
+    # seeded heads repeated on the device; the oracle checks sampled rows.
+    H0, reps, N, D = 16, 16875, 128, 64
+    q0, k0, v0 = make_qkv(1, H0, N, D, seed=82)
+    BH = H0 * reps
+    big = lambda a: to_dev(a).expand(reps, H0, N, D).reshape(1, BH, N, D).contiguous()  # noqa: E731
+    qd, kd, vd = big(q0), big(k0), big(v0)
+    o = torch.full_like(qd, float("nan"))
+    lse = torch.full((1, BH, N), float("nan"), device="cuda")
+    s = torch.cuda.current_stream()
+    assert pkg.attn_fwd(qd, kd, vd, o, lse, 1, BH, N, D, True, 0.125, s) == pkg.ATTN_OK
+    assert pkg.attn_last_status(s) == pkg.ATTN_OK
+    rng = np.random.default_rng(82)
+    bh = np.concatenate([rng.integers(0, BH, 2048), np.full(128, BH - 1)]).astype(np.int64)
+    ri = np.concatenate([rng.integers(0, N, 2048), np.arange(128)]).astype(np.int64)
+    idx_bh = torch.from_numpy(bh).cuda()
+    idx_r = torch.from_numpy(ri).cuda()
+    of = o.view(BH, N, D)[idx_bh, idx_r].float().cpu().numpy().astype(np.float64)
+    lf = lse.view(BH, N)[idx_bh, idx_r].cpu().numpy().astype(np.float64)
+    o_ref, lse_ref = oracle.attn_rows(q0, k0, v0, True, 0.125, bh % H0, ri)
+    assert_close(of, lf, o_ref, lse_ref, "270000 heads")
+    del qd, kd, vd, o, lse
+    torch.cuda.empty_cache()
+
+
+def test_long_sequence():
+    B, H, N, D = 1, 1, 32768 + 77, 128
+    q, k, v = make_qkv(B, H, N, D, seed=83)
+    o, lse = run(q, k, v, True, 1.0 / math.sqrt(D))
+    bh, ri = sampled_rows(1, N, 256, 83)
+    o_ref, lse_ref = oracle.attn_rows(q, k, v, True, 1.0 / math.sqrt(D), bh, ri)
+    assert_close(o.reshape(N, D)[ri], lse.reshape(N)[ri], o_ref, lse_ref, "N=32845 causal")
+
+
+def test_empty_problem_leaves_outputs_untouched():
+    o = torch.full((0, 2, 128, 64), 1.0, dtype=torch.bfloat16, device="cuda")
+    q = torch.zeros_like(o)
+    lse = torch.zeros((0, 2, 128), device="cuda")
+    assert pkg.attn_fwd(q, q, q, o, lse, 0, 2, 128, 64, False, 0.125, None) == pkg.ATTN_OK
+
+
+def test_boundary_errors_with_real_buffers():
+    q = torch.zeros((1, 1, 256, 64), dtype=torch.bfloat16, device="cuda")
+    o = torch.empty_like(q)
+    lse = torch.empty((1, 1, 256), device="cuda")
+    s = torch.cuda.current_stream()
+    assert pkg.attn_fwd(q.data_ptr() + 2, q, q, o, lse, 1, 1, 255, 64, False, 0.125, s) == pkg.ATTN_ERR_INVALID_ARG
+    assert pkg.attn_fwd(q, q, q, q, lse, 1, 1, 256, 64, False, 0.125, s) == pkg.ATTN_ERR_INVALID_ARG
+    assert pkg.attn_fwd(q, q, q, o, lse, 1, 1, 256, 96, False, 0.125, s) == pkg.ATTN_ERR_UNSUPPORTED
+    assert pkg.attn_last_status(s) == pkg.ATTN_OK
+
+
+def test_side_stream_and_fwd_wrapper():
+    q, k, v = make_qkv(1, 2, 512, 128, seed=84)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        o, lse = pkg.fwd(to_dev(q), to_dev(k), to_dev(v), causal=True)
+    s.synchronize()
+    o_ref, lse_ref = oracle.attn_fwd(q, k, v, True, 1.0 / math.sqrt(128))
+    assert_close(o_to_f64(o), lse.cpu().numpy().astype(np.float64), o_ref, lse_ref, "side stream")

@@ -1,0 +1,57 @@
+"""GB300 (sm_103a) fused attention forward: O = softmax(scale * Q K^T [+causal]) V and LSE.
+
+``attn_fwd`` and friends are the C ABI of include/attn.h under the same names;
+``fwd`` is the convenience call on torch tensors.  PyTorch only provides device
+memory and the stream; the arithmetic runs in the package's CUDA library.
+"""
+from __future__ import annotations
+
+import math
+
+from ._binding import (  # noqa: F401
+    ATTN_ERR_CUDA,
+    ATTN_ERR_INVALID_ARG,
+    ATTN_ERR_TIMEOUT,
+    ATTN_ERR_UNSUPPORTED,
+    ATTN_OK,
+    attn_fwd,
+    attn_fwd_flops,
+    attn_last_status,
+    attn_status_string,
+    library,
+)
+
+
+class AttnError(RuntimeError):
+    def __init__(self, status: int):
+        super().__init__(attn_status_string(status))
+        self.status = status
+
+
+def fwd(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None, stream=None):
+    """Fused forward on bf16 CUDA tensors [B, H, N, D] (contiguous).
+
+    Returns ``(o, lse)``: o bf16 [B, H, N, D], lse fp32 [B, H, N].  ``scale``
+    defaults to 1/sqrt(D).  Runs on ``stream`` (default: torch's current
+    stream) without synchronising.
+    """
+    import torch
+
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if t.dtype != torch.bfloat16 or not t.is_cuda or t.dim() != 4 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous bf16 CUDA tensor [B, H, N, D]")
+    if not (q.shape == k.shape == v.shape):
+        raise ValueError("q, k and v must have one shape")
+    B, H, N, D = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    st = attn_fwd(q, k, v, out, lse, B, H, N, D, causal, scale, stream)
+    if st != ATTN_OK:
+        raise AttnError(st)
+    return out, lse

@@ -1,0 +1,71 @@
+"""ctypes binding of the C ABI in include/attn.h -- argument marshalling only.
+
+Every step of the forward runs in the CUDA library; if the library is missing
+this module raises instead of computing anything another way.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from .build import LIB
+
+ATTN_OK = 0
+ATTN_ERR_INVALID_ARG = 1
+ATTN_ERR_UNSUPPORTED = 2
+ATTN_ERR_CUDA = 3
+ATTN_ERR_TIMEOUT = 4
+
+_lock = threading.Lock()
+_lib = None
+
+
+def library() -> ctypes.CDLL:
+    """The loaded CUDA library (built by ``build()``); raises if it is missing."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB):
+                raise RuntimeError(f"CUDA library not built: {LIB} is missing (run __graft_entry__.build())")
+            lib = ctypes.CDLL(LIB)
+            P, I64 = ctypes.c_void_p, ctypes.c_int64
+            lib.attn_fwd.argtypes = [P, P, P, P, P, I64, I64, I64, I64, ctypes.c_int, ctypes.c_float, P]
+            lib.attn_fwd.restype = ctypes.c_int
+            lib.attn_last_status.argtypes = [P]
+            lib.attn_last_status.restype = ctypes.c_int
+            lib.attn_status_string.argtypes = [ctypes.c_int]
+            lib.attn_status_string.restype = ctypes.c_char_p
+            lib.attn_fwd_flops.argtypes = [I64, I64, I64, I64, ctypes.c_int]
+            lib.attn_fwd_flops.restype = ctypes.c_double
+            _lib = lib
+    return _lib
+
+
+def _addr(x) -> int | None:
+    """A device/host address from a torch tensor, an int or None."""
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def attn_fwd(q, k, v, o, lse, B: int, H: int, N: int, D: int, causal: bool, scale: float, stream) -> int:
+    """Call ``attn_fwd``; tensors or raw addresses; ``stream`` a handle int or a torch stream."""
+    s = stream if (stream is None or isinstance(stream, int)) else stream.cuda_stream
+    return library().attn_fwd(_addr(q), _addr(k), _addr(v), _addr(o), _addr(lse), int(B), int(H), int(N),
+                              int(D), int(bool(causal)), float(scale), s)
+
+
+def attn_last_status(stream) -> int:
+    s = stream if (stream is None or isinstance(stream, int)) else stream.cuda_stream
+    return library().attn_last_status(s)
+
+
+def attn_status_string(status: int) -> str:
+    return library().attn_status_string(int(status)).decode()
+
+
+def attn_fwd_flops(B: int, H: int, N: int, D: int, causal: bool) -> float:
+    return library().attn_fwd_flops(int(B), int(H), int(N), int(D), int(bool(causal)))

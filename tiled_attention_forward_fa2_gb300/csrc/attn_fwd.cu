@@ -1,0 +1,193 @@
+// Host side of the C ABI declared in include/attn.h: argument validation,
+// TMA tensor maps, grid shape and launch of the sm_103a kernels, and the
+// device status word.  Nothing here allocates device memory.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cstdlib>
+#include <mutex>
+
+#include "attn.h"
+#include "attn_fwd_kernel.cuh"
+
+namespace {
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point, so the
+// library does not link libcuda directly and loads on machines without a GPU.
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+  });
+  return fn;
+}
+
+// [B*H, N, D] bf16 viewed as a 3-D tensor {D, N, B*H}; boxes of 64 x 128 x 1
+// (64 bf16 = one 128-byte swizzle span); rows past N read as zero.
+bool encode_qkv_map(EncodeTiledFn enc, CUtensorMap* map, const void* ptr, int64_t D, int64_t N, int64_t BH) {
+  const cuuint64_t dims[3] = {cuuint64_t(D), cuuint64_t(N), cuuint64_t(BH)};
+  const cuuint64_t strides[2] = {cuuint64_t(D) * 2u, cuuint64_t(N) * cuuint64_t(D) * 2u};
+  const cuuint32_t box[3] = {64u, 128u, 1u};
+  const cuuint32_t estride[3] = {1u, 1u, 1u};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estride,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Per-device one-time state: architecture check and the shared-memory opt-in
+// of every kernel instance.  0 = not yet, 1 = ready, 2 = unsupported, 3 = error.
+constexpr int kMaxDevices = 64;
+std::atomic<int> g_dev_state[kMaxDevices];
+std::mutex g_dev_mutex;
+
+template <int D, bool CAUSAL>
+cudaError_t opt_in_smem() {
+  return cudaFuncSetAttribute(attn::attn_fwd_sm103<D, CAUSAL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              int(attn::Cfg<D>::SMEM));
+}
+
+attn_status_t prepare_device(int dev) {
+  if (dev < 0 || dev >= kMaxDevices) return ATTN_ERR_UNSUPPORTED;
+  int st = g_dev_state[dev].load(std::memory_order_acquire);
+  if (st == 0) {
+    std::lock_guard<std::mutex> lock(g_dev_mutex);
+    st = g_dev_state[dev].load(std::memory_order_relaxed);
+    if (st == 0) {
+      int major = 0, minor = 0;
+      if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+          cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
+        st = 3;
+      } else if (major != 10 || minor != 3) {
+        st = 2;
+      } else if (opt_in_smem<64, false>() != cudaSuccess || opt_in_smem<64, true>() != cudaSuccess ||
+                 opt_in_smem<128, false>() != cudaSuccess || opt_in_smem<128, true>() != cudaSuccess) {
+        st = 3;
+      } else {
+        st = 1;
+      }
+      if (st != 3) g_dev_state[dev].store(st, std::memory_order_release);
+    }
+  }
+  if (st == 1) return ATTN_OK;
+  return st == 2 ? ATTN_ERR_UNSUPPORTED : ATTN_ERR_CUDA;
+}
+
+bool ranges_overlap(const void* a, uint64_t na, const void* b, uint64_t nb) {
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return x < y + nb && y < x + na;
+}
+
+long long timeout_cycles() {
+  // About two seconds at the GB300 clock; no legitimate wait comes near it.
+  static const long long v = [] {
+    const char* e = std::getenv("ATTN_WAIT_LIMIT_CYCLES");
+    const long long x = e ? std::atoll(e) : 0;
+    return x > 0 ? x : (1LL << 32);
+  }();
+  return v;
+}
+
+template <int D, bool CAUSAL>
+cudaError_t launch(const attn::FwdParams& prm, int64_t ctas, cudaStream_t stream) {
+  attn::attn_fwd_sm103<D, CAUSAL><<<dim3(unsigned(ctas)), dim3(attn::kThreads), attn::Cfg<D>::SMEM, stream>>>(prm);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+extern "C" {
+
+attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int64_t B, int64_t H,
+                       int64_t N, int64_t D, int causal, float scale, void* stream) {
+  if (!q || !k || !v || !o || !lse) return ATTN_ERR_INVALID_ARG;
+  if (B < 0 || H < 0 || N < 0 || D <= 0) return ATTN_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
+  if (B == 0 || H == 0 || N == 0) return ATTN_OK;
+  constexpr int64_t kI32 = 2147483647;
+  if (B > kI32 || H > kI32 || B * H > kI32 || N > kI32 - 256) return ATTN_ERR_INVALID_ARG;
+  const int64_t BH = B * H;
+  const int64_t n_tiles = (N + attn::BM - 1) / attn::BM;
+  if (BH > kI32 / n_tiles) return ATTN_ERR_INVALID_ARG;            // grid size
+  if (BH > (int64_t(1) << 62) / (N * D * 2)) return ATTN_ERR_INVALID_ARG;  // byte sizes
+  const uint64_t tensor_bytes = uint64_t(BH) * uint64_t(N) * uint64_t(D) * 2u;
+  const uint64_t lse_bytes = uint64_t(BH) * uint64_t(N) * 4u;
+  const auto mis16 = [](const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) != 0; };
+  if (mis16(q) || mis16(k) || mis16(v) || mis16(o) || (reinterpret_cast<uintptr_t>(lse) & 3u) != 0)
+    return ATTN_ERR_INVALID_ARG;
+  if (ranges_overlap(o, tensor_bytes, q, tensor_bytes) || ranges_overlap(o, tensor_bytes, k, tensor_bytes) ||
+      ranges_overlap(o, tensor_bytes, v, tensor_bytes) || ranges_overlap(o, tensor_bytes, lse, lse_bytes) ||
+      ranges_overlap(lse, lse_bytes, q, tensor_bytes) || ranges_overlap(lse, lse_bytes, k, tensor_bytes) ||
+      ranges_overlap(lse, lse_bytes, v, tensor_bytes))
+    return ATTN_ERR_INVALID_ARG;
+
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_CUDA;
+  const attn_status_t ready = prepare_device(dev);
+  if (ready != ATTN_OK) return ready;
+  const EncodeTiledFn enc = encode_fn();
+  if (!enc) return ATTN_ERR_CUDA;
+
+  attn::FwdParams prm{};
+  if (!encode_qkv_map(enc, &prm.tq, q, D, N, BH) || !encode_qkv_map(enc, &prm.tk, k, D, N, BH) ||
+      !encode_qkv_map(enc, &prm.tv, v, D, N, BH))
+    return ATTN_ERR_CUDA;
+  prm.o = static_cast<__nv_bfloat16*>(o);
+  prm.lse = lse;
+  prm.N = int(N);
+  prm.bh = int(BH);
+  prm.n_tiles = int(n_tiles);
+  prm.scale_log2 = scale * 1.4426950408889634f;
+  prm.timeout_cycles = timeout_cycles();
+
+  const int64_t ctas = n_tiles * BH;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t err;
+  if (D == 64)
+    err = causal ? launch<64, true>(prm, ctas, st) : launch<64, false>(prm, ctas, st);
+  else
+    err = causal ? launch<128, true>(prm, ctas, st) : launch<128, false>(prm, ctas, st);
+  return err == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+attn_status_t attn_last_status(void* stream) {
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return ATTN_ERR_CUDA;
+  int word = 0;
+  if (cudaMemcpyFromSymbol(&word, attn::g_attn_status, sizeof(int)) != cudaSuccess) return ATTN_ERR_CUDA;
+  if (word != 0) {
+    const int zero = 0;
+    if (cudaMemcpyToSymbol(attn::g_attn_status, &zero, sizeof(int)) != cudaSuccess) return ATTN_ERR_CUDA;
+  }
+  return word == 0 ? ATTN_OK : ATTN_ERR_TIMEOUT;
+}
+
+const char* attn_status_string(attn_status_t status) {
+  switch (status) {
+    case ATTN_OK: return "ATTN_OK";
+    case ATTN_ERR_INVALID_ARG: return "ATTN_ERR_INVALID_ARG";
+    case ATTN_ERR_UNSUPPORTED: return "ATTN_ERR_UNSUPPORTED";
+    case ATTN_ERR_CUDA: return "ATTN_ERR_CUDA";
+    case ATTN_ERR_TIMEOUT: return "ATTN_ERR_TIMEOUT";
+  }
+  return "ATTN_ERR_UNKNOWN";
+}
+
+double attn_fwd_flops(int64_t B, int64_t H, int64_t N, int64_t D, int causal) {
+  const double f = 4.0 * double(B) * double(H) * double(N) * double(N) * double(D);
+  return causal ? 0.5 * f : f;
+}
+
+}  // extern "C"
