@@ -236,7 +236,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_sm103(const __grid_const
     const uint32_t tO = tmem + lane_off + kTmemO;
     const float sl2 = p.scale_log2;
     float m_run = -INFINITY;  // running max of scale*log2(e)*s
-    float l_run = 0.f;        // running sum of the bf16-rounded p
+    float l_run = 0.f;        // running sum of p (fp32, before the bf16 rounding of P)
     bool ok = true;
     for (int j = 0; j < nk; ++j) {
       const int b = j & 1;
@@ -281,11 +281,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_sm103(const __grid_const
           const float p1 = sm103::ex2_approx(fmaf(s[q * 32 + 2 * e + 1], sl2, neg_m));
           pk[e] = sm103::pack_bf16x2(p0, p1);
           if (e & 1) {
-            sum2 += sm103::bf16lo_to_f32(pk[e]);
-            sum3 += sm103::bf16hi_to_f32(pk[e]);
+            sum2 += p0;
+            sum3 += p1;
           } else {
-            sum0 += sm103::bf16lo_to_f32(pk[e]);
-            sum1 += sm103::bf16hi_to_f32(pk[e]);
+            sum0 += p0;
+            sum1 += p1;
           }
         }
         sm103::tmem_st16(tS + q * 16, pk);  // P over the first 64 columns of this S buffer
