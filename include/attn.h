@@ -50,7 +50,8 @@ typedef enum {
  *           Written.  Must not overlap q, k, v or o.
  * B, H, N : batch, heads, sequence length (queries = keys = N).  Any N >= 1
  *           (a ragged last tile is masked).  B, H or N equal to 0 is an empty
- *           problem: ATTN_OK, nothing launched.
+ *           problem: ATTN_OK, nothing launched, and the pointers (which may
+ *           then be null) are not examined.
  * D       : head dimension, 64 or 128 (others: ATTN_ERR_UNSUPPORTED).
  * causal  : nonzero -> key j is visible to query i only when j <= i.
  * scale   : softmax scale applied to the logits, finite and > 0 (usually

@@ -63,6 +63,9 @@ def test_unsupported_head_dims(lib):
 def test_empty_problem_is_a_no_op(lib):
     for kw in ({"B": 0}, {"H": 0}, {"N": 0}):
         assert call(**kw) == pkg.ATTN_OK
+        assert call(q=None, k=None, v=None, o=None, lse=None, **kw) == pkg.ATTN_OK
+    assert call(B=0, D=96) == pkg.ATTN_ERR_UNSUPPORTED
+    assert call(B=0, scale=-1.0) == pkg.ATTN_ERR_INVALID_ARG
 
 
 def test_misaligned_pointers(lib):

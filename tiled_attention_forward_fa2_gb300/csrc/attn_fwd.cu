@@ -112,11 +112,11 @@ extern "C" {
 
 attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int64_t B, int64_t H,
                        int64_t N, int64_t D, int causal, float scale, void* stream) {
-  if (!q || !k || !v || !o || !lse) return ATTN_ERR_INVALID_ARG;
   if (B < 0 || H < 0 || N < 0 || D <= 0) return ATTN_ERR_INVALID_ARG;
   if (!(scale > 0.f) || !std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
   if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
-  if (B == 0 || H == 0 || N == 0) return ATTN_OK;
+  if (B == 0 || H == 0 || N == 0) return ATTN_OK;  // nothing is read or written
+  if (!q || !k || !v || !o || !lse) return ATTN_ERR_INVALID_ARG;
   constexpr int64_t kI32 = 2147483647;
   if (B > kI32 || H > kI32 || B * H > kI32 || N > kI32 - 256) return ATTN_ERR_INVALID_ARG;
   const int64_t BH = B * H;
