@@ -47,10 +47,11 @@ bool encode_qkv_map(EncodeTiledFn enc, CUtensorMap* map, const void* ptr, int64_
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Per-device one-time state: architecture check and the shared-memory opt-in
-// of every kernel instance.  0 = not yet, 1 = ready, 2 = unsupported, 3 = error.
+// Per-device one-time state: architecture check, SM count and the shared-memory
+// opt-in of every kernel instance.  0 = not yet, 1 = ready, 2 = unsupported, 3 = error.
 constexpr int kMaxDevices = 64;
 std::atomic<int> g_dev_state[kMaxDevices];
+int g_dev_sms[kMaxDevices];
 std::mutex g_dev_mutex;
 
 template <int D, bool CAUSAL>
@@ -68,7 +69,8 @@ attn_status_t prepare_device(int dev) {
     if (st == 0) {
       int major = 0, minor = 0;
       if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-          cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
+          cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+          cudaDeviceGetAttribute(&g_dev_sms[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
         st = 3;
       } else if (major != 10 || minor != 3) {
         st = 2;
@@ -143,17 +145,23 @@ attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, flo
 
   attn::FwdParams prm{};
   if (!encode_qkv_map(enc, &prm.tq, q, D, N, BH) || !encode_qkv_map(enc, &prm.tk, k, D, N, BH) ||
-      !encode_qkv_map(enc, &prm.tv, v, D, N, BH))
+      !encode_qkv_map(enc, &prm.tv, v, D, N, BH) || !encode_qkv_map(enc, &prm.to, o, D, N, BH))
     return ATTN_ERR_CUDA;
-  prm.o = static_cast<__nv_bfloat16*>(o);
+  // Two query tiles per CTA share every K/V tile and let two softmax warpgroups
+  // take turns on the tensor core; use them whenever that still leaves at least
+  // two CTAs per SM to schedule, otherwise one tile per CTA for more parallelism.
+  const int64_t pairs = (n_tiles + 1) / 2;
+  const int T = pairs * BH >= 2 * int64_t(g_dev_sms[dev]) ? 2 : 1;
   prm.lse = lse;
   prm.N = int(N);
   prm.bh = int(BH);
   prm.n_tiles = int(n_tiles);
+  prm.tiles_per_cta = T;
+  prm.n_units = int((n_tiles + T - 1) / T);
   prm.scale_log2 = scale * 1.4426950408889634f;
   prm.timeout_cycles = timeout_cycles();
 
-  const int64_t ctas = n_tiles * BH;
+  const int64_t ctas = int64_t(prm.n_units) * BH;
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t err;
   if (D == 64)

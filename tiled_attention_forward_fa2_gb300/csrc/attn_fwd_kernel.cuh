@@ -1,4 +1,4 @@
-// Fused attention forward for sm_103a (GB300): one CTA per 128-row query tile.
+// Fused attention forward for sm_103a (GB300).
 //
 // What it computes ("[GPU] Deep Learning for HPC", bkkhyunn.github.io, section
 // "Flash Attention"): S = Q K^T, a row softmax, O = softmax(S) V, tiled so the
@@ -8,21 +8,28 @@
 // safe-softmax step (subtract the row max before exp) follows the softmax post
 // on the same site ("Original softmax").
 //
-// Hardware mapping (the pages' H100 design is prior art: "GPUの爆発的な性能向上",
-// ja.news.hada.io topic 14783, sections "WGMMA", "Shared memoryとbank conflict",
-// "アドレス生成とTMA"):
-//   warp 4   : TMA producer.  Q tile once, then K_j and V_j into NS-deep rings of
-//              128-byte-swizzled shared-memory tiles, completion on mbarriers.
-//   warp 5   : allocates 512 TMEM columns, then one thread issues tcgen05.mma:
-//              S_j = Q K_j^T into one of two TMEM score buffers, and
-//              O += P_j V_j with P_j read from TMEM (bf16, written over S_j).
-//              It issues S_{j+1} before waiting for P_j, so the tensor core
-//              computes the next scores while the softmax warps work.
-//   warps 0-3: one thread per query row (= TMEM lane).  Per key tile: load the
-//              score row from TMEM, mask (causal diagonal, keys past N), update
-//              the running max m and sum l in base 2, write P as bf16 into TMEM,
-//              rescale the O accumulator in TMEM when m grew, signal the MMA
-//              warp.  Epilogue: O / l -> bf16, LSE = ln2 * (m + log2 l).
+// Hardware mapping.  The pages' H100 design (wgmma into registers, TMA,
+// swizzled shared memory; "GPUの爆発的な性能向上", ja.news.hada.io topic 14783,
+// sections "WGMMA", "Shared memoryとbank conflict", "アドレス生成とTMA",
+// "Occupancyが隠してくれるコスト") is prior art.  Here a CTA owns T = 1 or 2
+// query tiles of 128 rows of one (batch, head) and streams that head's K and
+// V tiles once for both:
+//   warp 12      : TMA producer.  Q tiles once; K_j, V_j into a ring of
+//                  128-byte-swizzled shared-memory slots (full/empty mbarriers).
+//   warp 13      : allocates the 512 TMEM columns; one thread issues tcgen05.mma:
+//                  S_i = Q_i K_j^T into TMEM buffer i, and O_i += P_i V_j with P_i
+//                  read back from TMEM (bf16, written over S_i).  The order
+//                  PV_0(j), S_0(j+1), PV_1(j), S_1(j+1) keeps the tensor core on
+//                  one tile while the other tile's softmax runs (ping-pong).
+//   warpgroup i  : (i = 0, 1; warps 4i..4i+3) softmax of query tile i, one
+//                  thread per row (= TMEM lane).  Masks, running max in base 2,
+//                  p = 2^(s*scale*log2e - m) with packed fp32x2 math, P -> TMEM,
+//                  running sum.  The reference max m only moves when a row's max
+//                  grows by more than 2^8; rescale factors go to TMEM for the
+//                  correction warps; the LSE is written at the end.
+//   warpgroup 2  : (warps 8..11) correction: O_i *= alpha in TMEM between PV
+//                  steps (skipped when no row of the warp moved its max);
+//                  epilogue O_i / l -> bf16 -> swizzled shared memory -> TMA store.
 // Every barrier wait is bounded: on expiry the kernel records a timeout in a
 // device status word, the other roles see a shared abort flag, in-flight TMA
 // copies and MMAs are drained, TMEM is freed and the CTA returns.
@@ -35,25 +42,30 @@
 
 namespace attn {
 
-constexpr int BM = 128;                   // query rows per CTA (= TMEM lanes)
-constexpr int BN = 128;                   // keys per tile
-constexpr int kThreads = 192;             // 4 softmax warps + TMA warp + MMA warp
-constexpr int kLoadWarp = 4;
-constexpr int kMmaWarp = 5;
+constexpr int BM = 128;                     // query rows per tile (= TMEM lanes)
+constexpr int BN = 128;                     // keys per tile
+constexpr int kThreads = 512;               // 4 warpgroups
+constexpr int kCorrWarp0 = 8;               // warps 8..11: correction / epilogue
+constexpr int kLoadWarp = 12;
+constexpr int kMmaWarp = 13;                // warps 14, 15 idle (complete the warpgroup)
 constexpr uint32_t kSubTile = 128u * 128u;  // 128 rows x 64 bf16 (one 128-B swizzle span)
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kTmemS = 0;            // two score buffers: columns [0,128) and [128,256)
-constexpr uint32_t kTmemO = 256;          // O accumulator: columns [256, 256 + D)
-constexpr int kStatusTimeout = 4;         // value of ATTN_ERR_TIMEOUT
+constexpr float kRescaleLog2 = 8.0f;        // move the reference max only when it grows by > 2^8
+constexpr int kStatusTimeout = 4;           // value of ATTN_ERR_TIMEOUT
+// Register split (setmaxnreg): 2 x 128 softmax threads at 184, 128 correction
+// threads at 96, 128 load/MMA/idle threads at 48 = 65536 = 512 threads x 128.
+constexpr uint32_t kRegSoftmax = 184, kRegCorr = 96, kRegOther = 48;
+static_assert(2 * 128 * kRegSoftmax + 128 * kRegCorr + 128 * kRegOther == kThreads * 128, "register split");
 
 struct FwdParams {
-  CUtensorMap tq, tk, tv;  // 3-D maps {D, N, B*H}, box {64, 128, 1}, 128-B swizzle, zero fill
-  __nv_bfloat16* o;        // [B*H, N, D]
-  float* lse;              // [B*H, N]
+  CUtensorMap tq, tk, tv, to;  // 3-D maps {D, N, B*H}, box {64, 128, 1}, 128-B swizzle, zero fill
+  float* lse;                  // [B*H, N]
   int N;
-  int bh;                  // B*H
-  int n_tiles;             // ceil(N / 128), for queries and keys alike
-  float scale_log2;        // scale * log2(e)
+  int bh;                      // B*H
+  int n_tiles;                 // ceil(N / 128), for queries and keys alike
+  int tiles_per_cta;           // T = 1 or 2 query tiles per CTA
+  int n_units;                 // ceil(n_tiles / T): CTAs per (batch, head)
+  float scale_log2;            // scale * log2(e)
   long long timeout_cycles;
 };
 
@@ -61,20 +73,27 @@ template <int D>
 struct Cfg {
   static_assert(D == 64 || D == 128, "head dim");
   static constexpr int KB = D / 64;                      // 64-column sub-tiles per tile
-  static constexpr int NS = D == 128 ? 3 : 4;            // K and V ring depth
   static constexpr uint32_t TILE = KB * kSubTile;        // bytes of one 128 x D bf16 tile
+  static constexpr int NSLOT = D == 128 ? 5 : 10;        // K/V ring slots (one tile each)
   static constexpr uint32_t OFF_Q = 1024;                // first 1 KB: barriers and flags
-  static constexpr uint32_t OFF_K = OFF_Q + TILE;
-  static constexpr uint32_t OFF_V = OFF_K + NS * TILE;
-  static constexpr uint32_t USED = OFF_V + NS * TILE;
-  // + 1 KB to align the base; D = 64 also keeps 32 KB of tail room so that no
-  // operand descriptor of the last V stage can address past the allocation.
-  static constexpr uint32_t SMEM = USED + 1024 + (D == 64 ? 32768u : 0u);
+  static constexpr uint32_t OFF_KV = OFF_Q + 2 * TILE;
+  static constexpr uint32_t USED = OFF_KV + NSLOT * TILE;
+  static constexpr uint32_t SMEM = USED + 1024;          // + slack to align the base to 1 KB
+  static_assert(SMEM <= 232448, "shared memory");
   // barrier slots
-  static constexpr int B_Q = 0, B_KF = 1, B_KE = 1 + NS, B_VF = 1 + 2 * NS, B_VE = 1 + 3 * NS;
-  static constexpr int B_SF = 1 + 4 * NS, B_PF = 3 + 4 * NS, B_OF = 5 + 4 * NS, B_DONE = 6 + 4 * NS;
-  static constexpr int NBAR = 7 + 4 * NS;
+  static constexpr int B_Q = 0, B_FULL = 1, B_EMPTY = 1 + NSLOT;
+  static constexpr int B_SF = 1 + 2 * NSLOT;  // [2] scores of tile i ready (MMA commit)
+  static constexpr int B_PF = B_SF + 2;       // [2] P of tile i in TMEM (128 softmax threads)
+  static constexpr int B_AR = B_PF + 2;       // [2] rescale factor / final 1/l in TMEM (128 softmax threads)
+  static constexpr int B_OR = B_AR + 2;       // [2] O of tile i rescaled (128 correction threads)
+  static constexpr int B_OF = B_OR + 2;       // [2] O_i += P_i V_j finished (MMA commit)
+  static constexpr int B_DONE = B_OF + 2;
+  static constexpr int NBAR = B_DONE + 1;
   static_assert(NBAR * 8 <= 512, "barrier area");
+  // TMEM columns
+  static constexpr uint32_t COL_S = 0;     // S_i at COL_S + 128 i (P_i over its first 64 columns)
+  static constexpr uint32_t COL_O = 256;   // O_i at COL_O + D i
+  static constexpr uint32_t COL_ALPHA = 64, COL_INVL = 65;  // inside S_i, above P_i
 };
 
 __device__ int g_attn_status;  // 0 or kStatusTimeout; read and cleared by the host
@@ -103,11 +122,16 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, cons
   }
 }
 
+// Warp-uniform version: every lane waits, the warp proceeds only if all saw it.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const Abort& ab) {
+  return __all_sync(0xffffffffu, wait_bounded(bar, parity, ab));
+}
+
 template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 1) attn_fwd_sm103(const __grid_constant__ FwdParams p) {
   using C = Cfg<D>;
-  constexpr int NS = C::NS;
   constexpr int KB = C::KB;
+  constexpr int NSLOT = C::NSLOT;
 
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = sm103::smem_u32(smem_raw);
@@ -115,29 +139,37 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_sm103(const __grid_const
   uint8_t* const sbase = smem_raw + (base - raw);
   uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(sbase + 512);
   volatile uint32_t* const abort_flag = reinterpret_cast<volatile uint32_t*>(sbase + 516);
-  const uint32_t sQ = base + C::OFF_Q, sK = base + C::OFF_K, sV = base + C::OFF_V;
+  const uint32_t sQ = base + C::OFF_Q;   // Q_i at sQ + i * TILE (later: O_i staging)
+  const uint32_t sKV = base + C::OFF_KV; // slot s at sKV + s * TILE
   auto bar = [base](int i) { return base + 8u * uint32_t(i); };
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  // Tile order.  Causal: heaviest query tiles first (longest-processing-time
-  // order across all heads).  Full: the query tiles of one head are adjacent
-  // so that its K and V stay hot in L2.
-  int qt, bh;
+  // Work of this CTA.  Causal: heaviest units first (longest-processing-time
+  // order across all heads).  Full: the units of one head are adjacent so its
+  // K and V stay hot in L2.
+  const int T = p.tiles_per_cta;
+  int unit, bh;
   if (CAUSAL) {
-    qt = p.n_tiles - 1 - int(blockIdx.x / uint32_t(p.bh));
+    unit = p.n_units - 1 - int(blockIdx.x / uint32_t(p.bh));
     bh = int(blockIdx.x % uint32_t(p.bh));
   } else {
-    qt = int(blockIdx.x % uint32_t(p.n_tiles));
-    bh = int(blockIdx.x / uint32_t(p.n_tiles));
+    unit = int(blockIdx.x % uint32_t(p.n_units));
+    bh = int(blockIdx.x / uint32_t(p.n_units));
   }
-  const int m0 = qt * BM;
-  const int nk = CAUSAL ? qt + 1 : p.n_tiles;  // key tiles this query tile visits
+  const int t0 = unit * T;
+  // key tiles visited by query tile 0 and 1 (0 when the CTA has one tile)
+  const int nk0 = CAUSAL ? t0 + 1 : p.n_tiles;
+  const int nk1 = T == 2 ? (CAUSAL ? min(t0 + 2, p.n_tiles) : p.n_tiles) : 0;
+  const int nk = max(nk0, nk1);
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < C::NBAR; ++i)
-      sm103::mbar_init(bar(i), (i == C::B_PF || i == C::B_PF + 1) ? uint32_t(BM) : 1u);
+    for (int i = 0; i < C::NBAR; ++i) {
+      uint32_t cnt = 1;
+      if (i >= C::B_PF && i < C::B_OR + 2) cnt = BM;  // P, alpha and O-ready barriers: 128 threads
+      sm103::mbar_init(bar(i), cnt);
+    }
     *abort_flag = 0u;
     sm103::fence_mbar_init();
   }
@@ -149,6 +181,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_sm103(const __grid_const
     sm103::tma_prefetch_map(&p.tq);
     sm103::tma_prefetch_map(&p.tk);
     sm103::tma_prefetch_map(&p.tv);
+    sm103::tma_prefetch_map(&p.to);
   }
   sm103::tc_fence_before();
   __syncthreads();
@@ -156,188 +189,269 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_sm103(const __grid_const
   const uint32_t tmem = *tmem_slot;
   const Abort ab{abort_flag, p.timeout_cycles};
 
-  if (warp == kLoadWarp) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      sm103::mbar_arrive_expect_tx(bar(C::B_Q), C::TILE);
-      for (int kb = 0; kb < KB; ++kb)
-        sm103::tma_load_3d(sQ + kb * kSubTile, &p.tq, bar(C::B_Q), kb * 64, m0, bh);
-      int kiss = 0, viss = 0;  // K and V tiles issued
-      for (int j = 0; j < nk; ++j) {
-        const int s = j % NS;
-        const uint32_t ph = uint32_t(j / NS) & 1u;
-        if (j >= NS && !wait_bounded(bar(C::B_KE + s), ph ^ 1u, ab)) break;
-        sm103::mbar_arrive_expect_tx(bar(C::B_KF + s), C::TILE);
-        for (int kb = 0; kb < KB; ++kb)
-          sm103::tma_load_3d(sK + s * C::TILE + kb * kSubTile, &p.tk, bar(C::B_KF + s), kb * 64, j * BN, bh);
-        ++kiss;
-        if (j >= NS && !wait_bounded(bar(C::B_VE + s), ph ^ 1u, ab)) break;
-        sm103::mbar_arrive_expect_tx(bar(C::B_VF + s), C::TILE);
-        for (int kb = 0; kb < KB; ++kb)
-          sm103::tma_load_3d(sV + s * C::TILE + kb * kSubTile, &p.tv, bar(C::B_VF + s), kb * 64, j * BN, bh);
-        ++viss;
-      }
-      // Drain: no copy may land in shared memory after this CTA has left.
-      wait_bounded(bar(C::B_Q), 0u, ab, false);
-      for (int t = kiss > NS ? kiss - NS : 0; t < kiss; ++t)
-        wait_bounded(bar(C::B_KF + t % NS), uint32_t(t / NS) & 1u, ab, false);
-      for (int t = viss > NS ? viss - NS : 0; t < viss; ++t)
-        wait_bounded(bar(C::B_VF + t % NS), uint32_t(t / NS) & 1u, ab, false);
-    }
-    __syncwarp();
-  } else if (warp == kMmaWarp) {
-    // ------------------------------------------------------------- MMA issue
-    if (lane == 0) {
-      constexpr uint32_t kIdescS = sm103::idesc_bf16_f32(BM, BN, 0, 0);  // Q, K both K-major
-      constexpr uint32_t kIdescO = sm103::idesc_bf16_f32(BM, D, 0, 1);   // P K-major, V MN-major
-      auto issue_pv = [&](int jj) -> bool {
-        const int s = jj % NS;
-        const int b = jj & 1;
-        if (!wait_bounded(bar(C::B_PF + b), uint32_t(jj >> 1) & 1u, ab)) return false;
-        if (!wait_bounded(bar(C::B_VF + s), uint32_t(jj / NS) & 1u, ab)) return false;
-        sm103::tc_fence_after();
-        const uint32_t aP = tmem + kTmemS + uint32_t(b) * BN;
-        const uint32_t vbase = sV + s * C::TILE;
-#pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk)  // 16 keys per MMA: 8 TMEM columns of P, 16 rows of V
-          sm103::mma_ts(tmem + kTmemO, aP + kk * 8, sm103::sdesc_sw128(vbase + kk * 2048, kSubTile, 1024),
-                        kIdescO, (jj > 0 || kk > 0) ? 1u : 0u);
-        sm103::mma_commit(bar(C::B_OF));
-        sm103::mma_commit(bar(C::B_VE + s));
-        return true;
-      };
-      bool ok = wait_bounded(bar(C::B_Q), 0u, ab);
-      for (int j = 0; ok && j < nk; ++j) {
-        const int s = j % NS;
-        const int b = j & 1;
-        if (!(ok = wait_bounded(bar(C::B_KF + s), uint32_t(j / NS) & 1u, ab))) break;
-        sm103::tc_fence_after();
-        const uint32_t kbase = sK + s * C::TILE;
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {  // 16 of the head dim per MMA
-          const uint32_t off = uint32_t(kk >> 2) * kSubTile + uint32_t(kk & 3) * 32u;
-          sm103::mma_ss(tmem + kTmemS + uint32_t(b) * BN, sm103::sdesc_sw128(sQ + off, 16, 1024),
-                        sm103::sdesc_sw128(kbase + off, 16, 1024), kIdescS, kk > 0 ? 1u : 0u);
-        }
-        sm103::mma_commit(bar(C::B_SF + b));
-        sm103::mma_commit(bar(C::B_KE + s));
-        if (j > 0) ok = issue_pv(j - 1);
-      }
-      if (ok) issue_pv(nk - 1);
-      // Every MMA must be finished before TMEM is freed.
-      sm103::mma_commit(bar(C::B_DONE));
-      wait_bounded(bar(C::B_DONE), 0u, ab, false);
-    }
-    __syncwarp();
-  } else {
-    // ---------------------------------------------------- softmax, epilogue
-    const int r = threadIdx.x;  // row within the tile = TMEM lane
-    const uint32_t lane_off = uint32_t(warp * 32) << 16;
-    const uint32_t tO = tmem + lane_off + kTmemO;
-    const float sl2 = p.scale_log2;
-    float m_run = -INFINITY;  // running max of scale*log2(e)*s
-    float l_run = 0.f;        // running sum of p (fp32, before the bf16 rounding of P)
-    bool ok = true;
-    for (int j = 0; j < nk; ++j) {
-      const int b = j & 1;
-      ok = __all_sync(0xffffffffu, wait_bounded(bar(C::B_SF + b), uint32_t(j >> 1) & 1u, ab));
-      if (!ok) break;
-      sm103::tc_fence_after();
-      const uint32_t tS = tmem + lane_off + kTmemS + uint32_t(b) * BN;
-      float s[BN];
-#pragma unroll
-      for (int q = 0; q < BN / 32; ++q) {
-        uint32_t u[32];
-        sm103::tmem_ld32(tS + q * 32, u);
-#pragma unroll
-        for (int e = 0; e < 32; ++e) s[q * 32 + e] = __uint_as_float(u[e]);
-      }
-      // Masks: the causal diagonal tile (key c visible iff c <= r) and keys past N.
-      int lim = BN - 1;
-      if (CAUSAL && j == nk - 1) lim = r;
-      if (j == p.n_tiles - 1) lim = min(lim, p.N - 1 - j * BN);
-      if (lim < BN - 1) {
-#pragma unroll
-        for (int c = 0; c < BN; ++c) s[c] = c > lim ? -INFINITY : s[c];
-      }
-      float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
-#pragma unroll
-      for (int c = 4; c < BN; c += 4) {
-        mx0 = fmaxf(mx0, s[c]);
-        mx1 = fmaxf(mx1, s[c + 1]);
-        mx2 = fmaxf(mx2, s[c + 2]);
-        mx3 = fmaxf(mx3, s[c + 3]);
-      }
-      const float m_new = fmaxf(m_run, fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2);
-      const float alpha = sm103::ex2_approx(m_run - m_new);  // 0 on the first tile
-      const float neg_m = -m_new;
-      float sum0 = 0.f, sum1 = 0.f, sum2 = 0.f, sum3 = 0.f;
-#pragma unroll
-      for (int q = 0; q < BN / 32; ++q) {
-        uint32_t pk[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const float p0 = sm103::ex2_approx(fmaf(s[q * 32 + 2 * e], sl2, neg_m));
-          const float p1 = sm103::ex2_approx(fmaf(s[q * 32 + 2 * e + 1], sl2, neg_m));
-          pk[e] = sm103::pack_bf16x2(p0, p1);
-          if (e & 1) {
-            sum2 += p0;
-            sum3 += p1;
-          } else {
-            sum0 += p0;
-            sum1 += p1;
+  if (warp >= kLoadWarp) {
+    sm103::regs_decrease<kRegOther>();
+    if (warp == kLoadWarp) {
+      // ---------------------------------------------------------- producer
+      if (lane == 0) {
+        sm103::mbar_arrive_expect_tx(bar(C::B_Q), uint32_t(T) * C::TILE);
+        for (int i = 0; i < T; ++i)
+          for (int kb = 0; kb < KB; ++kb)
+            sm103::tma_load_3d(sQ + i * C::TILE + kb * kSubTile, &p.tq, bar(C::B_Q), kb * 64, (t0 + i) * BM, bh);
+        int c = 0;  // loads issued; K_j is load 2j, V_j load 2j+1
+        bool ok = true;
+        for (int j = 0; ok && j < nk; ++j) {
+          for (int kv = 0; kv < 2; ++kv, ++c) {
+            const int s = c % NSLOT;
+            if (c >= NSLOT && !(ok = wait_bounded(bar(C::B_EMPTY + s), uint32_t(c / NSLOT - 1) & 1u, ab))) break;
+            sm103::mbar_arrive_expect_tx(bar(C::B_FULL + s), C::TILE);
+            const CUtensorMap* map = kv == 0 ? &p.tk : &p.tv;
+            for (int kb = 0; kb < KB; ++kb)
+              sm103::tma_load_3d(sKV + s * C::TILE + kb * kSubTile, map, bar(C::B_FULL + s), kb * 64, j * BN, bh);
           }
         }
-        sm103::tmem_st16(tS + q * 16, pk);  // P over the first 64 columns of this S buffer
+        // Drain: no copy may land in shared memory after this CTA has left.
+        wait_bounded(bar(C::B_Q), 0u, ab, false);
+        for (int t = c > NSLOT ? c - NSLOT : 0; t < c; ++t)
+          wait_bounded(bar(C::B_FULL + t % NSLOT), uint32_t(t / NSLOT) & 1u, ab, false);
       }
-      sm103::tmem_st_wait();
-      l_run = alpha * l_run + ((sum0 + sum1) + (sum2 + sum3));
-      m_run = m_new;
-      if (j > 0) {
-        // O holds sum over earlier tiles; P_{j-1} V_{j-1} must have landed first.
-        ok = __all_sync(0xffffffffu, wait_bounded(bar(C::B_OF), uint32_t(j - 1) & 1u, ab));
-        if (!ok) break;
+      __syncwarp();
+    } else if (warp == kMmaWarp) {
+      // ----------------------------------------------------------- MMA issue
+      if (lane == 0) {
+        constexpr uint32_t kIdescS = sm103::idesc_bf16_f32(BM, BN, 0, 0);  // Q, K both K-major
+        constexpr uint32_t kIdescO = sm103::idesc_bf16_f32(BM, D, 0, 1);   // P K-major, V MN-major
+        // Descriptors are built once; moving an operand by `off` bytes adds off >> 4
+        // to the start-address field (no carry: shared addresses stay below 256 KB).
+        const uint64_t desc_q = sm103::sdesc_sw128(sQ, 16, 1024);         // K-major Q tiles
+        const uint64_t desc_k = sm103::sdesc_sw128(sKV, 16, 1024);        // K-major K slots
+        const uint64_t desc_v = sm103::sdesc_sw128(sKV, kSubTile, 1024);  // MN-major V slots
+        auto slot_off = [](int c) { return uint64_t(uint32_t(c % NSLOT) * (C::TILE >> 4)); };
+        auto wait_full = [&](int c) { return wait_bounded(bar(C::B_FULL + c % NSLOT), uint32_t(c / NSLOT) & 1u, ab); };
+        auto release = [&](int c) { sm103::mma_commit(bar(C::B_EMPTY + c % NSLOT)); };
+        auto issue_s = [&](int i, int j) {
+          const uint64_t dk = desc_k + slot_off(2 * j), dq = desc_q + uint64_t(uint32_t(i) * (C::TILE >> 4));
+          const uint32_t dS = tmem + C::COL_S + uint32_t(i) * BN;
+#pragma unroll 1
+          for (int kk = 0; kk < D / 16; ++kk) {  // 16 of the head dim per MMA
+            const uint64_t off = uint64_t((uint32_t(kk >> 2) * kSubTile + uint32_t(kk & 3) * 32u) >> 4);
+            sm103::mma_ss(dS, dq + off, dk + off, kIdescS, kk > 0 ? 1u : 0u);
+          }
+          sm103::mma_commit(bar(C::B_SF + i));
+        };
+        auto issue_pv = [&](int i, int j) -> bool {
+          if (!wait_bounded(bar(C::B_PF + i), uint32_t(j) & 1u, ab)) return false;
+          if (j > 0 && !wait_bounded(bar(C::B_OR + i), uint32_t(j - 1) & 1u, ab)) return false;
+          sm103::tc_fence_after();
+          const uint64_t dv = desc_v + slot_off(2 * j + 1);
+          const uint32_t aP = tmem + C::COL_S + uint32_t(i) * BN;
+          const uint32_t dO = tmem + C::COL_O + uint32_t(i) * D;
+#pragma unroll 1
+          for (int kk = 0; kk < BN / 16; ++kk)  // 16 keys per MMA: 8 TMEM columns of P, 16 rows of V
+            sm103::mma_ts(dO, aP + kk * 8, dv + uint64_t(kk * (2048 >> 4)), kIdescO, (j > 0 || kk > 0) ? 1u : 0u);
+          sm103::mma_commit(bar(C::B_OF + i));
+          return true;
+        };
+        bool ok = wait_bounded(bar(C::B_Q), 0u, ab) && wait_full(0);
+        if (ok) {
+          sm103::tc_fence_after();
+          issue_s(0, 0);
+          if (nk1 > 0) issue_s(1, 0);
+          release(0);
+        }
+        for (int j = 0; ok && j < nk; ++j) {
+          const bool next = j + 1 < nk;
+          if (next && !(ok = wait_full(2 * j + 2))) break;
+          if (!(ok = wait_full(2 * j + 1))) break;
+          sm103::tc_fence_after();
+          if (j < nk0) {
+            if (!(ok = issue_pv(0, j))) break;
+            if (j + 1 < nk0) issue_s(0, j + 1);
+          }
+          if (j < nk1) {
+            if (!(ok = issue_pv(1, j))) break;
+            if (j + 1 < nk1) issue_s(1, j + 1);
+          }
+          release(2 * j + 1);
+          if (next) release(2 * j + 2);
+        }
+        // Every MMA must be finished before TMEM is freed.
+        sm103::mma_commit(bar(C::B_DONE));
+        wait_bounded(bar(C::B_DONE), 0u, ab, false);
+      }
+      __syncwarp();
+    }
+  } else if (warp < kCorrWarp0) {
+    // ------------------------------------------------------------- softmax
+    sm103::regs_increase<kRegSoftmax>();
+    const int i = warp >> 2;            // query tile of this warpgroup
+    const int r = threadIdx.x & 127;    // row within the tile = TMEM lane
+    const int nki = i == 0 ? nk0 : nk1;
+    if (nki > 0) {
+      const uint32_t lane_off = uint32_t((warp & 3) * 32) << 16;
+      const uint32_t tS = tmem + lane_off + C::COL_S + uint32_t(i) * BN;
+      const int row = (t0 + i) * BM + r;
+      const float sl2 = p.scale_log2;
+      const uint64_t sl2x2 = sm103::f2_pack(sl2, sl2);
+      float m_ref = 0.f;  // reference max (base 2) the exponents are taken against
+      float l_run = 0.f;  // running sum of p (fp32, before the bf16 rounding of P)
+      bool ok = true;
+      for (int j = 0; j < nki; ++j) {
+        if (!(ok = warp_wait(bar(C::B_SF + i), uint32_t(j) & 1u, ab))) break;
         sm103::tc_fence_after();
-        if (__any_sync(0xffffffffu, alpha < 1.f)) {
+        float s[BN];
+        {
+          uint32_t u[BN];
+          sm103::tmem_ld128(tS, u);
+#pragma unroll
+          for (int c = 0; c < BN; ++c) s[c] = __uint_as_float(u[c]);
+        }
+        // Masks: keys past N, and keys after the query row when causal.
+        int lim = min(BN - 1, p.N - 1 - j * BN);
+        if (CAUSAL) lim = min(lim, row - j * BN);
+        if (lim < BN - 1) {
+#pragma unroll
+          for (int c = 0; c < BN; ++c) s[c] = c > lim ? -INFINITY : s[c];
+        }
+        float mx0 = sm103::max3(s[0], s[1], s[2]);
+        float mx1 = sm103::max3(s[3], s[4], s[5]);
+        float mx2 = sm103::max3(s[6], s[7], s[8]);
+        float mx3 = sm103::max3(s[9], s[10], s[11]);
+#pragma unroll
+        for (int c = 12; c + 8 <= BN - 4; c += 8) {
+          mx0 = sm103::max3(mx0, s[c], s[c + 1]);
+          mx1 = sm103::max3(mx1, s[c + 2], s[c + 3]);
+          mx2 = sm103::max3(mx2, s[c + 4], s[c + 5]);
+          mx3 = sm103::max3(mx3, s[c + 6], s[c + 7]);
+        }
+        mx0 = sm103::max3(mx0, s[BN - 4], s[BN - 3]);
+        mx1 = sm103::max3(mx1, s[BN - 2], s[BN - 1]);
+        const float cand = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
+        float alpha = 1.f;
+        if (j == 0) {
+          m_ref = cand;
+        } else {
+          if (cand > m_ref + kRescaleLog2) {
+            alpha = sm103::ex2_approx(m_ref - cand);
+            m_ref = cand;
+          }
+          // Hand alpha to the correction warps now, so O is rescaled while the exps run.
+          sm103::tmem_st1(tS + C::COL_ALPHA, __float_as_uint(alpha));
+          sm103::tmem_st_wait();
+          sm103::tc_fence_before();
+          sm103::mbar_arrive(bar(C::B_AR + i));
+        }
+        const uint64_t negm = sm103::f2_pack(-m_ref, -m_ref);
+        uint64_t acc0 = 0, acc1 = 0;  // packed fp32 partial sums (+0.0f, +0.0f)
+#pragma unroll
+        for (int q = 0; q < BN / 32; ++q) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const uint64_t t = sm103::f2_fma(sm103::f2_pack(s[q * 32 + 2 * e], s[q * 32 + 2 * e + 1]), sl2x2, negm);
+            float t_lo, t_hi;
+            sm103::f2_unpack(t, t_lo, t_hi);
+            const float p0 = sm103::ex2_approx(t_lo);
+            const float p1 = sm103::ex2_approx(t_hi);
+            pk[e] = sm103::pack_bf16x2(p0, p1);
+            if (e & 1)
+              acc1 = sm103::f2_add(acc1, sm103::f2_pack(p0, p1));
+            else
+              acc0 = sm103::f2_add(acc0, sm103::f2_pack(p0, p1));
+          }
+          sm103::tmem_st16(tS + q * 16, pk);  // P over the first 64 columns of S_i
+        }
+        float a0, a1, a2, a3;
+        sm103::f2_unpack(acc0, a0, a1);
+        sm103::f2_unpack(acc1, a2, a3);
+        const float rowsum = (a0 + a1) + (a2 + a3);
+        l_run = j == 0 ? rowsum : fmaf(alpha, l_run, rowsum);
+        sm103::tmem_st_wait();
+        sm103::tc_fence_before();
+        sm103::mbar_arrive(bar(C::B_PF + i));
+      }
+      if (ok) {
+        // 1/l for the correction warps' epilogue; LSE from here.
+        sm103::tmem_st1(tS + C::COL_INVL, __float_as_uint(1.f / l_run));
+        sm103::tmem_st_wait();
+        sm103::tc_fence_before();
+        sm103::mbar_arrive(bar(C::B_AR + i));
+        if (row < p.N) p.lse[size_t(bh) * size_t(p.N) + size_t(row)] = (m_ref + log2f(l_run)) * 0.6931471805599453f;
+      }
+    }
+  } else {
+    // ------------------------------------------------- correction, epilogue
+    sm103::regs_decrease<kRegCorr>();
+    const int r = threadIdx.x & 127;
+    const uint32_t lane_off = uint32_t((warp & 3) * 32) << 16;
+    bool ok = true;
+    for (int j = 1; ok && j < nk; ++j) {
+      for (int i = 0; i < T; ++i) {
+        if (j >= (i == 0 ? nk0 : nk1)) continue;
+        const uint32_t tS = tmem + lane_off + C::COL_S + uint32_t(i) * BN;
+        const uint32_t tO = tmem + lane_off + C::COL_O + uint32_t(i) * D;
+        if (!(ok = warp_wait(bar(C::B_AR + i), uint32_t(j - 1) & 1u, ab))) break;
+        sm103::tc_fence_after();
+        const float alpha = __uint_as_float(sm103::tmem_ld1(tS + C::COL_ALPHA));
+        if (!(ok = warp_wait(bar(C::B_OF + i), uint32_t(j - 1) & 1u, ab))) break;
+        sm103::tc_fence_after();
+        if (__any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll
           for (int q = 0; q < D / 32; ++q) {
-            uint32_t u[32];
-            sm103::tmem_ld32(tO + q * 32, u);
+            uint32_t v[32];
+            sm103::tmem_ld32(tO + q * 32, v);
 #pragma unroll
-            for (int e = 0; e < 32; ++e) u[e] = __float_as_uint(__uint_as_float(u[e]) * alpha);
-            sm103::tmem_st32(tO + q * 32, u);
+            for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
+            sm103::tmem_st32(tO + q * 32, v);
           }
           sm103::tmem_st_wait();
         }
+        sm103::tc_fence_before();
+        sm103::mbar_arrive(bar(C::B_OR + i));
       }
-      sm103::tc_fence_before();
-      sm103::mbar_arrive(bar(C::B_PF + b));
     }
-    if (ok) ok = __all_sync(0xffffffffu, wait_bounded(bar(C::B_OF), uint32_t(nk - 1) & 1u, ab));
-    if (ok) {
+    // Epilogue.  The four warps agree (reduction barrier) before touching the
+    // shared staging tile, so a warp that gave up on a wait cannot leave the
+    // others stuck at the named barrier below.
+    for (int i = 0; i < T; ++i) {
+      const int nki = i == 0 ? nk0 : nk1;
+      const uint32_t tS = tmem + lane_off + C::COL_S + uint32_t(i) * BN;
+      const uint32_t tO = tmem + lane_off + C::COL_O + uint32_t(i) * D;
+      if (ok) ok = warp_wait(bar(C::B_AR + i), uint32_t(nki - 1) & 1u, ab);
+      if (ok) ok = warp_wait(bar(C::B_OF + i), uint32_t(nki - 1) & 1u, ab);
+      ok = sm103::named_bar_and(1, 128, ok);
+      if (!ok) break;
       sm103::tc_fence_after();
-      const float inv_l = 1.f / l_run;
-      const int row = m0 + r;
-      const bool live = row < p.N;
-      __nv_bfloat16* const orow = p.o + (size_t(bh) * size_t(p.N) + size_t(live ? row : 0)) * D;
+      const int m0 = (t0 + i) * BM;
+      if (m0 >= p.N) continue;  // a second tile wholly past N: nothing to store
+      const float inv_l = __uint_as_float(sm103::tmem_ld1(tS + C::COL_INVL));
+      // O_i / l -> bf16 into the (now idle) Q_i tile, laid out as TMA's 128-byte
+      // swizzle expects: row r at 128 r, 16-byte chunk c at ((c ^ (r & 7)) * 16).
+      const uint32_t stage = sQ + uint32_t(i) * C::TILE;
 #pragma unroll
       for (int q = 0; q < D / 32; ++q) {
-        uint32_t u[32];
-        sm103::tmem_ld32(tO + q * 32, u);
+        uint32_t v[32];
+        sm103::tmem_ld32(tO + q * 32, v);
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e)
-          pk[e] = sm103::pack_bf16x2(__uint_as_float(u[2 * e]) * inv_l, __uint_as_float(u[2 * e + 1]) * inv_l);
-        if (live) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + q * 32);
-          dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-          dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
-          dst[2] = make_uint4(pk[8], pk[9], pk[10], pk[11]);
-          dst[3] = make_uint4(pk[12], pk[13], pk[14], pk[15]);
+          pk[e] = sm103::pack_bf16x2(__uint_as_float(v[2 * e]) * inv_l, __uint_as_float(v[2 * e + 1]) * inv_l);
+        const uint32_t rowbase = stage + uint32_t(q >> 1) * kSubTile + uint32_t(r) * 128u;
+#pragma unroll
+        for (int c4 = 0; c4 < 4; ++c4) {
+          const uint32_t chunk = uint32_t((q & 1) * 4 + c4);
+          sm103::st_shared_v4(rowbase + ((chunk ^ uint32_t(r & 7)) << 4), pk[4 * c4], pk[4 * c4 + 1],
+                              pk[4 * c4 + 2], pk[4 * c4 + 3]);
         }
       }
-      if (live) p.lse[size_t(bh) * size_t(p.N) + size_t(row)] = (m_run + log2f(l_run)) * 0.6931471805599453f;
+      sm103::fence_proxy_async_smem();
+      sm103::named_bar_sync(1, 128);
+      if (r == 0) {
+        for (int kb = 0; kb < KB; ++kb) sm103::tma_store_3d(&p.to, stage + kb * kSubTile, kb * 64, m0, bh);
+        sm103::bulk_commit();
+      }
     }
+    if (r == 0) sm103::bulk_wait_read0();  // the stores have read shared memory
   }
 
   sm103::tc_fence_before();
