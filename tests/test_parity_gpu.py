@@ -76,20 +76,34 @@ def test_workload_sampled(name):
     assert_close(of, lf, o_ref, lse_ref, name)
 
 
+@pytest.fixture(params=["1", "2"], ids=["one_tile_per_cta", "two_tiles_per_cta"])
+def tiles_per_cta(request, monkeypatch):
+    """Force the launcher's choice of query tiles per CTA (normally picked from the grid size)."""
+    monkeypatch.setenv("ATTN_TILES_PER_CTA", request.param)
+    return int(request.param)
+
+
 @pytest.mark.parametrize("D", [64, 128])
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("N", [1, 2, 17, 127, 128, 129, 200, 383, 640])
-def test_ragged_and_tiny_lengths(N, D, causal):
+def test_ragged_and_tiny_lengths(N, D, causal, tiles_per_cta):
     q, k, v = make_qkv(2, 3, N, D, seed=500 + N + D)
-    full_check(q, k, v, causal, 1.0 / math.sqrt(D), f"N={N} D={D} causal={causal}")
+    full_check(q, k, v, causal, 1.0 / math.sqrt(D), f"N={N} D={D} causal={causal} T={tiles_per_cta}")
 
 
 @pytest.mark.parametrize("D", [64, 128])
-def test_large_logits_stress_rescaling(D):
+def test_large_logits_stress_rescaling(D, tiles_per_cta):
     # Q spread 8x: logits up to ~40 in magnitude; the running max moves often.
     q, k, v = make_qkv(1, 4, 1000, D, seed=77, q_std=8.0)
     for causal in (False, True):
-        full_check(q, k, v, causal, 1.0 / math.sqrt(D), f"q_std=8 D={D} causal={causal}")
+        full_check(q, k, v, causal, 1.0 / math.sqrt(D), f"q_std=8 D={D} causal={causal} T={tiles_per_cta}")
+
+
+@pytest.mark.parametrize("name", SMALL)
+def test_workload_full_both_tilings(name, tiles_per_cta):
+    w = WORKLOADS[name]
+    q, k, v = w.qkv()
+    full_check(q, k, v, w.causal, w.scale, f"{name} T={tiles_per_cta}")
 
 
 def test_identical_keys_give_mean_of_v():

@@ -150,8 +150,13 @@ attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, flo
   // Two query tiles per CTA share every K/V tile and let two softmax warpgroups
   // take turns on the tensor core; use them whenever that still leaves at least
   // two CTAs per SM to schedule, otherwise one tile per CTA for more parallelism.
+  // ATTN_TILES_PER_CTA=1|2 overrides the choice (testing and tuning).
   const int64_t pairs = (n_tiles + 1) / 2;
-  const int T = pairs * BH >= 2 * int64_t(g_dev_sms[dev]) ? 2 : 1;
+  int T = pairs * BH >= 2 * int64_t(g_dev_sms[dev]) ? 2 : 1;
+  if (const char* e = std::getenv("ATTN_TILES_PER_CTA")) {
+    if (e[0] == '1' && e[1] == 0) T = 1;
+    if (e[0] == '2' && e[1] == 0) T = 2;
+  }
   prm.lse = lse;
   prm.N = int(N);
   prm.bh = int(BH);
