@@ -52,9 +52,9 @@ constexpr uint32_t kSubTile = 128u * 128u;  // 128 rows x 64 bf16 (one 128-B swi
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleLog2 = 8.0f;        // move the reference max only when it grows by > 2^8
 constexpr int kStatusTimeout = 4;           // value of ATTN_ERR_TIMEOUT
-// Register split (setmaxnreg): 2 x 128 softmax threads at 184, 128 correction
-// threads at 96, 128 load/MMA/idle threads at 48 = 65536 = 512 threads x 128.
-constexpr uint32_t kRegSoftmax = 184, kRegCorr = 96, kRegOther = 48;
+// Register split (setmaxnreg): 2 x 128 softmax threads at 176, 128 correction
+// threads at 80, 128 load/MMA/idle threads at 80 = 65536 = 512 threads x 128.
+constexpr uint32_t kRegSoftmax = 176, kRegCorr = 80, kRegOther = 80;
 static_assert(2 * 128 * kRegSoftmax + 128 * kRegCorr + 128 * kRegOther == kThreads * 128, "register split");
 
 struct FwdParams {
@@ -103,21 +103,22 @@ struct Abort {
   long long limit;
 };
 
-// Spin on an mbarrier phase, bounded.  Returns false when another role aborted
-// (if honour_abort) or when `limit` cycles pass; the latter records a timeout.
+// Wait for an mbarrier phase, bounded.  Each try suspends the thread until the
+// phase completes or about a millisecond passes; between tries the wait gives
+// up when another role aborted (if honour_abort) or when `limit` cycles have
+// passed, the latter recording a timeout.
+constexpr uint32_t kSuspendNs = 1000000;
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, const Abort& ab,
                                              bool honour_abort = true) {
   if (sm103::mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
-  for (uint32_t it = 1;; ++it) {
-    if (sm103::mbar_try_wait(bar, parity)) return true;
-    if ((it & 31u) == 0) {
-      if (honour_abort && *ab.flag) return false;
-      if (clock64() - t0 > ab.limit) {
-        atomicCAS(&g_attn_status, 0, kStatusTimeout);
-        *ab.flag = 1u;
-        return false;
-      }
+  for (;;) {
+    if (sm103::mbar_try_wait_sleep(bar, parity, kSuspendNs)) return true;
+    if (honour_abort && *ab.flag) return false;
+    if (clock64() - t0 > ab.limit) {
+      atomicCAS(&g_attn_status, 0, kStatusTimeout);
+      *ab.flag = 1u;
+      return false;
     }
   }
 }
@@ -218,68 +219,67 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_sm103(const __grid_const
       __syncwarp();
     } else if (warp == kMmaWarp) {
       // ----------------------------------------------------------- MMA issue
-      if (lane == 0) {
-        constexpr uint32_t kIdescS = sm103::idesc_bf16_f32(BM, BN, 0, 0);  // Q, K both K-major
-        constexpr uint32_t kIdescO = sm103::idesc_bf16_f32(BM, D, 0, 1);   // P K-major, V MN-major
-        // Descriptors are built once; moving an operand by `off` bytes adds off >> 4
-        // to the start-address field (no carry: shared addresses stay below 256 KB).
-        const uint64_t desc_q = sm103::sdesc_sw128(sQ, 16, 1024);         // K-major Q tiles
-        const uint64_t desc_k = sm103::sdesc_sw128(sKV, 16, 1024);        // K-major K slots
-        const uint64_t desc_v = sm103::sdesc_sw128(sKV, kSubTile, 1024);  // MN-major V slots
-        auto slot_off = [](int c) { return uint64_t(uint32_t(c % NSLOT) * (C::TILE >> 4)); };
-        auto wait_full = [&](int c) { return wait_bounded(bar(C::B_FULL + c % NSLOT), uint32_t(c / NSLOT) & 1u, ab); };
-        auto release = [&](int c) { sm103::mma_commit(bar(C::B_EMPTY + c % NSLOT)); };
-        auto issue_s = [&](int i, int j) {
-          const uint64_t dk = desc_k + slot_off(2 * j), dq = desc_q + uint64_t(uint32_t(i) * (C::TILE >> 4));
-          const uint32_t dS = tmem + C::COL_S + uint32_t(i) * BN;
-#pragma unroll 1
-          for (int kk = 0; kk < D / 16; ++kk) {  // 16 of the head dim per MMA
-            const uint64_t off = uint64_t((uint32_t(kk >> 2) * kSubTile + uint32_t(kk & 3) * 32u) >> 4);
-            sm103::mma_ss(dS, dq + off, dk + off, kIdescS, kk > 0 ? 1u : 0u);
-          }
-          sm103::mma_commit(bar(C::B_SF + i));
-        };
-        auto issue_pv = [&](int i, int j) -> bool {
-          if (!wait_bounded(bar(C::B_PF + i), uint32_t(j) & 1u, ab)) return false;
-          if (j > 0 && !wait_bounded(bar(C::B_OR + i), uint32_t(j - 1) & 1u, ab)) return false;
-          sm103::tc_fence_after();
-          const uint64_t dv = desc_v + slot_off(2 * j + 1);
-          const uint32_t aP = tmem + C::COL_S + uint32_t(i) * BN;
-          const uint32_t dO = tmem + C::COL_O + uint32_t(i) * D;
-#pragma unroll 1
-          for (int kk = 0; kk < BN / 16; ++kk)  // 16 keys per MMA: 8 TMEM columns of P, 16 rows of V
-            sm103::mma_ts(dO, aP + kk * 8, dv + uint64_t(kk * (2048 >> 4)), kIdescO, (j > 0 || kk > 0) ? 1u : 0u);
-          sm103::mma_commit(bar(C::B_OF + i));
-          return true;
-        };
-        bool ok = wait_bounded(bar(C::B_Q), 0u, ab) && wait_full(0);
-        if (ok) {
-          sm103::tc_fence_after();
-          issue_s(0, 0);
-          if (nk1 > 0) issue_s(1, 0);
-          release(0);
+      // The whole warp runs this loop with warp-uniform values; one elected
+      // lane issues each tcgen05.mma and tcgen05.commit.
+      constexpr uint32_t kIdescS = sm103::idesc_bf16_f32(BM, BN, 0, 0);  // Q, K both K-major
+      constexpr uint32_t kIdescO = sm103::idesc_bf16_f32(BM, D, 0, 1);   // P K-major, V MN-major
+      // Descriptors are built once; moving an operand by `off` bytes adds off >> 4
+      // to the start-address field (no carry: shared addresses stay below 256 KB).
+      const uint64_t desc_q = sm103::sdesc_sw128(sQ, 16, 1024);         // K-major Q tiles
+      const uint64_t desc_k = sm103::sdesc_sw128(sKV, 16, 1024);        // K-major K slots
+      const uint64_t desc_v = sm103::sdesc_sw128(sKV, kSubTile, 1024);  // MN-major V slots
+      auto slot_off = [](int c) { return uint64_t(uint32_t(c % NSLOT) * (C::TILE >> 4)); };
+      auto wait_full = [&](int c) { return warp_wait(bar(C::B_FULL + c % NSLOT), uint32_t(c / NSLOT) & 1u, ab); };
+      auto release = [&](int c) { sm103::mma_commit_warp(bar(C::B_EMPTY + c % NSLOT)); };
+      auto issue_s = [&](int i, int j) {
+        const uint64_t dk = desc_k + slot_off(2 * j), dq = desc_q + uint64_t(uint32_t(i) * (C::TILE >> 4));
+        const uint32_t dS = tmem + C::COL_S + uint32_t(i) * BN;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {  // 16 of the head dim per MMA
+          const uint64_t off = uint64_t((uint32_t(kk >> 2) * kSubTile + uint32_t(kk & 3) * 32u) >> 4);
+          sm103::mma_ss_warp(dS, dq + off, dk + off, kIdescS, kk > 0 ? 1u : 0u);
         }
-        for (int j = 0; ok && j < nk; ++j) {
-          const bool next = j + 1 < nk;
-          if (next && !(ok = wait_full(2 * j + 2))) break;
-          if (!(ok = wait_full(2 * j + 1))) break;
-          sm103::tc_fence_after();
-          if (j < nk0) {
-            if (!(ok = issue_pv(0, j))) break;
-            if (j + 1 < nk0) issue_s(0, j + 1);
-          }
-          if (j < nk1) {
-            if (!(ok = issue_pv(1, j))) break;
-            if (j + 1 < nk1) issue_s(1, j + 1);
-          }
-          release(2 * j + 1);
-          if (next) release(2 * j + 2);
-        }
-        // Every MMA must be finished before TMEM is freed.
-        sm103::mma_commit(bar(C::B_DONE));
-        wait_bounded(bar(C::B_DONE), 0u, ab, false);
+        sm103::mma_commit_warp(bar(C::B_SF + i));
+      };
+      auto issue_pv = [&](int i, int j) -> bool {
+        if (!warp_wait(bar(C::B_PF + i), uint32_t(j) & 1u, ab)) return false;
+        if (j > 0 && !warp_wait(bar(C::B_OR + i), uint32_t(j - 1) & 1u, ab)) return false;
+        sm103::tc_fence_after();
+        const uint64_t dv = desc_v + slot_off(2 * j + 1);
+        const uint32_t aP = tmem + C::COL_S + uint32_t(i) * BN;
+        const uint32_t dO = tmem + C::COL_O + uint32_t(i) * D;
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk)  // 16 keys per MMA: 8 TMEM columns of P, 16 rows of V
+          sm103::mma_ts_warp(dO, aP + kk * 8, dv + uint64_t(kk * (2048 >> 4)), kIdescO, (j > 0 || kk > 0) ? 1u : 0u);
+        sm103::mma_commit_warp(bar(C::B_OF + i));
+        return true;
+      };
+      bool ok = warp_wait(bar(C::B_Q), 0u, ab) && wait_full(0);
+      if (ok) {
+        sm103::tc_fence_after();
+        issue_s(0, 0);
+        if (nk1 > 0) issue_s(1, 0);
+        release(0);
       }
-      __syncwarp();
+      for (int j = 0; ok && j < nk; ++j) {
+        const bool next = j + 1 < nk;
+        if (next && !(ok = wait_full(2 * j + 2))) break;
+        if (!(ok = wait_full(2 * j + 1))) break;
+        sm103::tc_fence_after();
+        if (j < nk0) {
+          if (!(ok = issue_pv(0, j))) break;
+          if (j + 1 < nk0) issue_s(0, j + 1);
+        }
+        if (j < nk1) {
+          if (!(ok = issue_pv(1, j))) break;
+          if (j + 1 < nk1) issue_s(1, j + 1);
+        }
+        release(2 * j + 1);
+        if (next) release(2 * j + 2);
+      }
+      // Every MMA must be finished before TMEM is freed.
+      sm103::mma_commit_warp(bar(C::B_DONE));
+      __all_sync(0xffffffffu, wait_bounded(bar(C::B_DONE), 0u, ab, false));
     }
   } else if (warp < kCorrWarp0) {
     // ------------------------------------------------------------- softmax
