@@ -75,8 +75,7 @@ struct Cfg {
   static constexpr int KB = D / 64;                      // 64-column sub-tiles per tile
   static constexpr uint32_t TILE = KB * kSubTile;        // bytes of one 128 x D bf16 tile
   static constexpr int NSLOT = D == 128 ? 5 : 10;        // K/V ring slots (one tile each)
-  static constexpr uint32_t OFF_ALPHA = 1024;            // [2][128] fp32 rescale factors
-  static constexpr uint32_t OFF_Q = 2048;                // first 2 KB: barriers, flags, factors
+  static constexpr uint32_t OFF_Q = 1024;                // first 1 KB: barriers and flags
   static constexpr uint32_t OFF_KV = OFF_Q + 2 * TILE;
   static constexpr uint32_t USED = OFF_KV + NSLOT * TILE;
   static constexpr uint32_t SMEM = USED + 1024;          // + slack to align the base to 1 KB
@@ -84,8 +83,8 @@ struct Cfg {
   // barrier slots
   static constexpr int B_Q = 0, B_FULL = 1, B_EMPTY = 1 + NSLOT;
   static constexpr int B_SF = 1 + 2 * NSLOT;  // [2] scores of tile i ready (MMA commit)
-  static constexpr int B_PF = B_SF + 2;       // [2][2] half h of P_i in TMEM (128 softmax threads)
-  static constexpr int B_AR = B_PF + 4;       // [2] rescale factor (shared) / final 1/l (TMEM) (128 softmax threads)
+  static constexpr int B_PF = B_SF + 2;       // [2] P of tile i in TMEM (128 softmax threads)
+  static constexpr int B_AR = B_PF + 2;       // [2] rescale factor / final 1/l in TMEM (128 softmax threads)
   static constexpr int B_OR = B_AR + 2;       // [2] O of tile i rescaled (128 correction threads)
   static constexpr int B_OF = B_OR + 2;       // [2] O_i += P_i V_j finished (MMA commit)
   static constexpr int B_DONE = B_OF + 2;
@@ -94,7 +93,7 @@ struct Cfg {
   // TMEM columns
   static constexpr uint32_t COL_S = 0;     // S_i at COL_S + 128 i (P_i over its first 64 columns)
   static constexpr uint32_t COL_O = 256;   // O_i at COL_O + D i
-  static constexpr uint32_t COL_INVL = 65;  // inside S_i, above P_i
+  static constexpr uint32_t COL_ALPHA = 64, COL_INVL = 65;  // inside S_i, above P_i
 };
 
 __device__ int g_attn_status;  // 0 or kStatusTimeout; read and cleared by the host
@@ -129,27 +128,6 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const A
   return __all_sync(0xffffffffu, wait_bounded(bar, parity, ab));
 }
 
-// Polling version for the MMA warp, whose reaction time is on the critical
-// path: no suspend hint (one polling warp costs the others little issue time).
-__device__ __forceinline__ bool warp_wait_poll(uint32_t bar, uint32_t parity, const Abort& ab) {
-  bool ok = sm103::mbar_try_wait(bar, parity);
-  if (!ok) {
-    const long long t0 = clock64();
-    for (uint32_t it = 1;; ++it) {
-      if ((ok = sm103::mbar_try_wait(bar, parity))) break;
-      if ((it & 63u) == 0) {
-        if (*ab.flag) break;
-        if (clock64() - t0 > ab.limit) {
-          atomicCAS(&g_attn_status, 0, kStatusTimeout);
-          *ab.flag = 1u;
-          break;
-        }
-      }
-    }
-  }
-  return __all_sync(0xffffffffu, ok);
-}
-
 template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 1) attn_fwd_sm103(const __grid_constant__ FwdParams p) {
   using C = Cfg<D>;
@@ -162,7 +140,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_sm103(const __grid_const
   uint8_t* const sbase = smem_raw + (base - raw);
   uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(sbase + 512);
   volatile uint32_t* const abort_flag = reinterpret_cast<volatile uint32_t*>(sbase + 516);
-  float* const alpha_smem = reinterpret_cast<float*>(sbase + C::OFF_ALPHA);  // [tile][row]
   const uint32_t sQ = base + C::OFF_Q;   // Q_i at sQ + i * TILE (later: O_i staging)
   const uint32_t sKV = base + C::OFF_KV; // slot s at sKV + s * TILE
   auto bar = [base](int i) { return base + 8u * uint32_t(i); };
@@ -191,7 +168,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_sm103(const __grid_const
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::NBAR; ++i) {
       uint32_t cnt = 1;
-      if (i >= C::B_PF && i < C::B_OR + 2) cnt = BM;  // P, factor and O-ready barriers: 128 threads
+      if (i >= C::B_PF && i < C::B_OR + 2) cnt = BM;  // P, alpha and O-ready barriers: 128 threads
       sm103::mbar_init(bar(i), cnt);
     }
     *abort_flag = 0u;
@@ -252,7 +229,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_sm103(const __grid_const
       const uint64_t desc_k = sm103::sdesc_sw128(sKV, 16, 1024);        // K-major K slots
       const uint64_t desc_v = sm103::sdesc_sw128(sKV, kSubTile, 1024);  // MN-major V slots
       auto slot_off = [](int c) { return uint64_t(uint32_t(c % NSLOT) * (C::TILE >> 4)); };
-      auto wait_full = [&](int c) { return warp_wait_poll(bar(C::B_FULL + c % NSLOT), uint32_t(c / NSLOT) & 1u, ab); };
+      auto wait_full = [&](int c) { return warp_wait(bar(C::B_FULL + c % NSLOT), uint32_t(c / NSLOT) & 1u, ab); };
       auto release = [&](int c) { sm103::mma_commit_warp(bar(C::B_EMPTY + c % NSLOT)); };
       auto issue_s = [&](int i, int j) {
         const uint64_t dk = desc_k + slot_off(2 * j), dq = desc_q + uint64_t(uint32_t(i) * (C::TILE >> 4));
@@ -265,26 +242,19 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_sm103(const __grid_const
         sm103::mma_commit_warp(bar(C::B_SF + i));
       };
       auto issue_pv = [&](int i, int j) -> bool {
-        // P_i arrives in two halves of 64 keys; the first four MMAs start on the
-        // first half while the softmax warps still compute the second.
-        if (!warp_wait_poll(bar(C::B_PF + 2 * i), uint32_t(j) & 1u, ab)) return false;
-        if (j > 0 && !warp_wait_poll(bar(C::B_OR + i), uint32_t(j - 1) & 1u, ab)) return false;
+        if (!warp_wait(bar(C::B_PF + i), uint32_t(j) & 1u, ab)) return false;
+        if (j > 0 && !warp_wait(bar(C::B_OR + i), uint32_t(j - 1) & 1u, ab)) return false;
         sm103::tc_fence_after();
         const uint64_t dv = desc_v + slot_off(2 * j + 1);
         const uint32_t aP = tmem + C::COL_S + uint32_t(i) * BN;
         const uint32_t dO = tmem + C::COL_O + uint32_t(i) * D;
 #pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk) {  // 16 keys per MMA: 8 TMEM columns of P, 16 rows of V
-          if (kk == BN / 32) {
-            if (!warp_wait_poll(bar(C::B_PF + 2 * i + 1), uint32_t(j) & 1u, ab)) return false;
-            sm103::tc_fence_after();
-          }
+        for (int kk = 0; kk < BN / 16; ++kk)  // 16 keys per MMA: 8 TMEM columns of P, 16 rows of V
           sm103::mma_ts_warp(dO, aP + kk * 8, dv + uint64_t(kk * (2048 >> 4)), kIdescO, (j > 0 || kk > 0) ? 1u : 0u);
-        }
         sm103::mma_commit_warp(bar(C::B_OF + i));
         return true;
       };
-      bool ok = warp_wait_poll(bar(C::B_Q), 0u, ab) && wait_full(0);
+      bool ok = warp_wait(bar(C::B_Q), 0u, ab) && wait_full(0);
       if (ok) {
         sm103::tc_fence_after();
         issue_s(0, 0);
@@ -292,17 +262,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_sm103(const __grid_const
         release(0);
       }
       for (int j = 0; ok && j < nk; ++j) {
-        // Each MMA group waits only for its own operands: V_j for the PV
-        // products, K_{j+1} for the next scores.
         const bool next = j + 1 < nk;
+        if (next && !(ok = wait_full(2 * j + 2))) break;
         if (!(ok = wait_full(2 * j + 1))) break;
         sm103::tc_fence_after();
-        if (j < nk0 && !(ok = issue_pv(0, j))) break;
-        if (next) {
-          if (!(ok = wait_full(2 * j + 2))) break;
-          sm103::tc_fence_after();
+        if (j < nk0) {
+          if (!(ok = issue_pv(0, j))) break;
+          if (j + 1 < nk0) issue_s(0, j + 1);
         }
-        if (j + 1 < nk0) issue_s(0, j + 1);
         if (j < nk1) {
           if (!(ok = issue_pv(1, j))) break;
           if (j + 1 < nk1) issue_s(1, j + 1);
@@ -332,43 +299,33 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_sm103(const __grid_const
       for (int j = 0; j < nki; ++j) {
         if (!(ok = warp_wait(bar(C::B_SF + i), uint32_t(j) & 1u, ab))) break;
         sm103::tc_fence_after();
-        // Scores: the second half's TMEM load overlaps the first half's max.
-        uint32_t u0[BN / 2], u1[BN / 2];
-        sm103::tmem_ld64(tS, u0);
-        sm103::tmem_ld64_async(tS + BN / 2, u1);
+        float s[BN];
+        {
+          uint32_t u[BN];
+          sm103::tmem_ld128(tS, u);
+#pragma unroll
+          for (int c = 0; c < BN; ++c) s[c] = __uint_as_float(u[c]);
+        }
         // Masks: keys past N, and keys after the query row when causal.
         int lim = min(BN - 1, p.N - 1 - j * BN);
         if (CAUSAL) lim = min(lim, row - j * BN);
-        float s[BN];
+        if (lim < BN - 1) {
 #pragma unroll
-        for (int c = 0; c < BN / 2; ++c) s[c] = __uint_as_float(u0[c]);
-        if (lim < BN / 2 - 1) {
-#pragma unroll
-          for (int c = 0; c < BN / 2; ++c) s[c] = c > lim ? -INFINITY : s[c];
+          for (int c = 0; c < BN; ++c) s[c] = c > lim ? -INFINITY : s[c];
         }
         float mx0 = sm103::max3(s[0], s[1], s[2]);
         float mx1 = sm103::max3(s[3], s[4], s[5]);
+        float mx2 = sm103::max3(s[6], s[7], s[8]);
+        float mx3 = sm103::max3(s[9], s[10], s[11]);
 #pragma unroll
-        for (int c = 6; c + 4 <= BN / 2 - 2; c += 4) {
+        for (int c = 12; c + 8 <= BN - 4; c += 8) {
           mx0 = sm103::max3(mx0, s[c], s[c + 1]);
           mx1 = sm103::max3(mx1, s[c + 2], s[c + 3]);
+          mx2 = sm103::max3(mx2, s[c + 4], s[c + 5]);
+          mx3 = sm103::max3(mx3, s[c + 6], s[c + 7]);
         }
-        mx0 = sm103::max3(mx0, s[BN / 2 - 2], s[BN / 2 - 1]);
-        sm103::tmem_wait_ld64(u1);
-#pragma unroll
-        for (int c = 0; c < BN / 2; ++c) s[BN / 2 + c] = __uint_as_float(u1[c]);
-        if (lim < BN - 1) {
-#pragma unroll
-          for (int c = BN / 2; c < BN; ++c) s[c] = c > lim ? -INFINITY : s[c];
-        }
-        float mx2 = sm103::max3(s[BN / 2], s[BN / 2 + 1], s[BN / 2 + 2]);
-        float mx3 = sm103::max3(s[BN / 2 + 3], s[BN / 2 + 4], s[BN / 2 + 5]);
-#pragma unroll
-        for (int c = BN / 2 + 6; c + 4 <= BN - 2; c += 4) {
-          mx2 = sm103::max3(mx2, s[c], s[c + 1]);
-          mx3 = sm103::max3(mx3, s[c + 2], s[c + 3]);
-        }
-        mx2 = sm103::max3(mx2, s[BN - 2], s[BN - 1]);
+        mx0 = sm103::max3(mx0, s[BN - 4], s[BN - 3]);
+        mx1 = sm103::max3(mx1, s[BN - 2], s[BN - 1]);
         const float cand = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
         float alpha = 1.f;
         if (j == 0) {
@@ -379,7 +336,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_sm103(const __grid_const
             m_ref = cand;
           }
           // Hand alpha to the correction warps now, so O is rescaled while the exps run.
-          alpha_smem[i * BM + r] = alpha;
+          sm103::tmem_st1(tS + C::COL_ALPHA, __float_as_uint(alpha));
+          sm103::tmem_st_wait();
+          sm103::tc_fence_before();
           sm103::mbar_arrive(bar(C::B_AR + i));
         }
         const uint64_t negm = sm103::f2_pack(-m_ref, -m_ref);
@@ -401,18 +360,15 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_sm103(const __grid_const
               acc0 = sm103::f2_add(acc0, sm103::f2_pack(p0, p1));
           }
           sm103::tmem_st16(tS + q * 16, pk);  // P over the first 64 columns of S_i
-          if (q == BN / 64 - 1 || q == BN / 32 - 1) {
-            // Half of P is in TMEM: let the MMA warp start on it.
-            sm103::tmem_st_wait();
-            sm103::tc_fence_before();
-            sm103::mbar_arrive(bar(C::B_PF + 2 * i + (q == BN / 32 - 1 ? 1 : 0)));
-          }
         }
         float a0, a1, a2, a3;
         sm103::f2_unpack(acc0, a0, a1);
         sm103::f2_unpack(acc1, a2, a3);
         const float rowsum = (a0 + a1) + (a2 + a3);
         l_run = j == 0 ? rowsum : fmaf(alpha, l_run, rowsum);
+        sm103::tmem_st_wait();
+        sm103::tc_fence_before();
+        sm103::mbar_arrive(bar(C::B_PF + i));
       }
       if (ok) {
         // 1/l for the correction warps' epilogue; LSE from here.
@@ -432,9 +388,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_sm103(const __grid_const
     for (int j = 1; ok && j < nk; ++j) {
       for (int i = 0; i < T; ++i) {
         if (j >= (i == 0 ? nk0 : nk1)) continue;
+        const uint32_t tS = tmem + lane_off + C::COL_S + uint32_t(i) * BN;
         const uint32_t tO = tmem + lane_off + C::COL_O + uint32_t(i) * D;
         if (!(ok = warp_wait(bar(C::B_AR + i), uint32_t(j - 1) & 1u, ab))) break;
-        const float alpha = alpha_smem[i * BM + r];
+        sm103::tc_fence_after();
+        const float alpha = __uint_as_float(sm103::tmem_ld1(tS + C::COL_ALPHA));
         if (!(ok = warp_wait(bar(C::B_OF + i), uint32_t(j - 1) & 1u, ab))) break;
         sm103::tc_fence_after();
         if (__any_sync(0xffffffffu, alpha != 1.f)) {
