@@ -94,12 +94,11 @@ bool ranges_overlap(const void* a, uint64_t na, const void* b, uint64_t nb) {
 
 long long timeout_cycles() {
   // About two seconds at the GB300 clock; no legitimate wait comes near it.
-  static const long long v = [] {
-    const char* e = std::getenv("ATTN_WAIT_LIMIT_CYCLES");
-    const long long x = e ? std::atoll(e) : 0;
-    return x > 0 ? x : (1LL << 32);
-  }();
-  return v;
+  // ATTN_WAIT_LIMIT_CYCLES (read at every call) lowers it, e.g. to test the
+  // timeout path.
+  const char* e = std::getenv("ATTN_WAIT_LIMIT_CYCLES");
+  const long long x = e ? std::atoll(e) : 0;
+  return x > 0 ? x : (1LL << 32);
 }
 
 template <int D, bool CAUSAL>

@@ -53,8 +53,8 @@ constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleLog2 = 8.0f;        // move the reference max only when it grows by > 2^8
 constexpr int kStatusTimeout = 4;           // value of ATTN_ERR_TIMEOUT
 // Register split (setmaxnreg): 2 x 128 softmax threads at 176, 128 correction
-// threads at 80, 128 load/MMA/idle threads at 80 = 65536 = 512 threads x 128.
-constexpr uint32_t kRegSoftmax = 176, kRegCorr = 80, kRegOther = 80;
+// threads at 88, 128 load/MMA/idle threads at 72 = 65536 = 512 threads x 128.
+constexpr uint32_t kRegSoftmax = 176, kRegCorr = 88, kRegOther = 72;
 static_assert(2 * 128 * kRegSoftmax + 128 * kRegCorr + 128 * kRegOther == kThreads * 128, "register split");
 
 struct FwdParams {
@@ -100,22 +100,31 @@ __device__ int g_attn_status;  // 0 or kStatusTimeout; read and cleared by the h
 
 struct Abort {
   volatile uint32_t* flag;
-  long long limit;
+  long long limit;  // cycles a wait may take before it reports a timeout
 };
 
+// Drains (copies in flight, MMAs before TMEM is freed) always get this long:
+// they wait on work that completes by itself, so it never runs out in practice.
+constexpr long long kDrainCycles = 1LL << 31;
+
 // Wait for an mbarrier phase, bounded.  Each try suspends the thread until the
-// phase completes or about a millisecond passes; between tries the wait gives
-// up when another role aborted (if honour_abort) or when `limit` cycles have
-// passed, the latter recording a timeout.
+// phase completes or the suspend hint passes; between tries the wait gives up
+// when another role aborted or when the limit has passed, the latter recording
+// a timeout.  A drain (honour_abort = false) ignores the abort flag and uses
+// at least kDrainCycles.
 constexpr uint32_t kSuspendNs = 1000000;
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, const Abort& ab,
                                              bool honour_abort = true) {
   if (sm103::mbar_try_wait(bar, parity)) return true;
+  const long long limit = honour_abort ? ab.limit : (ab.limit > kDrainCycles ? ab.limit : kDrainCycles);
+  // Suspend hint per try: 1 ms, or about a quarter of a shorter limit.
+  const uint32_t sleep_ns =
+      (!honour_abort || (limit >> 2) >= kSuspendNs) ? kSuspendNs : uint32_t((limit >> 2) < 32 ? 32 : (limit >> 2));
   const long long t0 = clock64();
   for (;;) {
-    if (sm103::mbar_try_wait_sleep(bar, parity, kSuspendNs)) return true;
+    if (sm103::mbar_try_wait_sleep(bar, parity, sleep_ns)) return true;
     if (honour_abort && *ab.flag) return false;
-    if (clock64() - t0 > ab.limit) {
+    if (clock64() - t0 > limit) {
       atomicCAS(&g_attn_status, 0, kStatusTimeout);
       *ab.flag = 1u;
       return false;
