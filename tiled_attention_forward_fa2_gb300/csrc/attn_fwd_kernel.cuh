@@ -113,10 +113,25 @@ constexpr long long kDrainCycles = 1LL << 31;
 // a timeout.  A drain (honour_abort = false) ignores the abort flag and uses
 // at least kDrainCycles.
 constexpr uint32_t kSuspendNs = 1000000;
+constexpr long long kPollBelowCycles = 1LL << 20;
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, const Abort& ab,
                                              bool honour_abort = true) {
-  if (sm103::mbar_try_wait(bar, parity)) return true;
+  if (sm103::mbar_test_wait(bar, parity)) return true;
   const long long limit = honour_abort ? ab.limit : (ab.limit > kDrainCycles ? ab.limit : kDrainCycles);
+  if (limit < kPollBelowCycles) {
+    // A short limit (set to exercise the timeout path): poll without suspending
+    // so the limit is checked at once.
+    const long long t0 = clock64();
+    for (;;) {
+      if (sm103::mbar_test_wait(bar, parity)) return true;
+      if (honour_abort && *ab.flag) return false;
+      if (clock64() - t0 > limit) {
+        atomicCAS(&g_attn_status, 0, kStatusTimeout);
+        *ab.flag = 1u;
+        return false;
+      }
+    }
+  }
   // Suspend hint per try: 1 ms, or about a quarter of a shorter limit.
   const uint32_t sleep_ns =
       (!honour_abort || (limit >> 2) >= kSuspendNs) ? kSuspendNs : uint32_t((limit >> 2) < 32 ? 32 : (limit >> 2));
