@@ -1,11 +1,12 @@
 """Failure detection on the GPU without faulting it.
 
-Every pipeline wait in the kernel is bounded.  Lowering the bound to a few
-dozen cycles (ATTN_WAIT_LIMIT_CYCLES) makes the waits run out in a normal
-launch: the kernel must record ATTN_ERR_TIMEOUT for attn_last_status, drain
-its in-flight copies and MMAs, free its tensor memory and return, leaving the
-device usable for the next, normal call.  Nothing here traps, hangs or touches
-memory out of bounds.
+Every pipeline wait in the kernel is bounded.  The test hook
+ATTN_TEST_WITHHOLD_KV=1 makes the kernel issue no K/V loads, so the waits for
+them can never complete; with the bound lowered to about a millisecond
+(ATTN_WAIT_LIMIT_CYCLES) the kernel must record ATTN_ERR_TIMEOUT for
+attn_last_status, drain its in-flight copies and MMAs, free its tensor memory
+and return, leaving the device usable for the next, normal call.  Nothing here
+traps, hangs or touches memory out of bounds.
 """
 import numpy as np
 import pytest
@@ -37,12 +38,14 @@ def test_wait_timeout_is_reported_and_device_stays_usable(tiles, monkeypatch):
     lse = torch.empty((B, H, N), device="cuda")
     s = torch.cuda.current_stream()
 
-    monkeypatch.setenv("ATTN_WAIT_LIMIT_CYCLES", "64")
+    monkeypatch.setenv("ATTN_WAIT_LIMIT_CYCLES", "2000000")
+    monkeypatch.setenv("ATTN_TEST_WITHHOLD_KV", "1")
     assert pkg.attn_fwd(qd, kd, vd, o, lse, B, H, N, D, True, 0.125, s) == pkg.ATTN_OK
     assert pkg.attn_last_status(s) == pkg.ATTN_ERR_TIMEOUT
     assert pkg.attn_last_status(s) == pkg.ATTN_OK  # reading the status clears it
 
     monkeypatch.delenv("ATTN_WAIT_LIMIT_CYCLES")
+    monkeypatch.delenv("ATTN_TEST_WITHHOLD_KV")
     assert pkg.attn_fwd(qd, kd, vd, o, lse, B, H, N, D, True, 0.125, s) == pkg.ATTN_OK
     assert pkg.attn_last_status(s) == pkg.ATTN_OK
     o_ref, lse_ref = oracle.attn_fwd(q, k, v, True, 0.125)

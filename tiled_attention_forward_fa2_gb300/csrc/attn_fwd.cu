@@ -164,6 +164,11 @@ attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, flo
   prm.n_units = int((n_tiles + T - 1) / T);
   prm.scale_log2 = scale * 1.4426950408889634f;
   prm.timeout_cycles = timeout_cycles();
+  // Test hook for the timeout path: ATTN_TEST_WITHHOLD_KV=1 makes the kernel
+  // issue no K/V loads, so its pipeline waits run out and it reports
+  // ATTN_ERR_TIMEOUT (use with a lowered ATTN_WAIT_LIMIT_CYCLES).
+  const char* wh = std::getenv("ATTN_TEST_WITHHOLD_KV");
+  prm.withhold_kv = (wh && wh[0] == '1') ? 1 : 0;
 
   const int64_t ctas = int64_t(prm.n_units) * BH;
   const cudaStream_t st = static_cast<cudaStream_t>(stream);

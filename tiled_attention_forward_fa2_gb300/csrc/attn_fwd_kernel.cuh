@@ -53,8 +53,8 @@ constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleLog2 = 8.0f;        // move the reference max only when it grows by > 2^8
 constexpr int kStatusTimeout = 4;           // value of ATTN_ERR_TIMEOUT
 // Register split (setmaxnreg): 2 x 128 softmax threads at 176, 128 correction
-// threads at 88, 128 load/MMA/idle threads at 72 = 65536 = 512 threads x 128.
-constexpr uint32_t kRegSoftmax = 176, kRegCorr = 88, kRegOther = 72;
+// threads at 80, 128 load/MMA/idle threads at 80 = 65536 = 512 threads x 128.
+constexpr uint32_t kRegSoftmax = 176, kRegCorr = 80, kRegOther = 80;
 static_assert(2 * 128 * kRegSoftmax + 128 * kRegCorr + 128 * kRegOther == kThreads * 128, "register split");
 
 struct FwdParams {
@@ -67,6 +67,7 @@ struct FwdParams {
   int n_units;                 // ceil(n_tiles / T): CTAs per (batch, head)
   float scale_log2;            // scale * log2(e)
   long long timeout_cycles;
+  int withhold_kv;             // test hook: nonzero -> no K/V loads are issued, so the pipeline waits run out
 };
 
 template <int D>
@@ -100,49 +101,39 @@ __device__ int g_attn_status;  // 0 or kStatusTimeout; read and cleared by the h
 
 struct Abort {
   volatile uint32_t* flag;
-  long long limit;  // cycles a wait may take before it reports a timeout
+  long long limit;
 };
 
-// Drains (copies in flight, MMAs before TMEM is freed) always get this long:
-// they wait on work that completes by itself, so it never runs out in practice.
-constexpr long long kDrainCycles = 1LL << 31;
-
 // Wait for an mbarrier phase, bounded.  Each try suspends the thread until the
-// phase completes or the suspend hint passes; between tries the wait gives up
-// when another role aborted or when the limit has passed, the latter recording
-// a timeout.  A drain (honour_abort = false) ignores the abort flag and uses
-// at least kDrainCycles.
+// phase completes or about a millisecond passes; between tries the wait gives
+// up when another role aborted (if honour_abort) or when `limit` cycles have
+// passed, the latter recording a timeout.
 constexpr uint32_t kSuspendNs = 1000000;
-constexpr long long kPollBelowCycles = 1LL << 20;
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, const Abort& ab,
                                              bool honour_abort = true) {
-  if (sm103::mbar_test_wait(bar, parity)) return true;
-  const long long limit = honour_abort ? ab.limit : (ab.limit > kDrainCycles ? ab.limit : kDrainCycles);
-  if (limit < kPollBelowCycles) {
-    // A short limit (set to exercise the timeout path): poll without suspending
-    // so the limit is checked at once.
-    const long long t0 = clock64();
-    for (;;) {
-      if (sm103::mbar_test_wait(bar, parity)) return true;
-      if (honour_abort && *ab.flag) return false;
-      if (clock64() - t0 > limit) {
-        atomicCAS(&g_attn_status, 0, kStatusTimeout);
-        *ab.flag = 1u;
-        return false;
-      }
-    }
-  }
-  // Suspend hint per try: 1 ms, or about a quarter of a shorter limit.
-  const uint32_t sleep_ns =
-      (!honour_abort || (limit >> 2) >= kSuspendNs) ? kSuspendNs : uint32_t((limit >> 2) < 32 ? 32 : (limit >> 2));
+  if (sm103::mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   for (;;) {
-    if (sm103::mbar_try_wait_sleep(bar, parity, sleep_ns)) return true;
+    if (sm103::mbar_try_wait_sleep(bar, parity, kSuspendNs)) return true;
     if (honour_abort && *ab.flag) return false;
-    if (clock64() - t0 > limit) {
+    if (clock64() - t0 > ab.limit) {
       atomicCAS(&g_attn_status, 0, kStatusTimeout);
       *ab.flag = 1u;
       return false;
+    }
+  }
+}
+
+// Wait on work that completes by itself (copies in flight, MMAs before TMEM is
+// freed): ignores the abort flag and allows about a second of SM cycles.
+constexpr long long kDrainCycles = 1LL << 31;
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
+  if (sm103::mbar_try_wait(bar, parity)) return;
+  const long long t0 = clock64();
+  while (!sm103::mbar_try_wait_sleep(bar, parity, kSuspendNs)) {
+    if (clock64() - t0 > kDrainCycles) {
+      atomicCAS(&g_attn_status, 0, kStatusTimeout);
+      return;
     }
   }
 }
@@ -225,7 +216,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_sm103(const __grid_const
             sm103::tma_load_3d(sQ + i * C::TILE + kb * kSubTile, &p.tq, bar(C::B_Q), kb * 64, (t0 + i) * BM, bh);
         int c = 0;  // loads issued; K_j is load 2j, V_j load 2j+1
         bool ok = true;
-        for (int j = 0; ok && j < nk; ++j) {
+        for (int j = 0; ok && !p.withhold_kv && j < nk; ++j) {
           for (int kv = 0; kv < 2; ++kv, ++c) {
             const int s = c % NSLOT;
             if (c >= NSLOT && !(ok = wait_bounded(bar(C::B_EMPTY + s), uint32_t(c / NSLOT - 1) & 1u, ab))) break;
@@ -236,9 +227,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_sm103(const __grid_const
           }
         }
         // Drain: no copy may land in shared memory after this CTA has left.
-        wait_bounded(bar(C::B_Q), 0u, ab, false);
-        for (int t = c > NSLOT ? c - NSLOT : 0; t < c; ++t)
-          wait_bounded(bar(C::B_FULL + t % NSLOT), uint32_t(t / NSLOT) & 1u, ab, false);
+        drain_wait(bar(C::B_Q), 0u);
+        for (int t = c > NSLOT ? c - NSLOT : 0; t < c; ++t) drain_wait(bar(C::B_FULL + t % NSLOT), uint32_t(t / NSLOT) & 1u);
       }
       __syncwarp();
     } else if (warp == kMmaWarp) {
@@ -303,7 +293,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_sm103(const __grid_const
       }
       // Every MMA must be finished before TMEM is freed.
       sm103::mma_commit_warp(bar(C::B_DONE));
-      __all_sync(0xffffffffu, wait_bounded(bar(C::B_DONE), 0u, ab, false));
+      drain_wait(bar(C::B_DONE), 0u);
+      __syncwarp();
     }
   } else if (warp < kCorrWarp0) {
     // ------------------------------------------------------------- softmax
