@@ -85,10 +85,14 @@ struct Cfg {
   static constexpr int B_Q = 0, B_FULL = 1, B_EMPTY = 1 + NSLOT;
   static constexpr int B_SF = 1 + 2 * NSLOT;  // [2] scores of tile i ready (MMA commit)
   static constexpr int B_PF = B_SF + 2;       // [2] P of tile i in TMEM (128 softmax threads)
-  static constexpr int B_AR = B_PF + 2;       // [2] rescale factor / final 1/l in TMEM (128 softmax threads)
+  static constexpr int B_AR = B_PF + 2;       // [2] per-step rescale factor in TMEM (128 softmax threads)
   static constexpr int B_OR = B_AR + 2;       // [2] O of tile i rescaled (128 correction threads)
   static constexpr int B_OF = B_OR + 2;       // [2] O_i += P_i V_j finished (MMA commit)
-  static constexpr int B_DONE = B_OF + 2;
+  // [2] final 1/l in TMEM (128 softmax threads).  Kept apart from B_AR: the
+  // final hand-off follows the last step's factor without waiting for the
+  // correction warps, so on one barrier it could run two phases ahead of them.
+  static constexpr int B_FIN = B_OF + 2;
+  static constexpr int B_DONE = B_FIN + 2;
   static constexpr int NBAR = B_DONE + 1;
   static_assert(NBAR * 8 <= 512, "barrier area");
   // TMEM columns
@@ -183,7 +187,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_sm103(const __grid_const
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::NBAR; ++i) {
       uint32_t cnt = 1;
-      if (i >= C::B_PF && i < C::B_OR + 2) cnt = BM;  // P, alpha and O-ready barriers: 128 threads
+      if ((i >= C::B_PF && i < C::B_OR + 2) || i == C::B_FIN || i == C::B_FIN + 1) cnt = BM;  // 128 threads
       sm103::mbar_init(bar(i), cnt);
     }
     *abort_flag = 0u;
@@ -390,7 +394,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_sm103(const __grid_const
         sm103::tmem_st1(tS + C::COL_INVL, __float_as_uint(1.f / l_run));
         sm103::tmem_st_wait();
         sm103::tc_fence_before();
-        sm103::mbar_arrive(bar(C::B_AR + i));
+        sm103::mbar_arrive(bar(C::B_FIN + i));
         if (row < p.N) p.lse[size_t(bh) * size_t(p.N) + size_t(row)] = (m_ref + log2f(l_run)) * 0.6931471805599453f;
       }
     }
@@ -432,7 +436,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_sm103(const __grid_const
       const int nki = i == 0 ? nk0 : nk1;
       const uint32_t tS = tmem + lane_off + C::COL_S + uint32_t(i) * BN;
       const uint32_t tO = tmem + lane_off + C::COL_O + uint32_t(i) * D;
-      if (ok) ok = warp_wait(bar(C::B_AR + i), uint32_t(nki - 1) & 1u, ab);
+      if (ok) ok = warp_wait(bar(C::B_FIN + i), 0u, ab);
       if (ok) ok = warp_wait(bar(C::B_OF + i), uint32_t(nki - 1) & 1u, ab);
       ok = sm103::named_bar_and(1, 128, ok);
       if (!ok) break;
