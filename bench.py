@@ -357,6 +357,21 @@ def run_ours(args, w):
     peak = float(peaks["bf16_tflops"])
     achieved = flops / (ms_per_step * 1e-3) / 1e12
     traffic = ncu_traffic(w.name)
+    # Below the ridge point (peak FLOP/s over HBM bytes/s) the kernel is bound by
+    # HBM bandwidth: algorithmic bytes = Q, K, V read + O written (bf16) + LSE (fp32).
+    alg_bytes = 8.0 * w.B * w.H * w.N * w.D + 4.0 * w.B * w.H * w.N
+    ridge = peak * 1e12 / (float(peaks["hbm_gbs"]) * 1e9)
+    if flops / alg_bytes < ridge:
+        roofline = {"bound": "hbm", "achieved": alg_bytes / (ms_per_step * 1e-3) / 1e9, "peak": float(peaks["hbm_gbs"]),
+                    "unit": "GB/s", "peak_source": f"hbm_gbs of {peak_src}"}
+    else:
+        roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                    "peak_source": f"bf16_tflops (burst) of {peak_src}"}
+    roofline["frac"] = roofline["achieved"] / roofline["peak"]
+    roofline["traffic"] = traffic
+    roofline["algorithmic_bytes"] = alg_bytes
+    roofline["flop_per_byte"] = flops / alg_bytes
+    roofline["kernel"] = f"attn_fwd_sm103<{w.D},{str(w.causal).lower()}>"
     cpu = None
     if not args.no_cpu_baseline:
         tf, secs, rows, cores = cpu_oracle_rate(w, args.cpu_seconds)
@@ -380,10 +395,7 @@ def run_ours(args, w):
             "l2": ("working set < 2x L2: 2x-L2 buffer rewritten between steps, each launch timed alone"
                    if flush else f"inputs {in_bytes / 2**20:.0f} MiB > 129 MiB L2, no flush"),
             "parallelism": f"independent replicas x{world}" if world > 1 else "single GPU"}),
-        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                     "frac": achieved / peak, "traffic": traffic,
-                     "peak_source": f"bf16_tflops (burst) of {peak_src}",
-                     "kernel": f"attn_fwd_sm103<{w.D},{str(w.causal).lower()}>"},
+        "roofline": roofline,
         "cpu_baseline": cpu,
         "e2e": {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": int(in_bytes), "d2h_bytes_per_step": int(o.numel() * 2 + lse.numel() * 4),
