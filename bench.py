@@ -58,6 +58,21 @@ def dist_env():
     return world, rank, local
 
 
+def max_over_ranks(value: float, dist_mod=None, device=None) -> float:
+    """The largest `value` over all ranks (the job is as slow as its slowest rank)."""
+    if dist_mod is None:
+        return float(value)
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist_mod.all_reduce(t, op=dist_mod.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(flops_per_rank: float, world: int, ms_per_step: float) -> float:
+    """Whole-job throughput: every rank runs its own replica, all within `ms_per_step`."""
+    return world * flops_per_rank / (ms_per_step * 1e-3) / 1e12
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -304,16 +319,13 @@ def run_ours(args, w):
     st = pkg.attn_last_status(stream)
     if st != pkg.ATTN_OK:
         raise RuntimeError(pkg.attn_status_string(st))
-    t = torch.tensor([elapsed_ms], dtype=torch.float64, device=dev)
-    if pg:
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-    elapsed_ms = float(t.item())
+    elapsed_ms = max_over_ranks(elapsed_ms, pg, dev)
     if sampler:
         sampler.stop()
 
     flops = pkg.attn_fwd_flops(w.B, w.H, w.N, w.D, w.causal)
     ms_per_step = elapsed_ms / args.steps
-    value = world * flops / (ms_per_step * 1e-3) / 1e12
+    value = job_tflops(flops, world, ms_per_step)
 
     # End to end through the C ABI with pinned host buffers.
     e2e_steps = max(3, min(args.steps, 50))
@@ -343,10 +355,7 @@ def run_ours(args, w):
     e1.record(stream)
     torch.cuda.synchronize(dev)
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
-    t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
-    if pg:
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-    e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e2e_ms, pg, dev)
 
     if rank != 0:
         if pg:
@@ -397,7 +406,7 @@ def run_ours(args, w):
             "parallelism": f"independent replicas x{world}" if world > 1 else "single GPU"}),
         "roofline": roofline,
         "cpu_baseline": cpu,
-        "e2e": {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+        "e2e": {"value": job_tflops(flops, world, e2e_ms), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": int(in_bytes), "d2h_bytes_per_step": int(o.numel() * 2 + lse.numel() * 4),
                 "ms_per_step": e2e_ms, "steps": e2e_steps},
         "gpu_launches": args.steps,
