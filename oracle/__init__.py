@@ -6,8 +6,10 @@ its Python binding) never imports, links or calls it, and it shares no code
 with that path: its arithmetic lives in ``attn_oracle.c`` (plain C, fp64),
 which is built with gcc into ``oracle/lib/liboracle_attn.so``.
 
-Every function takes Q, K, V as ``uint16`` arrays of bf16 bit patterns shaped
-[B, H, N, D] (the layout of the C ABI) and returns float64 results.
+Every function takes Q as ``uint16`` bf16 bit patterns shaped [B, H, Nq, D] and
+K, V shaped [B, H, Nk, D] (Nk = Nq for self-attention; the layout of the C
+ABI) and returns float64 results.  Causal masking is aligned at the
+bottom-right corner: key j is visible to query i iff j <= i + Nk - Nq.
 
 Pins for every function here live in ``tests/oracle_pins.py`` (closed forms,
 invariants, an independent tiled online-softmax restatement, a library
@@ -68,11 +70,11 @@ class Oracle:
     def __init__(self, libpath: str):
         lib = ctypes.CDLL(libpath)
         P, I64, I = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
-        lib.oracle_attn_fwd.argtypes = [P, P, P, P, P, I64, I64, I64, I64, I, ctypes.c_double, I]
-        lib.oracle_attn_rows.argtypes = [P, P, P, I64, I64, I64, I, ctypes.c_double, P, P, I64, P, P, I]
-        lib.oracle_attn_probs.argtypes = [P, P, P, P, P, P, I64, I64, I64, I64, I, ctypes.c_double]
+        lib.oracle_attn_fwd_qk.argtypes = [P, P, P, P, P, I64, I64, I64, I64, I64, I, ctypes.c_double, I]
+        lib.oracle_attn_rows_qk.argtypes = [P, P, P, I64, I64, I64, I64, I, ctypes.c_double, P, P, I64, P, P, I]
+        lib.oracle_attn_probs_qk.argtypes = [P, P, P, P, P, P, I64, I64, I64, I64, I64, I, ctypes.c_double]
         lib.oracle_threads.argtypes = [I]
-        for f in (lib.oracle_attn_fwd, lib.oracle_attn_rows, lib.oracle_attn_probs, lib.oracle_threads):
+        for f in (lib.oracle_attn_fwd_qk, lib.oracle_attn_rows_qk, lib.oracle_attn_probs_qk, lib.oracle_threads):
             f.restype = I
         self._lib = lib
         self.path = libpath
@@ -81,16 +83,21 @@ class Oracle:
         """OpenMP threads a call with ``nthreads`` uses (0 means all available)."""
         return self._lib.oracle_threads(nthreads)
 
+    @staticmethod
+    def _shapes(q, k, v):
+        if not (k.shape == v.shape and q.shape[:2] == k.shape[:2] and q.shape[3] == k.shape[3]):
+            raise ValueError("q [B,H,Nq,D], k and v [B,H,Nk,D] expected")
+        B, H, Nq, D = q.shape
+        return B, H, Nq, k.shape[2], D
+
     def attn_fwd(self, q, k, v, causal: bool, scale: float, nthreads: int = 0):
-        """(O [B,H,N,D] float64, LSE [B,H,N] float64) by the two-pass definition."""
+        """(O [B,H,Nq,D] float64, LSE [B,H,Nq] float64) by the two-pass definition."""
         q, k, v = _bits(q), _bits(k), _bits(v)
-        if not (q.shape == k.shape == v.shape):
-            raise ValueError("q, k, v must have one shape")
-        B, H, N, D = q.shape
-        o = np.empty((B, H, N, D), dtype=np.float64)
-        lse = np.empty((B, H, N), dtype=np.float64)
-        rc = self._lib.oracle_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, D,
-                                       int(bool(causal)), float(scale), int(nthreads))
+        B, H, Nq, Nk, D = self._shapes(q, k, v)
+        o = np.empty((B, H, Nq, D), dtype=np.float64)
+        lse = np.empty((B, H, Nq), dtype=np.float64)
+        rc = self._lib.oracle_attn_fwd_qk(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Nq, Nk, D,
+                                          int(bool(causal)), float(scale), int(nthreads))
         if rc != 0:
             raise RuntimeError("oracle_attn_fwd failed")
         return o, lse
@@ -98,7 +105,7 @@ class Oracle:
     def attn_rows(self, q, k, v, causal: bool, scale: float, bh_idx, row_idx, nthreads: int = 0):
         """O and LSE for the rows (bh_idx[r], row_idx[r]) only: shapes [R, D] and [R]."""
         q, k, v = _bits(q), _bits(k), _bits(v)
-        B, H, N, D = q.shape
+        B, H, Nq, Nk, D = self._shapes(q, k, v)
         bh = np.ascontiguousarray(bh_idx, dtype=np.int64)
         ri = np.ascontiguousarray(row_idx, dtype=np.int64)
         if bh.shape != ri.shape or bh.ndim != 1:
@@ -106,7 +113,7 @@ class Oracle:
         R = bh.shape[0]
         o = np.empty((R, D), dtype=np.float64)
         lse = np.empty((R,), dtype=np.float64)
-        rc = self._lib.oracle_attn_rows(_ptr(q), _ptr(k), _ptr(v), B * H, N, D, int(bool(causal)),
+        rc = self._lib.oracle_attn_rows_qk(_ptr(q), _ptr(k), _ptr(v), B * H, Nq, Nk, D, int(bool(causal)),
                                         float(scale), _ptr(bh), _ptr(ri), R, _ptr(o), _ptr(lse),
                                         int(nthreads))
         if rc != 0:
@@ -114,14 +121,14 @@ class Oracle:
         return o, lse
 
     def attn_probs(self, q, k, v, causal: bool, scale: float):
-        """(O, LSE, P [B,H,N,N]) for small problems; P is the softmax matrix."""
+        """(O, LSE, P [B,H,Nq,Nk]) for small problems; P is the softmax matrix."""
         q, k, v = _bits(q), _bits(k), _bits(v)
-        B, H, N, D = q.shape
-        o = np.empty((B, H, N, D), dtype=np.float64)
-        lse = np.empty((B, H, N), dtype=np.float64)
-        p = np.empty((B, H, N, N), dtype=np.float64)
-        rc = self._lib.oracle_attn_probs(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(p),
-                                         B, H, N, D, int(bool(causal)), float(scale))
+        B, H, Nq, Nk, D = self._shapes(q, k, v)
+        o = np.empty((B, H, Nq, D), dtype=np.float64)
+        lse = np.empty((B, H, Nq), dtype=np.float64)
+        p = np.empty((B, H, Nq, Nk), dtype=np.float64)
+        rc = self._lib.oracle_attn_probs_qk(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(p),
+                                            B, H, Nq, Nk, D, int(bool(causal)), float(scale))
         if rc != 0:
             raise RuntimeError("oracle_attn_probs failed")
         return o, lse, p

@@ -18,9 +18,11 @@
  *
  * Readings where the pages are silent (each listed with its reason in the
  * design notes): the scale multiplies the logits before the max and the exp;
- * causal means key j is visible to query i iff j <= i; LSE is the natural log
- * of sum_j exp(s_ij) over visible keys, i.e. m_i + log(l_i); layout is
- * [B, H, N, D] row-major with D innermost.
+ * causal means key j is visible to query i iff j <= i + (Nk - Nq) (aligned at
+ * the bottom-right corner of the score matrix, which for Nq = Nk is j <= i);
+ * LSE is the natural log of sum_j exp(s_ij) over visible keys, i.e.
+ * m_i + log(l_i); layout is [B, H, Nq, D] for Q and O, [B, H, Nk, D] for K and
+ * V, row-major with D innermost.
  *
  * Per output row (b, h, i), in this order:
  *   1. s_ij = scale * sum_d q_id k_jd           for every visible key j
@@ -29,8 +31,8 @@
  *   4. lse_i = m_i + log(l_i)
  * Every sum runs in increasing index order in double precision.  Rows are
  * independent and are spread over OpenMP threads; that changes no result.
- * A row with no visible key (impossible for square causal or full attention)
- * would give o = 0 and lse = -inf.
+ * A row with no visible key (only when causal and Nq > Nk, for the first
+ * Nq - Nk queries) gives o = 0 and lse = -inf.
  */
 #include <math.h>
 #include <stdint.h>
@@ -47,16 +49,21 @@ static double widen_bf16(uint16_t b) {
     return (double)f;
 }
 
-/* One output row.  s: scratch of N doubles; qd: scratch of D doubles; p_row:
- * optional N doubles that receive p_ij (zero for invisible keys). */
+/* One output row.  s: scratch of Nk doubles; qd: scratch of D doubles; p_row:
+ * optional Nk doubles that receive p_ij (zero for invisible keys). */
 static void attn_row(const uint16_t *q, const uint16_t *k, const uint16_t *v,
-                     int64_t N, int64_t D, int causal, double scale,
+                     int64_t Nq, int64_t Nk, int64_t D, int causal, double scale,
                      int64_t bh, int64_t i, double *s, double *qd,
                      double *o_row, double *lse_out, double *p_row) {
-    const uint16_t *qi = q + (bh * N + i) * D;
-    const uint16_t *kb = k + bh * N * D;
-    const uint16_t *vb = v + bh * N * D;
-    const int64_t n_vis = causal ? (i + 1 < N ? i + 1 : N) : N;
+    const uint16_t *qi = q + (bh * Nq + i) * D;
+    const uint16_t *kb = k + bh * Nk * D;
+    const uint16_t *vb = v + bh * Nk * D;
+    int64_t n_vis = Nk;
+    if (causal) {
+        n_vis = i + (Nk - Nq) + 1; /* keys 0 .. i + Nk - Nq */
+        if (n_vis > Nk) n_vis = Nk;
+        if (n_vis < 0) n_vis = 0;
+    }
     int64_t j, d;
 
     for (d = 0; d < D; ++d) qd[d] = widen_bf16(qi[d]);
@@ -87,7 +94,7 @@ static void attn_row(const uint16_t *q, const uint16_t *k, const uint16_t *v,
 
     for (d = 0; d < D; ++d) o_row[d] = 0.0;
     if (p_row)
-        for (j = 0; j < N; ++j) p_row[j] = 0.0;
+        for (j = 0; j < Nk; ++j) p_row[j] = 0.0;
     if (n_vis <= 0) {
         *lse_out = -INFINITY;
         return;
@@ -124,19 +131,19 @@ static int set_threads(int nthreads) {
 /* Number of OpenMP threads a call with `nthreads` would use (0 = all). */
 int oracle_threads(int nthreads) { return set_threads(nthreads); }
 
-/* Whole forward: o [B*H*N*D] and lse [B*H*N], fp64.  Returns 0, or -1 on a
- * bad argument or a failed scratch allocation. */
-int oracle_attn_fwd(const uint16_t *q, const uint16_t *k, const uint16_t *v,
-                    double *o, double *lse, int64_t B, int64_t H, int64_t N,
-                    int64_t D, int causal, double scale, int nthreads) {
-    if (!q || !k || !v || !o || !lse || B < 0 || H < 0 || N < 0 || D < 1) return -1;
-    const int64_t rows = B * H * N;
+/* Whole forward: q, o [B*H*Nq*D], k, v [B*H*Nk*D], lse [B*H*Nq], fp64.
+ * Returns 0, or -1 on a bad argument or a failed scratch allocation. */
+int oracle_attn_fwd_qk(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                       double *o, double *lse, int64_t B, int64_t H, int64_t Nq,
+                       int64_t Nk, int64_t D, int causal, double scale, int nthreads) {
+    if (!q || !k || !v || !o || !lse || B < 0 || H < 0 || Nq < 0 || Nk < 0 || D < 1) return -1;
+    const int64_t rows = B * H * Nq;
     int failed = 0;
     const int nt = set_threads(nthreads);
     (void)nt;
 #pragma omp parallel num_threads(nt) reduction(| : failed)
     {
-        double *s = (double *)malloc(sizeof(double) * (size_t)(N > 0 ? N : 1));
+        double *s = (double *)malloc(sizeof(double) * (size_t)(Nk > 0 ? Nk : 1));
         double *qd = (double *)malloc(sizeof(double) * (size_t)D);
         if (!s || !qd) {
             failed = 1;
@@ -144,7 +151,7 @@ int oracle_attn_fwd(const uint16_t *q, const uint16_t *k, const uint16_t *v,
             int64_t r;
 #pragma omp for schedule(dynamic, 16)
             for (r = 0; r < rows; ++r) {
-                attn_row(q, k, v, N, D, causal, scale, r / N, r % N, s, qd,
+                attn_row(q, k, v, Nq, Nk, D, causal, scale, r / Nq, r % Nq, s, qd,
                          o + r * D, lse + r, NULL);
             }
         }
@@ -154,20 +161,27 @@ int oracle_attn_fwd(const uint16_t *q, const uint16_t *k, const uint16_t *v,
     return failed ? -1 : 0;
 }
 
-/* Selected rows only: row r is (bh_idx[r], row_idx[r]); o [nrows*D], lse [nrows]. */
-int oracle_attn_rows(const uint16_t *q, const uint16_t *k, const uint16_t *v,
-                     int64_t BH, int64_t N, int64_t D, int causal, double scale,
-                     const int64_t *bh_idx, const int64_t *row_idx, int64_t nrows,
-                     double *o, double *lse, int nthreads) {
-    if (!q || !k || !v || !o || !lse || !bh_idx || !row_idx || N < 1 || D < 1) return -1;
+/* Square case (Nq = Nk = N): o [B*H*N*D] and lse [B*H*N]. */
+int oracle_attn_fwd(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                    double *o, double *lse, int64_t B, int64_t H, int64_t N,
+                    int64_t D, int causal, double scale, int nthreads) {
+    return oracle_attn_fwd_qk(q, k, v, o, lse, B, H, N, N, D, causal, scale, nthreads);
+}
+
+/* Selected rows only: row r is query (bh_idx[r], row_idx[r]); o [nrows*D], lse [nrows]. */
+int oracle_attn_rows_qk(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                        int64_t BH, int64_t Nq, int64_t Nk, int64_t D, int causal, double scale,
+                        const int64_t *bh_idx, const int64_t *row_idx, int64_t nrows,
+                        double *o, double *lse, int nthreads) {
+    if (!q || !k || !v || !o || !lse || !bh_idx || !row_idx || Nq < 1 || Nk < 1 || D < 1) return -1;
     for (int64_t r = 0; r < nrows; ++r)
-        if (bh_idx[r] < 0 || bh_idx[r] >= BH || row_idx[r] < 0 || row_idx[r] >= N) return -1;
+        if (bh_idx[r] < 0 || bh_idx[r] >= BH || row_idx[r] < 0 || row_idx[r] >= Nq) return -1;
     int failed = 0;
     const int nt = set_threads(nthreads);
     (void)nt;
 #pragma omp parallel num_threads(nt) reduction(| : failed)
     {
-        double *s = (double *)malloc(sizeof(double) * (size_t)N);
+        double *s = (double *)malloc(sizeof(double) * (size_t)Nk);
         double *qd = (double *)malloc(sizeof(double) * (size_t)D);
         if (!s || !qd) {
             failed = 1;
@@ -175,7 +189,7 @@ int oracle_attn_rows(const uint16_t *q, const uint16_t *k, const uint16_t *v,
             int64_t r;
 #pragma omp for schedule(dynamic, 4)
             for (r = 0; r < nrows; ++r)
-                attn_row(q, k, v, N, D, causal, scale, bh_idx[r], row_idx[r], s, qd,
+                attn_row(q, k, v, Nq, Nk, D, causal, scale, bh_idx[r], row_idx[r], s, qd,
                          o + r * D, lse + r, NULL);
         }
         free(s);
@@ -184,22 +198,38 @@ int oracle_attn_rows(const uint16_t *q, const uint16_t *k, const uint16_t *v,
     return failed ? -1 : 0;
 }
 
-/* The probability matrix as well (small problems): p [B*H*N*N], o, lse as above. */
-int oracle_attn_probs(const uint16_t *q, const uint16_t *k, const uint16_t *v,
-                      double *o, double *lse, double *p, int64_t B, int64_t H,
-                      int64_t N, int64_t D, int causal, double scale) {
-    if (!q || !k || !v || !o || !lse || !p || B < 0 || H < 0 || N < 1 || D < 1) return -1;
-    double *s = (double *)malloc(sizeof(double) * (size_t)N);
+/* Square case of oracle_attn_rows_qk. */
+int oracle_attn_rows(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                     int64_t BH, int64_t N, int64_t D, int causal, double scale,
+                     const int64_t *bh_idx, const int64_t *row_idx, int64_t nrows,
+                     double *o, double *lse, int nthreads) {
+    return oracle_attn_rows_qk(q, k, v, BH, N, N, D, causal, scale, bh_idx, row_idx, nrows, o, lse,
+                               nthreads);
+}
+
+/* The probability matrix as well (small problems): p [B*H*Nq*Nk], o, lse as above. */
+int oracle_attn_probs_qk(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                         double *o, double *lse, double *p, int64_t B, int64_t H,
+                         int64_t Nq, int64_t Nk, int64_t D, int causal, double scale) {
+    if (!q || !k || !v || !o || !lse || !p || B < 0 || H < 0 || Nq < 1 || Nk < 1 || D < 1) return -1;
+    double *s = (double *)malloc(sizeof(double) * (size_t)Nk);
     double *qd = (double *)malloc(sizeof(double) * (size_t)D);
     if (!s || !qd) {
         free(s);
         free(qd);
         return -1;
     }
-    for (int64_t r = 0; r < B * H * N; ++r)
-        attn_row(q, k, v, N, D, causal, scale, r / N, r % N, s, qd, o + r * D, lse + r,
-                 p + r * N);
+    for (int64_t r = 0; r < B * H * Nq; ++r)
+        attn_row(q, k, v, Nq, Nk, D, causal, scale, r / Nq, r % Nq, s, qd, o + r * D, lse + r,
+                 p + r * Nk);
     free(s);
     free(qd);
     return 0;
+}
+
+/* Square case of oracle_attn_probs_qk. */
+int oracle_attn_probs(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                      double *o, double *lse, double *p, int64_t B, int64_t H,
+                      int64_t N, int64_t D, int causal, double scale) {
+    return oracle_attn_probs_qk(q, k, v, o, lse, p, B, H, N, N, D, causal, scale);
 }

@@ -261,13 +261,17 @@ def decimal_attention(q, k, v, causal, scale, digits=50):
     Dec = decimal.Decimal
     Q, K, V = bf16_bits_to_f64(q), bf16_bits_to_f64(k), bf16_bits_to_f64(v)
     B, H, N, D = Q.shape
+    Nk = K.shape[2]
     sc = Dec(float(scale))
     O = np.zeros((B, H, N, D))
     LSE = np.zeros((B, H, N))
     for b in range(B):
         for h in range(H):
             for i in range(N):
-                n = i + 1 if causal else N
+                n = max(0, min(Nk, i + 1 + Nk - N)) if causal else Nk
+                if n == 0:
+                    LSE[b, h, i] = -np.inf
+                    continue
                 s = []
                 for j in range(n):
                     acc = Dec(0)
@@ -298,6 +302,76 @@ def check_decimal_brute_force(orc):
         _close(lse, lse_d, 1e-14, "LSE vs 50-digit brute force")
 
 
+# ------------------------------------------------ queries and keys of different lengths
+
+def check_causal_suffix_is_bottom_right(orc):
+    """A causal query block that ends with the keys sees exactly what the same rows
+    of the square causal problem see: rows N-Nq.. of causal(Q, K, V) equal
+    causal(Q[N-Nq:], K, V).  This pins the bottom-right alignment on the square case."""
+    B, H, N, D = 1, 2, 90, 16
+    q, k, v = make_qkv(B, H, N, D, seed=61)
+    o_sq, l_sq = orc.attn_fwd(q, k, v, True, 0.3)
+    for nq in (1, 7, 37, 90):
+        o_r, l_r = orc.attn_fwd(q[:, :, N - nq:], k, v, True, 0.3)
+        assert np.array_equal(o_r, o_sq[:, :, N - nq:]) and np.array_equal(l_r, l_sq[:, :, N - nq:]), \
+            f"causal Nq={nq}, Nk={N}: not the last rows of the square problem"
+
+
+def check_full_rows_depend_on_their_query_only(orc):
+    """Without the mask each query row is independent: any block of queries gives
+    the same rows as the square problem that contains it."""
+    B, H, N, D = 1, 2, 70, 8
+    q, k, v = make_qkv(B, H, N, D, seed=62)
+    o_sq, l_sq = orc.attn_fwd(q, k, v, False, 0.25)
+    for a, b in ((0, 1), (5, 40), (69, 70)):
+        o_r, l_r = orc.attn_fwd(q[:, :, a:b], k, v, False, 0.25)
+        assert np.array_equal(o_r, o_sq[:, :, a:b]) and np.array_equal(l_r, l_sq[:, :, a:b])
+
+
+def check_more_queries_than_keys_causal(orc):
+    """Causal with Nq > Nk: the first Nq - Nk queries see no key (O = 0, LSE = -inf);
+    the others are the square causal problem on the last Nk queries."""
+    B, H, Nq, Nk, D = 1, 2, 50, 30, 8
+    q, _, _ = make_qkv(B, H, Nq, D, seed=63)
+    _, k, v = make_qkv(B, H, Nk, D, seed=64)
+    o, lse = orc.attn_fwd(q, k, v, True, 0.4)
+    assert np.all(o[:, :, : Nq - Nk] == 0.0) and np.all(np.isneginf(lse[:, :, : Nq - Nk]))
+    o_sq, l_sq = orc.attn_fwd(q[:, :, Nq - Nk:], k, v, True, 0.4)
+    assert np.array_equal(o[:, :, Nq - Nk:], o_sq) and np.array_equal(lse[:, :, Nq - Nk:], l_sq)
+
+
+def check_rectangular_against_torch_mask(orc):
+    import torch
+
+    for (Nq, Nk, causal) in [(33, 100, True), (100, 33, False), (1, 77, True), (64, 64, True)]:
+        B, H, D = 1, 2, 32
+        q, _, _ = make_qkv(B, H, Nq, D, seed=70 + Nq)
+        _, k, v = make_qkv(B, H, Nk, D, seed=71 + Nk)
+        scale = float(np.float32(1.0 / math.sqrt(D)))
+        o, lse = orc.attn_fwd(q, k, v, causal, scale)
+        Q, K, V = (torch.from_numpy(bf16_bits_to_f64(x)) for x in (q, k, v))
+        visible = torch.ones(Nq, Nk, dtype=torch.bool)
+        if causal:
+            visible = torch.arange(Nk)[None, :] <= torch.arange(Nq)[:, None] + (Nk - Nq)
+        with torch.no_grad():
+            o_t = torch.nn.functional.scaled_dot_product_attention(Q, K, V, attn_mask=visible, scale=scale)
+            lse_t = torch.logsumexp((scale * (Q @ K.transpose(-1, -2))).masked_fill(~visible, float("-inf")), dim=-1)
+        _close(o, o_t.numpy(), TIGHT, f"O vs torch SDPA with mask (Nq={Nq}, Nk={Nk})")
+        _close(lse, lse_t.numpy(), TIGHT, f"LSE vs torch logsumexp (Nq={Nq}, Nk={Nk})")
+
+
+def check_rectangular_decimal(orc):
+    for (Nq, Nk, causal, seed) in [(3, 8, True, 81), (8, 3, False, 82), (6, 4, True, 83)]:
+        q, _, _ = make_qkv(1, 1, Nq, 4, seed=seed)
+        _, k, v = make_qkv(1, 1, Nk, 4, seed=seed + 100)
+        o, lse = orc.attn_fwd(q, k, v, causal, 0.5)
+        o_d, lse_d = decimal_attention(q, k, v, causal, 0.5)
+        fin = np.isfinite(lse_d)
+        _close(o, o_d, 1e-14, f"O vs 50-digit brute force (Nq={Nq}, Nk={Nk})")
+        assert np.array_equal(np.isfinite(lse), fin)
+        _close(lse[fin], lse_d[fin], 1e-14, f"LSE vs 50-digit brute force (Nq={Nq}, Nk={Nk})")
+
+
 ALL_CHECKS = [
     check_prob_rows_sum_to_one,
     check_o_is_p_times_v,
@@ -312,4 +386,9 @@ ALL_CHECKS = [
     check_rows_match_full,
     check_matches_torch_sdpa,
     check_decimal_brute_force,
+    check_causal_suffix_is_bottom_right,
+    check_full_rows_depend_on_their_query_only,
+    check_more_queries_than_keys_causal,
+    check_rectangular_against_torch_mask,
+    check_rectangular_decimal,
 ]

@@ -18,15 +18,16 @@ MUTANTS = {
                       ("s[j + 2] = scale * a2;", "s[j + 2] = a2;"),
                       ("s[j + 3] = scale * a3;", "s[j + 3] = a3;"),
                       ("s[j] = scale * a;", "s[j] = a;")],
-    "causal_excludes_diagonal": [("causal ? (i + 1 < N ? i + 1 : N) : N", "causal ? (i < N ? i : N) : N")],
+    "causal_excludes_diagonal": [("n_vis = i + (Nk - Nq) + 1;", "n_vis = i + (Nk - Nq);")],
+    "causal_top_left_alignment": [("n_vis = i + (Nk - Nq) + 1;", "n_vis = i + 1;")],
     "exp_sign_flipped": [("const double p = exp(s[j] - m) / l;", "const double p = exp(m - s[j]) / l;")],
     "lse_without_max": [("*lse_out = m + log(l);", "*lse_out = log(l);")],
     "sum_drops_first_key": [("for (j = 0; j < n_vis; ++j) l += exp(s[j] - m);",
                              "for (j = 1; j < n_vis; ++j) l += exp(s[j] - m);")],
-    "v_transposed": [("o_row[d] += p * widen_bf16(vj[d]);", "o_row[d] += p * widen_bf16(vb[d * N + j]);")],
-    "wrong_query_row": [("const uint16_t *qi = q + (bh * N + i) * D;",
-                         "const uint16_t *qi = q + (bh * N + (N - 1 - i)) * D;")],
-    "keys_of_head_zero": [("const uint16_t *kb = k + bh * N * D;", "const uint16_t *kb = k;")],
+    "v_transposed": [("o_row[d] += p * widen_bf16(vj[d]);", "o_row[d] += p * widen_bf16(vb[d * Nk + j]);")],
+    "wrong_query_row": [("const uint16_t *qi = q + (bh * Nq + i) * D;",
+                         "const uint16_t *qi = q + (bh * Nq + (Nq - 1 - i)) * D;")],
+    "keys_of_head_zero": [("const uint16_t *kb = k + bh * Nk * D;", "const uint16_t *kb = k;")],
     "last_dim_dropped": [("for (d = 0; d < D; ++d) {\n            a0", "for (d = 0; d + 1 < D; ++d) {\n            a0")],
 }
 
