@@ -184,7 +184,7 @@ def cpu_oracle_rate(w, budget_s: float, rows_cap: int | None = None, seed: int =
         return bh, ri
 
     def flops(ri):
-        vis = (ri + 1) if w.causal else np.full(ri.shape, w.N)
+        vis = np.minimum(ri + 1 + w.n_keys - w.N, w.n_keys) if w.causal else np.full(ri.shape, w.n_keys)
         return float(4.0 * w.D * vis.sum())
 
     bh, ri = sample(64)
@@ -217,7 +217,7 @@ def run_reference(args, w):
     rows = int(max(8, min(4096, 60.0 / (args.steps + args.warmup) / per_row)))
     bh = rng.integers(0, w.B * w.H, rows).astype(np.int64)
     ri = rng.integers(0, w.N, rows).astype(np.int64)
-    vis = (ri + 1) if w.causal else np.full(ri.shape, w.N)
+    vis = np.minimum(ri + 1 + w.n_keys - w.N, w.n_keys) if w.causal else np.full(ri.shape, w.n_keys)
     step_flops = float(4.0 * w.D * vis.sum())
     for _ in range(args.warmup):
         oracle.attn_rows(q, k, v, w.causal, w.scale, bh, ri)
@@ -240,7 +240,7 @@ def run_reference(args, w):
 
 
 def workload_config(w, extra=None):
-    cfg = {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "D": w.D, "causal": w.causal, "seed": w.seed,
+    cfg = {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "Nk": w.n_keys, "D": w.D, "causal": w.causal, "seed": w.seed,
            "q_std": w.q_std, "scale": w.scale, "layout": "[B,H,N,D] bf16, D innermost"}
     if extra:
         cfg.update(extra)
@@ -269,12 +269,15 @@ def run_ours(args, w):
     o = torch.empty_like(qd)
     lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
-    in_bytes = 3 * q.nbytes
+    in_bytes = q.nbytes + k.nbytes + v.nbytes
     flush = in_bytes + o.numel() * 2 < 2 * L2_BYTES
     scratch = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev) if flush else None
 
     def step():
-        st = pkg.attn_fwd(qd, kd, vd, o, lse, w.B, w.H, w.N, w.D, w.causal, w.scale, stream)
+        if w.n_keys == w.N:
+            st = pkg.attn_fwd(qd, kd, vd, o, lse, w.B, w.H, w.N, w.D, w.causal, w.scale, stream)
+        else:
+            st = pkg.attn_fwd_qk(qd, kd, vd, o, lse, w.B, w.H, w.N, w.n_keys, w.D, w.causal, w.scale, stream)
         if st != pkg.ATTN_OK:
             raise RuntimeError(pkg.attn_status_string(st))
 
@@ -323,7 +326,7 @@ def run_ours(args, w):
     if sampler:
         sampler.stop()
 
-    flops = pkg.attn_fwd_flops(w.B, w.H, w.N, w.D, w.causal)
+    flops = pkg.attn_fwd_qk_flops(w.B, w.H, w.N, w.n_keys, w.D, w.causal)
     ms_per_step = elapsed_ms / args.steps
     value = job_tflops(flops, world, ms_per_step)
 
@@ -368,7 +371,7 @@ def run_ours(args, w):
     traffic = ncu_traffic(w.name)
     # Below the ridge point (peak FLOP/s over HBM bytes/s) the kernel is bound by
     # HBM bandwidth: algorithmic bytes = Q, K, V read + O written (bf16) + LSE (fp32).
-    alg_bytes = 8.0 * w.B * w.H * w.N * w.D + 4.0 * w.B * w.H * w.N
+    alg_bytes = 2.0 * w.B * w.H * w.D * (2 * w.N + 2 * w.n_keys) + 4.0 * w.B * w.H * w.N
     ridge = peak * 1e12 / (float(peaks["hbm_gbs"]) * 1e9)
     if flops / alg_bytes < ridge:
         roofline = {"bound": "hbm", "achieved": alg_bytes / (ms_per_step * 1e-3) / 1e9, "peak": float(peaks["hbm_gbs"]),

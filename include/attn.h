@@ -70,6 +70,25 @@ attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, flo
                        void* stream);
 
 /*
+ * attn_fwd_qk -- attn_fwd for queries and keys of different lengths.
+ *
+ * q, o : [B, H, Nq, D] bf16;  k, v : [B, H, Nk, D] bf16;  lse : [B, H, Nq] fp32.
+ * Same pointer rules, layouts and errors as attn_fwd.  With `causal`, the mask
+ * is aligned at the bottom-right corner of the Nq x Nk score matrix: key j is
+ * visible to query i iff j <= i + (Nk - Nq), i.e. the queries are the last Nq
+ * positions of a sequence whose first Nk positions have keys (a query block
+ * appended to a key/value cache); for Nq = Nk this is attn_fwd's mask.  The
+ * pages give only an IS_CAUSAL flag for the Triton forward (null-ptr.tistory.com
+ * "development", the `_fwd_kernel` post); the alignment is this library's
+ * reading.  Requests in which some query sees no key -- Nk = 0 with Nq > 0, or
+ * causal with Nq > Nk -- return ATTN_ERR_UNSUPPORTED.  Nq = 0 (or B or H = 0)
+ * is an empty problem: ATTN_OK, nothing launched.
+ */
+attn_status_t attn_fwd_qk(const void* q, const void* k, const void* v, void* o, float* lse,
+                          int64_t B, int64_t H, int64_t Nq, int64_t Nk, int64_t D, int causal,
+                          float scale, void* stream);
+
+/*
  * attn_last_status -- synchronise `stream`, then report and clear the device
  * status word of the current device: ATTN_OK, or ATTN_ERR_TIMEOUT if a kernel
  * gave up on a pipeline wait since the last call; ATTN_ERR_CUDA if the
@@ -85,6 +104,13 @@ const char* attn_status_string(attn_status_t status);
  * 4 * B * H * N^2 * D, halved when causal (exp and softmax not counted).
  */
 double attn_fwd_flops(int64_t B, int64_t H, int64_t N, int64_t D, int causal);
+
+/*
+ * attn_fwd_qk_flops -- algorithmic FLOPs of one attn_fwd_qk call: 4 * B * H * D
+ * times the visible (query, key) pairs, Nq * Nk, or Nq * (Nk - Nq) + Nq^2 / 2
+ * when causal (equal to attn_fwd_flops when Nq = Nk).
+ */
+double attn_fwd_qk_flops(int64_t B, int64_t H, int64_t Nq, int64_t Nk, int64_t D, int causal);
 
 #ifdef __cplusplus
 }

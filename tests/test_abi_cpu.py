@@ -93,3 +93,32 @@ def test_no_gpu_means_cuda_error_not_a_crash(lib):
     if torch.cuda.is_available():
         pytest.skip("a GPU is present")
     assert call() == pkg.ATTN_ERR_CUDA
+
+
+def call_qk(Nq=100, Nk=300, causal=1, **kw):
+    args = dict(q=A16, k=A16 + 64 * MB, v=A16 + 128 * MB, o=A16 + 192 * MB, lse=A16 + 256 * MB,
+                B=1, H=2, D=64, scale=0.125)
+    args.update(kw)
+    return pkg.attn_fwd_qk(args["q"], args["k"], args["v"], args["o"], args["lse"], args["B"], args["H"], Nq, Nk,
+                           args["D"], causal, args["scale"], None)
+
+
+def test_qk_rows_without_keys_are_unsupported(lib):
+    assert call_qk(Nq=300, Nk=100, causal=1) == pkg.ATTN_ERR_UNSUPPORTED  # first 200 queries see nothing
+    assert call_qk(Nq=10, Nk=0, causal=0) == pkg.ATTN_ERR_UNSUPPORTED
+    assert call_qk(Nq=0, Nk=50) == pkg.ATTN_OK
+    assert call_qk(Nq=0, Nk=50, q=None, k=None, v=None, o=None, lse=None) == pkg.ATTN_OK
+    assert call_qk(Nq=-1, Nk=50) == pkg.ATTN_ERR_INVALID_ARG
+
+
+def test_qk_overlap_uses_each_tensors_own_length(lib):
+    # k holds Nk = 300 rows: an o placed right after a 100-row q but inside k overlaps.
+    assert call_qk(Nq=100, Nk=300, o=A16 + 64 * MB + 100 * 64 * 2 * 2) == pkg.ATTN_ERR_INVALID_ARG
+    assert call_qk(Nq=100, Nk=300, lse=A16 + 128 * MB + 16) == pkg.ATTN_ERR_INVALID_ARG
+
+
+def test_qk_flops(lib):
+    assert pkg.attn_fwd_qk_flops(2, 3, 256, 256, 64, True) == pkg.attn_fwd_flops(2, 3, 256, 64, True)
+    assert pkg.attn_fwd_qk_flops(2, 3, 256, 256, 64, False) == pkg.attn_fwd_flops(2, 3, 256, 64, False)
+    assert pkg.attn_fwd_qk_flops(1, 1, 100, 300, 64, False) == 4.0 * 100 * 300 * 64
+    assert pkg.attn_fwd_qk_flops(1, 1, 100, 300, 64, True) == 4.0 * (100 * 200 + 0.5 * 100 * 100) * 64

@@ -201,3 +201,45 @@ def test_side_stream_and_fwd_wrapper():
     s.synchronize()
     o_ref, lse_ref = oracle.attn_fwd(q, k, v, True, 1.0 / math.sqrt(128))
     assert_close(o_to_f64(o), lse.cpu().numpy().astype(np.float64), o_ref, lse_ref, "side stream")
+
+
+def run_qk(q, k, v, causal, scale):
+    B, H, Nq, D = q.shape
+    Nk = k.shape[2]
+    qd, kd, vd = to_dev(q), to_dev(k), to_dev(v)
+    o = torch.full_like(qd, float("nan"))
+    lse = torch.full((B, H, Nq), float("nan"), dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream()
+    st = pkg.attn_fwd_qk(qd, kd, vd, o, lse, B, H, Nq, Nk, D, causal, scale, stream)
+    assert st == pkg.ATTN_OK, pkg.attn_status_string(st)
+    assert pkg.attn_last_status(stream) == pkg.ATTN_OK
+    return o_to_f64(o), lse.cpu().numpy().astype(np.float64)
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("Nq,Nk,causal", [
+    (1, 1000, True), (1, 1000, False), (17, 300, True), (128, 4096, True), (200, 333, True),
+    (300, 300, True), (700, 129, False), (1000, 77, False), (384, 2048, False),
+])
+def test_queries_and_keys_of_different_lengths(Nq, Nk, causal, D, tiles_per_cta):
+    q, _, _ = make_qkv(2, 3, Nq, D, seed=900 + Nq)
+    _, k, v = make_qkv(2, 3, Nk, D, seed=901 + Nk)
+    scale = 1.0 / math.sqrt(D)
+    o, lse = run_qk(q, k, v, causal, scale)
+    o_ref, lse_ref = oracle.attn_fwd(q, k, v, causal, scale)
+    assert_close(o, lse, o_ref, lse_ref, f"Nq={Nq} Nk={Nk} D={D} causal={causal} T={tiles_per_cta}")
+
+
+def test_square_qk_call_is_attn_fwd():
+    q, k, v = make_qkv(1, 4, 640, 128, seed=950)
+    a = run_qk(q, k, v, True, 0.09)
+    b = run(q, k, v, True, 0.09)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+def test_fwd_wrapper_with_a_key_cache():
+    q, _, _ = make_qkv(1, 2, 256, 64, seed=951)
+    _, k, v = make_qkv(1, 2, 1500, 64, seed=952)
+    o, lse = pkg.fwd(to_dev(q), to_dev(k), to_dev(v), causal=True)
+    o_ref, lse_ref = oracle.attn_fwd(q, k, v, True, 0.125)
+    assert_close(o_to_f64(o), lse.cpu().numpy().astype(np.float64), o_ref, lse_ref, "fwd() Nq=256 Nk=1500")

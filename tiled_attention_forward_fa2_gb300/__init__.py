@@ -16,6 +16,8 @@ from ._binding import (  # noqa: F401
     ATTN_OK,
     attn_fwd,
     attn_fwd_flops,
+    attn_fwd_qk,
+    attn_fwd_qk_flops,
     attn_last_status,
     attn_status_string,
     library,
@@ -29,9 +31,10 @@ class AttnError(RuntimeError):
 
 
 def fwd(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None, stream=None):
-    """Fused forward on bf16 CUDA tensors [B, H, N, D] (contiguous).
+    """Fused forward on contiguous bf16 CUDA tensors q [B, H, Nq, D], k, v [B, H, Nk, D].
 
-    Returns ``(o, lse)``: o bf16 [B, H, N, D], lse fp32 [B, H, N].  ``scale``
+    Returns ``(o, lse)``: o bf16 [B, H, Nq, D], lse fp32 [B, H, Nq].  With
+    ``causal`` and Nq != Nk the mask is aligned at the bottom-right.  ``scale``
     defaults to 1/sqrt(D).  Runs on ``stream`` (default: torch's current
     stream) without synchronising.
     """
@@ -40,9 +43,10 @@ def fwd(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse
     for name, t in (("q", q), ("k", k), ("v", v)):
         if t.dtype != torch.bfloat16 or not t.is_cuda or t.dim() != 4 or not t.is_contiguous():
             raise ValueError(f"{name} must be a contiguous bf16 CUDA tensor [B, H, N, D]")
-    if not (q.shape == k.shape == v.shape):
-        raise ValueError("q, k and v must have one shape")
+    if not (k.shape == v.shape and q.shape[:2] == k.shape[:2] and q.shape[3] == k.shape[3]):
+        raise ValueError("q must be [B, H, Nq, D] and k, v [B, H, Nk, D]")
     B, H, N, D = q.shape
+    Nk = k.shape[2]
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     if out is None:
@@ -51,7 +55,10 @@ def fwd(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse
         lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
     if stream is None:
         stream = torch.cuda.current_stream(q.device)
-    st = attn_fwd(q, k, v, out, lse, B, H, N, D, causal, scale, stream)
+    if Nk == N:
+        st = attn_fwd(q, k, v, out, lse, B, H, N, D, causal, scale, stream)
+    else:
+        st = attn_fwd_qk(q, k, v, out, lse, B, H, N, Nk, D, causal, scale, stream)
     if st != ATTN_OK:
         raise AttnError(st)
     return out, lse

@@ -38,6 +38,10 @@ def library() -> ctypes.CDLL:
             lib.attn_status_string.restype = ctypes.c_char_p
             lib.attn_fwd_flops.argtypes = [I64, I64, I64, I64, ctypes.c_int]
             lib.attn_fwd_flops.restype = ctypes.c_double
+            lib.attn_fwd_qk.argtypes = [P, P, P, P, P, I64, I64, I64, I64, I64, ctypes.c_int, ctypes.c_float, P]
+            lib.attn_fwd_qk.restype = ctypes.c_int
+            lib.attn_fwd_qk_flops.argtypes = [I64, I64, I64, I64, I64, ctypes.c_int]
+            lib.attn_fwd_qk_flops.restype = ctypes.c_double
             _lib = lib
     return _lib
 
@@ -69,3 +73,15 @@ def attn_status_string(status: int) -> str:
 
 def attn_fwd_flops(B: int, H: int, N: int, D: int, causal: bool) -> float:
     return library().attn_fwd_flops(int(B), int(H), int(N), int(D), int(bool(causal)))
+
+
+def attn_fwd_qk(q, k, v, o, lse, B: int, H: int, Nq: int, Nk: int, D: int, causal: bool, scale: float,
+                stream) -> int:
+    """Call ``attn_fwd_qk`` (queries and keys of different lengths, bottom-right causal)."""
+    s = stream if (stream is None or isinstance(stream, int)) else stream.cuda_stream
+    return library().attn_fwd_qk(_addr(q), _addr(k), _addr(v), _addr(o), _addr(lse), int(B), int(H), int(Nq),
+                                 int(Nk), int(D), int(bool(causal)), float(scale), s)
+
+
+def attn_fwd_qk_flops(B: int, H: int, Nq: int, Nk: int, D: int, causal: bool) -> float:
+    return library().attn_fwd_qk_flops(int(B), int(H), int(Nq), int(Nk), int(D), int(bool(causal)))

@@ -107,32 +107,35 @@ cudaError_t launch(const attn::FwdParams& prm, int64_t ctas, cudaStream_t stream
   return cudaGetLastError();
 }
 
-}  // namespace
-
-extern "C" {
-
-attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int64_t B, int64_t H,
-                       int64_t N, int64_t D, int causal, float scale, void* stream) {
-  if (B < 0 || H < 0 || N < 0 || D <= 0) return ATTN_ERR_INVALID_ARG;
+// Shared launcher of attn_fwd and attn_fwd_qk: Q, O [B*H, Nq, D]; K, V [B*H, Nk, D].
+attn_status_t launch_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int64_t B, int64_t H,
+                         int64_t Nq, int64_t Nk, int64_t D, int causal, float scale, void* stream) {
+  if (B < 0 || H < 0 || Nq < 0 || Nk < 0 || D <= 0) return ATTN_ERR_INVALID_ARG;
   if (!(scale > 0.f) || !std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
   if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
-  if (B == 0 || H == 0 || N == 0) return ATTN_OK;  // nothing is read or written
+  if (B == 0 || H == 0 || Nq == 0) return ATTN_OK;  // nothing is read or written
+  // Query rows that see no key at all (Nk = 0, or causal with Nq > Nk) are not
+  // produced by the kernel.
+  if (Nk == 0 || (causal && Nq > Nk)) return ATTN_ERR_UNSUPPORTED;
   if (!q || !k || !v || !o || !lse) return ATTN_ERR_INVALID_ARG;
   constexpr int64_t kI32 = 2147483647;
-  if (B > kI32 || H > kI32 || B * H > kI32 || N > kI32 - 256) return ATTN_ERR_INVALID_ARG;
+  if (B > kI32 || H > kI32 || B * H > kI32 || Nq > kI32 - 256 || Nk > kI32 - 256) return ATTN_ERR_INVALID_ARG;
   const int64_t BH = B * H;
-  const int64_t n_tiles = (N + attn::BM - 1) / attn::BM;
-  if (BH > kI32 / n_tiles) return ATTN_ERR_INVALID_ARG;            // grid size
-  if (BH > (int64_t(1) << 62) / (N * D * 2)) return ATTN_ERR_INVALID_ARG;  // byte sizes
-  const uint64_t tensor_bytes = uint64_t(BH) * uint64_t(N) * uint64_t(D) * 2u;
-  const uint64_t lse_bytes = uint64_t(BH) * uint64_t(N) * 4u;
+  const int64_t n_qtiles = (Nq + attn::BM - 1) / attn::BM;
+  const int64_t n_ktiles = (Nk + attn::BN - 1) / attn::BN;
+  if (BH > kI32 / n_qtiles) return ATTN_ERR_INVALID_ARG;  // grid size
+  const int64_t Nmax = Nq > Nk ? Nq : Nk;
+  if (BH > (int64_t(1) << 62) / (Nmax * D * 2)) return ATTN_ERR_INVALID_ARG;  // byte sizes
+  const uint64_t q_bytes = uint64_t(BH) * uint64_t(Nq) * uint64_t(D) * 2u;
+  const uint64_t kv_bytes = uint64_t(BH) * uint64_t(Nk) * uint64_t(D) * 2u;
+  const uint64_t lse_bytes = uint64_t(BH) * uint64_t(Nq) * 4u;
   const auto mis16 = [](const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) != 0; };
   if (mis16(q) || mis16(k) || mis16(v) || mis16(o) || (reinterpret_cast<uintptr_t>(lse) & 3u) != 0)
     return ATTN_ERR_INVALID_ARG;
-  if (ranges_overlap(o, tensor_bytes, q, tensor_bytes) || ranges_overlap(o, tensor_bytes, k, tensor_bytes) ||
-      ranges_overlap(o, tensor_bytes, v, tensor_bytes) || ranges_overlap(o, tensor_bytes, lse, lse_bytes) ||
-      ranges_overlap(lse, lse_bytes, q, tensor_bytes) || ranges_overlap(lse, lse_bytes, k, tensor_bytes) ||
-      ranges_overlap(lse, lse_bytes, v, tensor_bytes))
+  if (ranges_overlap(o, q_bytes, q, q_bytes) || ranges_overlap(o, q_bytes, k, kv_bytes) ||
+      ranges_overlap(o, q_bytes, v, kv_bytes) || ranges_overlap(o, q_bytes, lse, lse_bytes) ||
+      ranges_overlap(lse, lse_bytes, q, q_bytes) || ranges_overlap(lse, lse_bytes, k, kv_bytes) ||
+      ranges_overlap(lse, lse_bytes, v, kv_bytes))
     return ATTN_ERR_INVALID_ARG;
 
   int dev = 0;
@@ -143,25 +146,28 @@ attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, flo
   if (!enc) return ATTN_ERR_CUDA;
 
   attn::FwdParams prm{};
-  if (!encode_qkv_map(enc, &prm.tq, q, D, N, BH) || !encode_qkv_map(enc, &prm.tk, k, D, N, BH) ||
-      !encode_qkv_map(enc, &prm.tv, v, D, N, BH) || !encode_qkv_map(enc, &prm.to, o, D, N, BH))
+  if (!encode_qkv_map(enc, &prm.tq, q, D, Nq, BH) || !encode_qkv_map(enc, &prm.tk, k, D, Nk, BH) ||
+      !encode_qkv_map(enc, &prm.tv, v, D, Nk, BH) || !encode_qkv_map(enc, &prm.to, o, D, Nq, BH))
     return ATTN_ERR_CUDA;
   // Two query tiles per CTA share every K/V tile and let two softmax warpgroups
   // take turns on the tensor core; use them whenever that still leaves at least
   // two CTAs per SM to schedule, otherwise one tile per CTA for more parallelism.
   // ATTN_TILES_PER_CTA=1|2 overrides the choice (testing and tuning).
-  const int64_t pairs = (n_tiles + 1) / 2;
+  const int64_t pairs = (n_qtiles + 1) / 2;
   int T = pairs * BH >= 2 * int64_t(g_dev_sms[dev]) ? 2 : 1;
   if (const char* e = std::getenv("ATTN_TILES_PER_CTA")) {
     if (e[0] == '1' && e[1] == 0) T = 1;
     if (e[0] == '2' && e[1] == 0) T = 2;
   }
   prm.lse = lse;
-  prm.N = int(N);
+  prm.Nq = int(Nq);
+  prm.Nk = int(Nk);
+  prm.kv_off = int(Nk - Nq);
   prm.bh = int(BH);
-  prm.n_tiles = int(n_tiles);
+  prm.n_qtiles = int(n_qtiles);
+  prm.n_ktiles = int(n_ktiles);
   prm.tiles_per_cta = T;
-  prm.n_units = int((n_tiles + T - 1) / T);
+  prm.n_units = int((n_qtiles + T - 1) / T);
   prm.scale_log2 = scale * 1.4426950408889634f;
   prm.timeout_cycles = timeout_cycles();
   // Test hook for the timeout path: ATTN_TEST_WITHHOLD_KV=1 makes the kernel
@@ -178,6 +184,20 @@ attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, flo
   else
     err = causal ? launch<128, true>(prm, ctas, st) : launch<128, false>(prm, ctas, st);
   return err == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int64_t B, int64_t H,
+                       int64_t N, int64_t D, int causal, float scale, void* stream) {
+  return launch_fwd(q, k, v, o, lse, B, H, N, N, D, causal, scale, stream);
+}
+
+attn_status_t attn_fwd_qk(const void* q, const void* k, const void* v, void* o, float* lse, int64_t B, int64_t H,
+                          int64_t Nq, int64_t Nk, int64_t D, int causal, float scale, void* stream) {
+  return launch_fwd(q, k, v, o, lse, B, H, Nq, Nk, D, causal, scale, stream);
 }
 
 attn_status_t attn_last_status(void* stream) {
@@ -205,6 +225,15 @@ const char* attn_status_string(attn_status_t status) {
 double attn_fwd_flops(int64_t B, int64_t H, int64_t N, int64_t D, int causal) {
   const double f = 4.0 * double(B) * double(H) * double(N) * double(N) * double(D);
   return causal ? 0.5 * f : f;
+}
+
+double attn_fwd_qk_flops(int64_t B, int64_t H, int64_t Nq, int64_t Nk, int64_t D, int causal) {
+  // Visible (query, key) pairs: Nq * Nk, or for the bottom-right causal mask
+  // (Nk >= Nq) sum over i of (i + 1 + Nk - Nq) = Nq * (Nk - Nq) + Nq (Nq + 1) / 2,
+  // taken as Nq * (Nk - Nq) + Nq^2 / 2 so that Nq = Nk gives exactly half.
+  const double nq = double(Nq), nk = double(Nk);
+  const double pairs = causal ? nq * (nk - nq) + 0.5 * nq * nq : nq * nk;
+  return 4.0 * double(B) * double(H) * pairs * double(D);
 }
 
 }  // extern "C"

@@ -58,13 +58,14 @@ constexpr uint32_t kRegSoftmax = 176, kRegCorr = 80, kRegOther = 80;
 static_assert(2 * 128 * kRegSoftmax + 128 * kRegCorr + 128 * kRegOther == kThreads * 128, "register split");
 
 struct FwdParams {
-  CUtensorMap tq, tk, tv, to;  // 3-D maps {D, N, B*H}, box {64, 128, 1}, 128-B swizzle, zero fill
-  float* lse;                  // [B*H, N]
-  int N;
+  CUtensorMap tq, tk, tv, to;  // 3-D maps {D, Nq or Nk, B*H}, box {64, 128, 1}, 128-B swizzle, zero fill
+  float* lse;                  // [B*H, Nq]
+  int Nq, Nk;                  // query and key lengths
+  int kv_off;                  // Nk - Nq: causal key j is visible to query i iff j <= i + kv_off
   int bh;                      // B*H
-  int n_tiles;                 // ceil(N / 128), for queries and keys alike
+  int n_qtiles, n_ktiles;      // ceil(Nq / 128), ceil(Nk / 128)
   int tiles_per_cta;           // T = 1 or 2 query tiles per CTA
-  int n_units;                 // ceil(n_tiles / T): CTAs per (batch, head)
+  int n_units;                 // ceil(n_qtiles / T): CTAs per (batch, head)
   float scale_log2;            // scale * log2(e)
   long long timeout_cycles;
   int withhold_kv;             // test hook: nonzero -> no K/V loads are issued, so the pipeline waits run out
@@ -179,9 +180,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_sm103(const __grid_const
     bh = int(blockIdx.x / uint32_t(p.n_units));
   }
   const int t0 = unit * T;
-  // key tiles visited by query tile 0 and 1 (0 when the CTA has one tile)
-  const int nk0 = CAUSAL ? t0 + 1 : p.n_tiles;
-  const int nk1 = T == 2 ? (CAUSAL ? min(t0 + 2, p.n_tiles) : p.n_tiles) : 0;
+  // Key tiles visited by query tile 0 and 1 (0 when the CTA has one tile).
+  // Causal: up to the key tile of the tile's last query row (past Nq: row Nq-1).
+  auto causal_tiles = [&](int t) {
+    const int last_row = min(t * BM + BM - 1, p.Nq - 1);
+    return min(p.n_ktiles, (last_row + p.kv_off) / BN + 1);
+  };
+  const int nk0 = CAUSAL ? causal_tiles(t0) : p.n_ktiles;
+  const int nk1 = T == 2 ? (CAUSAL ? causal_tiles(t0 + 1) : p.n_ktiles) : 0;
   const int nk = max(nk0, nk1);
 
   if (threadIdx.x == 0) {
@@ -326,8 +332,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_sm103(const __grid_const
           for (int c = 0; c < BN; ++c) s[c] = __uint_as_float(u[c]);
         }
         // Masks: keys past N, and keys after the query row when causal.
-        int lim = min(BN - 1, p.N - 1 - j * BN);
-        if (CAUSAL) lim = min(lim, row - j * BN);
+        int lim = min(BN - 1, p.Nk - 1 - j * BN);
+        if (CAUSAL) lim = min(lim, row + p.kv_off - j * BN);
         if (lim < BN - 1) {
 #pragma unroll
           for (int c = 0; c < BN; ++c) s[c] = c > lim ? -INFINITY : s[c];
@@ -395,7 +401,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_sm103(const __grid_const
         sm103::tmem_st_wait();
         sm103::tc_fence_before();
         sm103::mbar_arrive(bar(C::B_FIN + i));
-        if (row < p.N) p.lse[size_t(bh) * size_t(p.N) + size_t(row)] = (m_ref + log2f(l_run)) * 0.6931471805599453f;
+        if (row < p.Nq) p.lse[size_t(bh) * size_t(p.Nq) + size_t(row)] = (m_ref + log2f(l_run)) * 0.6931471805599453f;
       }
     }
   } else {
@@ -442,7 +448,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_sm103(const __grid_const
       if (!ok) break;
       sm103::tc_fence_after();
       const int m0 = (t0 + i) * BM;
-      if (m0 >= p.N) continue;  // a second tile wholly past N: nothing to store
+      if (m0 >= p.Nq) continue;  // a second tile wholly past Nq: nothing to store
       const float inv_l = __uint_as_float(sm103::tmem_ld1(tS + C::COL_INVL));
       // O_i / l -> bf16 into the (now idle) Q_i tile, laid out as TMA's 128-byte
       // swizzle expects: row r at 128 r, 16-byte chunk c at ((c ^ (r & 7)) * 16).

@@ -67,7 +67,10 @@ def make_qkv(B: int, H: int, N: int, D: int, seed: int, q_std: float = 1.0):
 
 @dataclass(frozen=True)
 class Workload:
-    """One named problem: shapes, mask, seed and the spread of Q."""
+    """One named problem: shapes, mask, seed and the spread of Q.
+
+    N is the query length; Nk the key length (0 means Nk = N).
+    """
     name: str
     B: int
     H: int
@@ -76,6 +79,11 @@ class Workload:
     causal: bool
     seed: int
     q_std: float = 1.0
+    Nk: int = 0
+
+    @property
+    def n_keys(self) -> int:
+        return self.Nk or self.N
 
     @property
     def scale(self) -> float:
@@ -84,12 +92,22 @@ class Workload:
 
     @property
     def flops(self) -> float:
-        """Algorithmic FLOPs: 4*B*H*N^2*D (QK^T and PV), halved when causal."""
-        f = 4.0 * self.B * self.H * self.N * self.N * self.D
-        return f / 2.0 if self.causal else f
+        """Algorithmic FLOPs: 4*B*H*D times the visible (query, key) pairs:
+        N*Nk, or N*(Nk-N) + N^2/2 with the (bottom-right) causal mask -- for
+        N = Nk, 4*B*H*N^2*D halved when causal."""
+        nq, nk = float(self.N), float(self.n_keys)
+        pairs = nq * (nk - nq) + 0.5 * nq * nq if self.causal else nq * nk
+        return 4.0 * self.B * self.H * pairs * self.D
 
     def qkv(self):
-        return make_qkv(self.B, self.H, self.N, self.D, self.seed, self.q_std)
+        if self.n_keys == self.N:
+            return make_qkv(self.B, self.H, self.N, self.D, self.seed, self.q_std)
+        shape_q = (self.B, self.H, self.N, self.D)
+        shape_kv = (self.B, self.H, self.n_keys, self.D)
+        q = normal_bf16_bits(self.B * self.H * self.N * self.D, self.seed, STREAM_Q, self.q_std).reshape(shape_q)
+        k = normal_bf16_bits(self.B * self.H * self.n_keys * self.D, self.seed, STREAM_K, 1.0).reshape(shape_kv)
+        v = normal_bf16_bits(self.B * self.H * self.n_keys * self.D, self.seed, STREAM_V, 1.0).reshape(shape_kv)
+        return q, k, v
 
 
 # The problem sizes the method is measured on: a tiny case, a short-sequence case
@@ -105,5 +123,8 @@ WORKLOADS = {
         Workload("b4h16n4096d128", 4, 16, 4096, 128, False, 1003),
         Workload("b1h16n16384d128_causal_q4", 1, 16, 16384, 128, True, 1004, 4.0),
         Workload("b16h32n512d64_causal", 16, 32, 512, 64, True, 1005),
+        # A block of 512 new queries against a key/value cache of 8192 positions
+        # (causal, aligned at the end of the cache).
+        Workload("b8h16nq512nk8192d128_causal", 8, 16, 512, 128, True, 1006, Nk=8192),
     ]
 }
