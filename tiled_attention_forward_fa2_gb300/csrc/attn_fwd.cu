@@ -150,11 +150,15 @@ attn_status_t launch_fwd(const void* q, const void* k, const void* v, void* o, f
       !encode_qkv_map(enc, &prm.tv, v, D, Nk, BH) || !encode_qkv_map(enc, &prm.to, o, D, Nq, BH))
     return ATTN_ERR_CUDA;
   // Two query tiles per CTA share every K/V tile and let two softmax warpgroups
-  // take turns on the tensor core; use them whenever that still leaves at least
-  // two CTAs per SM to schedule, otherwise one tile per CTA for more parallelism.
+  // take turns on the tensor core: one key step of both tiles costs about 3100
+  // SM cycles, against about 2500 for one tile alone (no partner to overlap
+  // with).  Pick the tiling whose waves of CTAs finish first:
+  //   waves(T=2) * 3100 <= waves(T=1) * 2500, i.e. about 5 * waves2 <= 4 * waves1.
   // ATTN_TILES_PER_CTA=1|2 overrides the choice (testing and tuning).
-  const int64_t pairs = (n_qtiles + 1) / 2;
-  int T = pairs * BH >= 2 * int64_t(g_dev_sms[dev]) ? 2 : 1;
+  const int64_t sms = g_dev_sms[dev] > 0 ? g_dev_sms[dev] : 1;
+  const int64_t waves2 = ((n_qtiles + 1) / 2 * BH + sms - 1) / sms;
+  const int64_t waves1 = (n_qtiles * BH + sms - 1) / sms;
+  int T = 5 * waves2 <= 4 * waves1 ? 2 : 1;
   if (const char* e = std::getenv("ATTN_TILES_PER_CTA")) {
     if (e[0] == '1' && e[1] == 0) T = 1;
     if (e[0] == '2' && e[1] == 0) T = 2;
