@@ -27,17 +27,19 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 SOURCE = os.path.join(_HERE, "attn_oracle.c")
+SOURCE_BWD = os.path.join(_HERE, "attn_oracle_bwd.c")
 _LIBDIR = os.path.join(_HERE, "lib")
 _LIB = os.path.join(_LIBDIR, "liboracle_attn.so")
 _lock = threading.Lock()
 _default = None
 
 
-def compile_source(src: str, out: str) -> str:
-    """gcc the C oracle ``src`` into the shared library ``out`` (OpenMP when available)."""
+def compile_source(src, out: str) -> str:
+    """gcc the C oracle source(s) ``src`` into the shared library ``out`` (OpenMP when available)."""
+    srcs = [src] if isinstance(src, str) else list(src)
     os.makedirs(os.path.dirname(out), exist_ok=True)
     tmp = out + f".tmp{os.getpid()}"
-    base = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fPIC", "-shared", "-o", tmp, src, "-lm"]
+    base = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fPIC", "-shared", "-o", tmp, *srcs, "-lm"]
     try:
         subprocess.run(base[:1] + ["-fopenmp"] + base[1:], check=True, capture_output=True)
     except subprocess.CalledProcessError:
@@ -48,9 +50,10 @@ def compile_source(src: str, out: str) -> str:
 
 def build(force: bool = False) -> str:
     """Build ``oracle/lib/liboracle_attn.so`` if it is missing or stale; returns its path."""
-    if not force and os.path.exists(_LIB) and os.path.getmtime(_LIB) >= os.path.getmtime(SOURCE):
+    if not force and os.path.exists(_LIB) and all(os.path.getmtime(_LIB) >= os.path.getmtime(f)
+                                                  for f in (SOURCE, SOURCE_BWD)):
         return _LIB
-    return compile_source(SOURCE, _LIB)
+    return compile_source([SOURCE, SOURCE_BWD], _LIB)
 
 
 def _bits(a: np.ndarray) -> np.ndarray:
@@ -76,6 +79,13 @@ class Oracle:
         lib.oracle_threads.argtypes = [I]
         for f in (lib.oracle_attn_fwd_qk, lib.oracle_attn_rows_qk, lib.oracle_attn_probs_qk, lib.oracle_threads):
             f.restype = I
+        self.has_bwd = hasattr(lib, "oracle_attn_bwd")
+        if self.has_bwd:
+            args = [P] * 10 + [I64, I64, I64, I64, I64, I, ctypes.c_double, I]
+            lib.oracle_attn_bwd.argtypes = args
+            lib.oracle_attn_bwd_f64.argtypes = args
+            lib.oracle_attn_bwd.restype = I
+            lib.oracle_attn_bwd_f64.restype = I
         self._lib = lib
         self.path = libpath
 
@@ -132,6 +142,44 @@ class Oracle:
         if rc != 0:
             raise RuntimeError("oracle_attn_probs failed")
         return o, lse, p
+
+
+def _bwd_call(fn, q, k, v, do, causal, scale, nthreads):
+    B, H, Nq, D = q.shape
+    Nk = k.shape[2]
+    if not (k.shape == v.shape and q.shape == do.shape and q.shape[:2] == k.shape[:2] and k.shape[3] == D):
+        raise ValueError("q, do [B,H,Nq,D] and k, v [B,H,Nk,D] expected")
+    out = {n: np.empty(sh, dtype=np.float64) for n, sh in
+           (("dq", q.shape), ("dk", k.shape), ("dv", k.shape), ("delta", (B, H, Nq)), ("o", q.shape), ("lse", (B, H, Nq)))}
+    rc = fn(_ptr(q), _ptr(k), _ptr(v), _ptr(do), _ptr(out["dq"]), _ptr(out["dk"]), _ptr(out["dv"]),
+            _ptr(out["delta"]), _ptr(out["o"]), _ptr(out["lse"]), B, H, Nq, Nk, D, int(bool(causal)), float(scale),
+            int(nthreads))
+    if rc != 0:
+        raise RuntimeError("oracle backward failed")
+    return out
+
+
+def _bwd_methods(cls):
+    def attn_bwd(self, q, k, v, do, causal: bool, scale: float, nthreads: int = 0):
+        """Gradients of sum(dO * O) from bf16 bit inputs: dict dq, dk, dv, delta, o, lse (float64)."""
+        q, k, v, do = _bits(q), _bits(k), _bits(v), _bits(do)
+        return _bwd_call(self._lib.oracle_attn_bwd, q, k, v, do, causal, scale, nthreads)
+
+    def attn_bwd_f64(self, q, k, v, do, causal: bool, scale: float, nthreads: int = 0):
+        """Same from float64 inputs (for finite-difference checks)."""
+        arr = [np.ascontiguousarray(x, dtype=np.float64) for x in (q, k, v, do)]
+        return _bwd_call(self._lib.oracle_attn_bwd_f64, *arr, causal, scale, nthreads)
+
+    cls.attn_bwd = attn_bwd
+    cls.attn_bwd_f64 = attn_bwd_f64
+    return cls
+
+
+_bwd_methods(Oracle)
+
+
+def attn_bwd(q, k, v, do, causal: bool, scale: float, nthreads: int = 0):
+    return default().attn_bwd(q, k, v, do, causal, scale, nthreads)
 
 
 def default() -> Oracle:
