@@ -39,6 +39,8 @@ DEFAULT_WORKLOAD = "b4h16n4096d128"
 L2_BYTES = 129 * 2**20
 FALLBACK_PEAK_TFLOPS = 1900.0
 KERNEL_SOURCES = ["tiled_attention_forward_fa2_gb300/csrc/attn_fwd_kernel.cuh",
+                  "tiled_attention_forward_fa2_gb300/csrc/attn_bwd_kernel.cuh",
+                  "tiled_attention_forward_fa2_gb300/csrc/attn_bwd_host.cuh",
                   "tiled_attention_forward_fa2_gb300/csrc/sm103_ptx.cuh",
                   "tiled_attention_forward_fa2_gb300/csrc/attn_fwd.cu"]
 
@@ -273,8 +275,18 @@ def run_ours(args, w):
     flush = in_bytes + o.numel() * 2 < 2 * L2_BYTES
     scratch = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev) if flush else None
 
+    if args.backward:
+        # Inputs of the backward: the forward's O and LSE, and an upstream dO.
+        assert pkg.attn_fwd_qk(qd, kd, vd, o, lse, w.B, w.H, w.N, w.n_keys, w.D, w.causal, w.scale, stream) == pkg.ATTN_OK
+        dod = to_dev(w.qkv()[0][..., ::-1].copy(), dev)  # any bf16 tensor of O's shape
+        dq, dk, dv = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
+        delta = torch.empty_like(lse)
+
     def step():
-        if w.n_keys == w.N:
+        if args.backward:
+            st = pkg.attn_bwd_qk(qd, kd, vd, o, lse, dod, dq, dk, dv, delta, w.B, w.H, w.N, w.n_keys, w.D, w.causal,
+                                 w.scale, stream)
+        elif w.n_keys == w.N:
             st = pkg.attn_fwd(qd, kd, vd, o, lse, w.B, w.H, w.N, w.D, w.causal, w.scale, stream)
         else:
             st = pkg.attn_fwd_qk(qd, kd, vd, o, lse, w.B, w.H, w.N, w.n_keys, w.D, w.causal, w.scale, stream)
@@ -326,9 +338,30 @@ def run_ours(args, w):
     if sampler:
         sampler.stop()
 
-    flops = pkg.attn_fwd_qk_flops(w.B, w.H, w.N, w.n_keys, w.D, w.causal)
+    flops = (pkg.attn_bwd_qk_flops if args.backward else pkg.attn_fwd_qk_flops)(w.B, w.H, w.N, w.n_keys, w.D,
+                                                                                w.causal)
     ms_per_step = elapsed_ms / args.steps
     value = job_tflops(flops, world, ms_per_step)
+
+    if args.backward:
+        if rank == 0:
+            peaks, peak_src = measured_peaks()
+            peak = float(peaks["bf16_tflops"])
+            achieved = flops / (ms_per_step * 1e-3) / 1e12
+            line = {"metric": "attention bwd TFLOP/s (bf16, 1\u00d7GB300; 2.5x forward FLOPs)", "value": value,
+                    "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+                    "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                    "dtype": "bf16", "data": "synthetic", "config": workload_config(w, {"pass": "backward"}),
+                    "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                                 "frac": achieved / peak, "traffic": None,
+                                 "peak_source": f"bf16_tflops (burst) of {peak_src}",
+                                 "kernel": "attn_bwd_dq_sm103 + attn_bwd_dkdv_sm103"},
+                    "gpu_launches": 2 * args.steps, "clocks": sampler.summary() if sampler else None,
+                    "kernel_source": kernel_source_hash()}
+            print(json.dumps(line), flush=True)
+        if pg:
+            pg.destroy_process_group()
+        return
 
     # End to end through the C ABI with pinned host buffers.
     e2e_steps = max(3, min(args.steps, 50))
@@ -430,6 +463,8 @@ def main():
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU-oracle baseline budget")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--backward", action="store_true",
+                    help="time the backward (dQ, dK, dV; 2.5x the forward FLOPs) instead of the forward; device timing only")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -89,6 +89,38 @@ attn_status_t attn_fwd_qk(const void* q, const void* k, const void* v, void* o, 
                           float scale, void* stream);
 
 /*
+ * attn_bwd -- enqueue the backward of attn_fwd on `stream`: the gradients of
+ * sum(dO * O) with respect to Q, K and V.
+ *
+ * q, k, v : the forward's inputs; o, lse : its outputs (bf16 [B,H,N,D], fp32
+ * [B,H,N]); dout : the upstream gradient dO, bf16 [B,H,N,D].  All read only.
+ * dq, dk, dv : bf16 [B,H,N,D], written.  delta : fp32 [B,H,N], written:
+ * D_i = sum_d dO_id O_id, which the chain rule through the softmax needs
+ * (ds_ij = p_ij (dp_ij - D_i)); returned so that no scratch memory is needed.
+ * Outputs must not overlap each other or any input.  Same sizes, alignment
+ * (16 bytes for bf16 tensors, 4 for fp32), scale and head-dim rules as
+ * attn_fwd.  The pages call the backward an order of magnitude harder than
+ * the forward ("GPUの爆発的な性能向上", ja.news.hada.io topic 14783) without a
+ * formula; the math is the chain rule written out in oracle/attn_oracle_bwd.c
+ * and the kernels' header comment.  Two kernels are enqueued (dQ and D first,
+ * then dK and dV); errors as attn_fwd, timeouts through attn_last_status.
+ */
+attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                       const void* dout, void* dq, void* dk, void* dv, float* delta, int64_t B,
+                       int64_t H, int64_t N, int64_t D, int causal, float scale, void* stream);
+
+/*
+ * attn_bwd_qk -- attn_bwd for queries and keys of different lengths, the
+ * backward of attn_fwd_qk: q, o, dout, dq [B,H,Nq,D]; k, v, dk, dv [B,H,Nk,D];
+ * lse, delta [B,H,Nq].  Causal alignment and the unsupported cases (some query
+ * without a key; also Nq = 0 with Nk > 0) as attn_fwd_qk.
+ */
+attn_status_t attn_bwd_qk(const void* q, const void* k, const void* v, const void* o,
+                          const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                          float* delta, int64_t B, int64_t H, int64_t Nq, int64_t Nk, int64_t D,
+                          int causal, float scale, void* stream);
+
+/*
  * attn_last_status -- synchronise `stream`, then report and clear the device
  * status word of the current device: ATTN_OK, or ATTN_ERR_TIMEOUT if a kernel
  * gave up on a pipeline wait since the last call; ATTN_ERR_CUDA if the
@@ -111,6 +143,13 @@ double attn_fwd_flops(int64_t B, int64_t H, int64_t N, int64_t D, int causal);
  * when causal (equal to attn_fwd_flops when Nq = Nk).
  */
 double attn_fwd_qk_flops(int64_t B, int64_t H, int64_t Nq, int64_t Nk, int64_t D, int causal);
+
+/*
+ * attn_bwd_qk_flops -- algorithmic FLOPs of one attn_bwd_qk call: the five
+ * products S = Q K^T, dP = dO V^T, dV, dK and dQ, i.e. 2.5 times
+ * attn_fwd_qk_flops (the kernels recompute S and dP once more).
+ */
+double attn_bwd_qk_flops(int64_t B, int64_t H, int64_t Nq, int64_t Nk, int64_t D, int causal);
 
 #ifdef __cplusplus
 }

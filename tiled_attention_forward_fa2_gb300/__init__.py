@@ -14,6 +14,9 @@ from ._binding import (  # noqa: F401
     ATTN_ERR_TIMEOUT,
     ATTN_ERR_UNSUPPORTED,
     ATTN_OK,
+    attn_bwd,
+    attn_bwd_qk,
+    attn_bwd_qk_flops,
     attn_fwd,
     attn_fwd_flops,
     attn_fwd_qk,
@@ -62,3 +65,21 @@ def fwd(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse
     if st != ATTN_OK:
         raise AttnError(st)
     return out, lse
+
+
+def bwd(q, k, v, o, lse, do, causal: bool = False, scale: float | None = None, stream=None):
+    """Backward of ``fwd``: returns ``(dq, dk, dv, delta)`` for contiguous bf16 CUDA tensors."""
+    import torch
+
+    B, H, Nq, D = q.shape
+    Nk = k.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    delta = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    st = attn_bwd_qk(q, k, v, o, lse, do, dq, dk, dv, delta, B, H, Nq, Nk, D, causal, scale, stream)
+    if st != ATTN_OK:
+        raise AttnError(st)
+    return dq, dk, dv, delta

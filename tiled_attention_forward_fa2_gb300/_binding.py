@@ -42,6 +42,12 @@ def library() -> ctypes.CDLL:
             lib.attn_fwd_qk.restype = ctypes.c_int
             lib.attn_fwd_qk_flops.argtypes = [I64, I64, I64, I64, I64, ctypes.c_int]
             lib.attn_fwd_qk_flops.restype = ctypes.c_double
+            lib.attn_bwd.argtypes = [P] * 10 + [I64, I64, I64, I64, ctypes.c_int, ctypes.c_float, P]
+            lib.attn_bwd.restype = ctypes.c_int
+            lib.attn_bwd_qk.argtypes = [P] * 10 + [I64, I64, I64, I64, I64, ctypes.c_int, ctypes.c_float, P]
+            lib.attn_bwd_qk.restype = ctypes.c_int
+            lib.attn_bwd_qk_flops.argtypes = [I64, I64, I64, I64, I64, ctypes.c_int]
+            lib.attn_bwd_qk_flops.restype = ctypes.c_double
             _lib = lib
     return _lib
 
@@ -85,3 +91,26 @@ def attn_fwd_qk(q, k, v, o, lse, B: int, H: int, Nq: int, Nk: int, D: int, causa
 
 def attn_fwd_qk_flops(B: int, H: int, Nq: int, Nk: int, D: int, causal: bool) -> float:
     return library().attn_fwd_qk_flops(int(B), int(H), int(Nq), int(Nk), int(D), int(bool(causal)))
+
+
+def _stream(stream):
+    return stream if (stream is None or isinstance(stream, int)) else stream.cuda_stream
+
+
+def attn_bwd(q, k, v, o, lse, dout, dq, dk, dv, delta, B: int, H: int, N: int, D: int, causal: bool,
+             scale: float, stream) -> int:
+    """Call ``attn_bwd`` (gradients of sum(dO * O) for the square forward)."""
+    a = [_addr(x) for x in (q, k, v, o, lse, dout, dq, dk, dv, delta)]
+    return library().attn_bwd(*a, int(B), int(H), int(N), int(D), int(bool(causal)), float(scale), _stream(stream))
+
+
+def attn_bwd_qk(q, k, v, o, lse, dout, dq, dk, dv, delta, B: int, H: int, Nq: int, Nk: int, D: int, causal: bool,
+                scale: float, stream) -> int:
+    """Call ``attn_bwd_qk`` (queries and keys of different lengths)."""
+    a = [_addr(x) for x in (q, k, v, o, lse, dout, dq, dk, dv, delta)]
+    return library().attn_bwd_qk(*a, int(B), int(H), int(Nq), int(Nk), int(D), int(bool(causal)), float(scale),
+                                 _stream(stream))
+
+
+def attn_bwd_qk_flops(B: int, H: int, Nq: int, Nk: int, D: int, causal: bool) -> float:
+    return library().attn_bwd_qk_flops(int(B), int(H), int(Nq), int(Nk), int(D), int(bool(causal)))

@@ -17,7 +17,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIBDIR = os.path.join(PKG, "lib")
 LIB = os.path.join(LIBDIR, "libattn_fwd_gb300.so")
-SOURCES = [os.path.join(CSRC, "attn_fwd.cu")]
+SOURCES = [os.path.join(CSRC, "attn_fwd.cu")]  # includes the backward (one module, one status word)
 DEPS = SOURCES + [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith(".cuh")] + \
     [os.path.join(INCLUDE, f) for f in os.listdir(INCLUDE) if f.endswith(".h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -1,0 +1,128 @@
+// Host side of the backward entry points (attn_bwd, attn_bwd_qk): validation,
+// tensor maps, launch of the dQ kernel and then the dK/dV kernel on one stream.
+// Included by attn_fwd.cu so both passes share one module (one status word).
+#pragma once
+#include "attn_bwd_kernel.cuh"
+
+namespace {
+
+template <int D, bool CAUSAL>
+cudaError_t opt_in_bwd_smem() {
+  cudaError_t e = cudaFuncSetAttribute(attn::attn_bwd_dq_sm103<D, CAUSAL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       int(attn::CfgDq<D>::SMEM));
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(attn::attn_bwd_dkdv_sm103<D, CAUSAL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              int(attn::CfgDkv<D>::SMEM));
+}
+
+std::atomic<int> g_bwd_ready[kMaxDevices];
+
+attn_status_t prepare_bwd(int dev) {
+  if (g_bwd_ready[dev].load(std::memory_order_acquire) == 1) return ATTN_OK;
+  std::lock_guard<std::mutex> lock(g_dev_mutex);
+  if (g_bwd_ready[dev].load(std::memory_order_relaxed) == 1) return ATTN_OK;
+  if (opt_in_bwd_smem<64, false>() != cudaSuccess || opt_in_bwd_smem<64, true>() != cudaSuccess ||
+      opt_in_bwd_smem<128, false>() != cudaSuccess || opt_in_bwd_smem<128, true>() != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  g_bwd_ready[dev].store(1, std::memory_order_release);
+  return ATTN_OK;
+}
+
+template <int D, bool CAUSAL>
+cudaError_t launch_bwd_kernels(const attn::BwdParams& prm, cudaStream_t st) {
+  attn::attn_bwd_dq_sm103<D, CAUSAL>
+      <<<dim3(unsigned(int64_t(prm.n_qtiles) * prm.bh)), dim3(attn::kBwdThreads), attn::CfgDq<D>::SMEM, st>>>(prm);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  attn::attn_bwd_dkdv_sm103<D, CAUSAL>
+      <<<dim3(unsigned(int64_t(prm.n_ktiles) * prm.bh)), dim3(attn::kBwdThreads), attn::CfgDkv<D>::SMEM, st>>>(prm);
+  return cudaGetLastError();
+}
+
+attn_status_t launch_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                         const void* dout, void* dq, void* dk, void* dv, float* delta, int64_t B, int64_t H,
+                         int64_t Nq, int64_t Nk, int64_t D, int causal, float scale, void* stream) {
+  if (B < 0 || H < 0 || Nq < 0 || Nk < 0 || D <= 0) return ATTN_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
+  if (B == 0 || H == 0 || (Nq == 0 && Nk == 0)) return ATTN_OK;  // nothing is read or written
+  // Nq = 0 leaves dK = dV = 0 and Nk = 0 leaves rows without keys: neither is
+  // produced by these kernels.
+  if (Nq == 0 || Nk == 0 || (causal && Nq > Nk)) return ATTN_ERR_UNSUPPORTED;
+  if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv || !delta) return ATTN_ERR_INVALID_ARG;
+  constexpr int64_t kI32 = 2147483647;
+  if (B > kI32 || H > kI32 || B * H > kI32 || Nq > kI32 - 256 || Nk > kI32 - 256) return ATTN_ERR_INVALID_ARG;
+  const int64_t BH = B * H;
+  const int64_t n_qtiles = (Nq + attn::BM - 1) / attn::BM, n_ktiles = (Nk + attn::BN - 1) / attn::BN;
+  if (BH > kI32 / (n_qtiles > n_ktiles ? n_qtiles : n_ktiles)) return ATTN_ERR_INVALID_ARG;
+  const int64_t Nmax = Nq > Nk ? Nq : Nk;
+  if (BH > (int64_t(1) << 62) / (Nmax * D * 2)) return ATTN_ERR_INVALID_ARG;
+  const uint64_t qb = uint64_t(BH) * uint64_t(Nq) * uint64_t(D) * 2u, kb = uint64_t(BH) * uint64_t(Nk) * uint64_t(D) * 2u;
+  const uint64_t vb4 = uint64_t(BH) * uint64_t(Nq) * 4u;
+  const auto mis16 = [](const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) != 0; };
+  const auto mis4 = [](const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 3u) != 0; };
+  if (mis16(q) || mis16(k) || mis16(v) || mis16(o) || mis16(dout) || mis16(dq) || mis16(dk) || mis16(dv) || mis4(lse) ||
+      mis4(delta))
+    return ATTN_ERR_INVALID_ARG;
+  // Outputs must not overlap each other or any input.
+  const struct { const void* p; uint64_t n; } outs[4] = {{dq, qb}, {dk, kb}, {dv, kb}, {delta, vb4}};
+  const struct { const void* p; uint64_t n; } ins[6] = {{q, qb}, {k, kb}, {v, kb}, {o, qb}, {lse, vb4}, {dout, qb}};
+  for (int a = 0; a < 4; ++a) {
+    for (int b = 0; b < 6; ++b)
+      if (ranges_overlap(outs[a].p, outs[a].n, ins[b].p, ins[b].n)) return ATTN_ERR_INVALID_ARG;
+    for (int b = a + 1; b < 4; ++b)
+      if (ranges_overlap(outs[a].p, outs[a].n, outs[b].p, outs[b].n)) return ATTN_ERR_INVALID_ARG;
+  }
+
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_CUDA;
+  attn_status_t ready = prepare_device(dev);
+  if (ready != ATTN_OK) return ready;
+  if ((ready = prepare_bwd(dev)) != ATTN_OK) return ready;
+  const EncodeTiledFn enc = encode_fn();
+  if (!enc) return ATTN_ERR_CUDA;
+  attn::BwdParams prm{};
+  if (!encode_qkv_map(enc, &prm.tq, q, D, Nq, BH) || !encode_qkv_map(enc, &prm.tdo, dout, D, Nq, BH) ||
+      !encode_qkv_map(enc, &prm.tk, k, D, Nk, BH) || !encode_qkv_map(enc, &prm.tv, v, D, Nk, BH) ||
+      !encode_qkv_map(enc, &prm.tdq, dq, D, Nq, BH) || !encode_qkv_map(enc, &prm.tdk, dk, D, Nk, BH) ||
+      !encode_qkv_map(enc, &prm.tdv, dv, D, Nk, BH))
+    return ATTN_ERR_CUDA;
+  prm.o = static_cast<const __nv_bfloat16*>(o);
+  prm.dout = static_cast<const __nv_bfloat16*>(dout);
+  prm.lse = lse;
+  prm.delta = delta;
+  prm.Nq = int(Nq);
+  prm.Nk = int(Nk);
+  prm.kv_off = int(Nk - Nq);
+  prm.bh = int(BH);
+  prm.n_qtiles = int(n_qtiles);
+  prm.n_ktiles = int(n_ktiles);
+  prm.scale = scale;
+  prm.scale_log2 = scale * 1.4426950408889634f;
+  prm.timeout_cycles = timeout_cycles();
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t err;
+  if (D == 64)
+    err = causal ? launch_bwd_kernels<64, true>(prm, st) : launch_bwd_kernels<64, false>(prm, st);
+  else
+    err = causal ? launch_bwd_kernels<128, true>(prm, st) : launch_bwd_kernels<128, false>(prm, st);
+  return err == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
+                       void* dq, void* dk, void* dv, float* delta, int64_t B, int64_t H, int64_t N, int64_t D,
+                       int causal, float scale, void* stream) {
+  return launch_bwd(q, k, v, o, lse, dout, dq, dk, dv, delta, B, H, N, N, D, causal, scale, stream);
+}
+
+attn_status_t attn_bwd_qk(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                          const void* dout, void* dq, void* dk, void* dv, float* delta, int64_t B, int64_t H,
+                          int64_t Nq, int64_t Nk, int64_t D, int causal, float scale, void* stream) {
+  return launch_bwd(q, k, v, o, lse, dout, dq, dk, dv, delta, B, H, Nq, Nk, D, causal, scale, stream);
+}
+
+}  // extern "C"

@@ -1,0 +1,497 @@
+// Attention backward for sm_103a (GB300): dQ, dK, dV of sum(dO * O) for the
+// forward in attn_fwd_kernel.cuh.
+//
+// The pages ("GPUの爆発的な性能向上", ja.news.hada.io topic 14783, closing
+// discussion and section "アドレス生成とTMA") call the backward an order of
+// magnitude harder than the forward and print no formula; this is the chain
+// rule through the softmax with the forward's saved LSE:
+//   p_ij  = exp(scale s_ij - LSE_i),  dp_ij = dO_i . v_j,  D_i = dO_i . O_i,
+//   ds_ij = p_ij (dp_ij - D_i),  dQ = scale dS K,  dK = scale dS^T Q,  dV = P^T dO.
+// Two kernels, launched in this order on one stream; neither needs scratch
+// memory (D is an output):
+//   attn_bwd_dq_sm103  : one CTA per 128-query tile.  D_i from O and dO, then
+//       per key tile S = Q K^T and dP = dO V^T into TMEM, dS (bf16) over S,
+//       dQ += dS K with dS read from TMEM; dQ stored with TMA.
+//   attn_bwd_dkdv_sm103: one CTA per 128-key tile, transposed: per query tile
+//       S^T = K Q^T and dP^T = V dO^T, P^T and dS^T (bf16) over them, then
+//       dV += P^T dO and dK += dS^T Q; the per-query LSE and D reach every
+//       thread through shared memory; dK, dV stored with TMA.
+// Warp roles as in the forward: warps 0-3 elementwise (thread = TMEM lane =
+// row), warp 4 TMA producer, warp 5 TMEM allocation and warp-uniform MMA issue.
+// Every wait is bounded (see wait_bounded in attn_fwd_kernel.cuh).
+#pragma once
+#include "attn_fwd_kernel.cuh"
+
+namespace attn {
+
+constexpr int kBwdThreads = 192;
+constexpr int kBwdLoadWarp = 4, kBwdMmaWarp = 5;
+
+struct BwdParams {
+  CUtensorMap tq, tdo, tk, tv;  // Q, dO {D, Nq, B*H}; K, V {D, Nk, B*H}; box {64, 128, 1}
+  CUtensorMap tdq, tdk, tdv;    // stores: dQ {D, Nq, B*H}; dK, dV {D, Nk, B*H}
+  const __nv_bfloat16* o;       // [B*H, Nq, D] forward output
+  const __nv_bfloat16* dout;    // [B*H, Nq, D]
+  const float* lse;             // [B*H, Nq] natural log
+  float* delta;                 // [B*H, Nq] D_i: written by the dQ kernel, read by the dK/dV kernel
+  int Nq, Nk, kv_off, bh, n_qtiles, n_ktiles;
+  float scale;                  // softmax scale
+  float scale_log2;             // scale * log2(e)
+  long long timeout_cycles;
+};
+
+// ------------------------------------------------------------------ dQ kernel
+template <int D>
+struct CfgDq {
+  static constexpr int KB = D / 64;
+  static constexpr uint32_t TILE = KB * kSubTile;
+  static constexpr int NSLOT = D == 128 ? 4 : 8;   // K/V ring (K_j, V_j alternate)
+  static constexpr uint32_t OFF_Q = 1024, OFF_DO = OFF_Q + TILE, OFF_KV = OFF_DO + TILE;
+  static constexpr uint32_t SMEM = OFF_KV + NSLOT * TILE + 1024;
+  static_assert(SMEM <= 232448, "shared memory");
+  static constexpr int B_Q = 0, B_FULL = 1, B_EMPTY = 1 + NSLOT, B_SF = 1 + 2 * NSLOT, B_DSF = B_SF + 1,
+                       B_QDONE = B_DSF + 1, B_DONE = B_QDONE + 1, NBAR = B_DONE + 1;
+  static constexpr uint32_t COL_S = 0, COL_DP = 128, COL_DQ = 256;  // dS (bf16) over S's first 64 columns
+};
+
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dq_sm103(const __grid_constant__ BwdParams p) {
+  using C = CfgDq<D>;
+  constexpr int KB = C::KB, NSLOT = C::NSLOT;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = sm103::smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* const sbase = smem_raw + (base - raw);
+  uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(sbase + 512);
+  volatile uint32_t* const abort_flag = reinterpret_cast<volatile uint32_t*>(sbase + 516);
+  const uint32_t sQ = base + C::OFF_Q, sDO = base + C::OFF_DO, sKV = base + C::OFF_KV;
+  auto bar = [base](int i) { return base + 8u * uint32_t(i); };
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  // Causal: heaviest query tiles first; full: the tiles of one head adjacent.
+  int qt, bh;
+  if (CAUSAL) {
+    qt = p.n_qtiles - 1 - int(blockIdx.x / uint32_t(p.bh));
+    bh = int(blockIdx.x % uint32_t(p.bh));
+  } else {
+    qt = int(blockIdx.x % uint32_t(p.n_qtiles));
+    bh = int(blockIdx.x / uint32_t(p.n_qtiles));
+  }
+  const int m0 = qt * BM;
+  const int nk = CAUSAL ? min(p.n_ktiles, (min(m0 + BM - 1, p.Nq - 1) + p.kv_off) / BN + 1) : p.n_ktiles;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < C::NBAR; ++i) sm103::mbar_init(bar(i), i == C::B_DSF ? uint32_t(BM) : 1u);
+    *abort_flag = 0u;
+    sm103::fence_mbar_init();
+  }
+  if (warp == kBwdMmaWarp) {
+    sm103::tmem_alloc(sm103::smem_u32(tmem_slot), kTmemCols);
+    sm103::tmem_relinquish();
+  }
+  sm103::tc_fence_before();
+  __syncthreads();
+  sm103::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const Abort ab{abort_flag, p.timeout_cycles};
+
+  if (warp == kBwdLoadWarp) {
+    if (lane == 0) {
+      sm103::mbar_arrive_expect_tx(bar(C::B_Q), 2u * C::TILE);
+      for (int kb = 0; kb < KB; ++kb) {
+        sm103::tma_load_3d(sQ + kb * kSubTile, &p.tq, bar(C::B_Q), kb * 64, m0, bh);
+        sm103::tma_load_3d(sDO + kb * kSubTile, &p.tdo, bar(C::B_Q), kb * 64, m0, bh);
+      }
+      int c = 0;
+      bool ok = true;
+      for (int j = 0; ok && j < nk; ++j) {
+        for (int kv = 0; kv < 2; ++kv, ++c) {
+          const int s = c % NSLOT;
+          if (c >= NSLOT && !(ok = wait_bounded(bar(C::B_EMPTY + s), uint32_t(c / NSLOT - 1) & 1u, ab))) break;
+          sm103::mbar_arrive_expect_tx(bar(C::B_FULL + s), C::TILE);
+          const CUtensorMap* map = kv == 0 ? &p.tk : &p.tv;
+          for (int kb = 0; kb < KB; ++kb)
+            sm103::tma_load_3d(sKV + s * C::TILE + kb * kSubTile, map, bar(C::B_FULL + s), kb * 64, j * BN, bh);
+        }
+      }
+      drain_wait(bar(C::B_Q), 0u);
+      for (int t = c > NSLOT ? c - NSLOT : 0; t < c; ++t) drain_wait(bar(C::B_FULL + t % NSLOT), uint32_t(t / NSLOT) & 1u);
+    }
+    __syncwarp();
+  } else if (warp == kBwdMmaWarp) {
+    constexpr uint32_t kIdescS = sm103::idesc_bf16_f32(BM, BN, 0, 0);  // both operands K-major
+    constexpr uint32_t kIdescQ = sm103::idesc_bf16_f32(BM, D, 0, 1);   // dS from TMEM, K MN-major
+    const uint64_t dq_k = sm103::sdesc_sw128(sQ, 16, 1024), ddo_k = sm103::sdesc_sw128(sDO, 16, 1024);
+    const uint64_t dkv_k = sm103::sdesc_sw128(sKV, 16, 1024), dkv_mn = sm103::sdesc_sw128(sKV, kSubTile, 1024);
+    auto slot_off = [](int c) { return uint64_t(uint32_t(c % NSLOT) * (C::TILE >> 4)); };
+    auto wait_full = [&](int c) { return warp_wait(bar(C::B_FULL + c % NSLOT), uint32_t(c / NSLOT) & 1u, ab); };
+    auto release = [&](int c) { sm103::mma_commit_warp(bar(C::B_EMPTY + c % NSLOT)); };
+    auto issue_s_dp = [&](int j) {  // S = Q K_j^T, dP = dO V_j^T
+      const uint64_t dk = dkv_k + slot_off(2 * j), dv = dkv_k + slot_off(2 * j + 1);
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint64_t off = uint64_t((uint32_t(kk >> 2) * kSubTile + uint32_t(kk & 3) * 32u) >> 4);
+        sm103::mma_ss_warp(tmem + C::COL_S, dq_k + off, dk + off, kIdescS, kk > 0 ? 1u : 0u);
+      }
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint64_t off = uint64_t((uint32_t(kk >> 2) * kSubTile + uint32_t(kk & 3) * 32u) >> 4);
+        sm103::mma_ss_warp(tmem + C::COL_DP, ddo_k + off, dv + off, kIdescS, kk > 0 ? 1u : 0u);
+      }
+      sm103::mma_commit_warp(bar(C::B_SF));
+      release(2 * j + 1);  // V_j is done with
+    };
+    bool ok = warp_wait(bar(C::B_Q), 0u, ab) && wait_full(0) && wait_full(1);
+    if (ok) {
+      sm103::tc_fence_after();
+      issue_s_dp(0);
+    }
+    for (int j = 0; ok && j < nk; ++j) {
+      if (!(ok = warp_wait(bar(C::B_DSF), uint32_t(j) & 1u, ab))) break;
+      sm103::tc_fence_after();
+      const uint64_t dkmn = dkv_mn + slot_off(2 * j);
+#pragma unroll
+      for (int kk = 0; kk < BN / 16; ++kk)  // dQ += dS K_j: 16 keys per MMA
+        sm103::mma_ts_warp(tmem + C::COL_DQ, tmem + C::COL_S + kk * 8, dkmn + uint64_t(kk * (2048 >> 4)), kIdescQ,
+                           (j > 0 || kk > 0) ? 1u : 0u);
+      release(2 * j);  // K_j is done with
+      if (j + 1 < nk) {
+        if (!(ok = wait_full(2 * j + 2) && wait_full(2 * j + 3))) break;
+        sm103::tc_fence_after();
+        issue_s_dp(j + 1);
+      }
+    }
+    sm103::mma_commit_warp(bar(C::B_QDONE));
+    sm103::mma_commit_warp(bar(C::B_DONE));
+    drain_wait(bar(C::B_DONE), 0u);
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------- elementwise
+    const int r = threadIdx.x;
+    const int row = m0 + r;
+    const uint32_t lane_off = uint32_t(warp * 32) << 16;
+    const float sl2 = p.scale_log2;
+    // D_i = dO_i . O_i and the row's LSE in base 2 (rows past Nq: P = 0).
+    float dlt = 0.f, lse2 = INFINITY;
+    if (row < p.Nq) {
+      const uint4* po = reinterpret_cast<const uint4*>(p.o + (size_t(bh) * p.Nq + row) * D);
+      const uint4* pd = reinterpret_cast<const uint4*>(p.dout + (size_t(bh) * p.Nq + row) * D);
+      float a0 = 0.f, a1 = 0.f;
+#pragma unroll 4
+      for (int x = 0; x < D / 8; ++x) {
+        const uint4 uo = po[x], ud = pd[x];
+        const uint32_t wo[4] = {uo.x, uo.y, uo.z, uo.w}, wd[4] = {ud.x, ud.y, ud.z, ud.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          a0 = fmaf(sm103::bf16lo_to_f32(wo[e]), sm103::bf16lo_to_f32(wd[e]), a0);
+          a1 = fmaf(sm103::bf16hi_to_f32(wo[e]), sm103::bf16hi_to_f32(wd[e]), a1);
+        }
+      }
+      dlt = a0 + a1;
+      lse2 = p.lse[size_t(bh) * p.Nq + row] * 1.4426950408889634f;
+      p.delta[size_t(bh) * p.Nq + row] = dlt;
+    }
+    const uint64_t sl2x2 = sm103::f2_pack(sl2, sl2), nl2 = sm103::f2_pack(-lse2, -lse2);
+    bool ok = true;
+    for (int j = 0; j < nk; ++j) {
+      if (!(ok = warp_wait(bar(C::B_SF), uint32_t(j) & 1u, ab))) break;
+      sm103::tc_fence_after();
+      int lim = min(BN - 1, p.Nk - 1 - j * BN);
+      if (CAUSAL) lim = min(lim, row + p.kv_off - j * BN);
+#pragma unroll
+      for (int q = 0; q < BN / 32; ++q) {
+        uint32_t us[32], ud[32];
+        sm103::tmem_ld32(tmem + lane_off + C::COL_S + q * 32, us);
+        sm103::tmem_ld32(tmem + lane_off + C::COL_DP + q * 32, ud);
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const uint64_t t = sm103::f2_fma(sm103::f2_pack(__uint_as_float(us[2 * e]), __uint_as_float(us[2 * e + 1])), sl2x2, nl2);
+          float t0, t1;
+          sm103::f2_unpack(t, t0, t1);
+          const int c = q * 32 + 2 * e;
+          const float p0 = c > lim ? 0.f : sm103::ex2_approx(t0);
+          const float p1 = c + 1 > lim ? 0.f : sm103::ex2_approx(t1);
+          pk[e] = sm103::pack_bf16x2(p0 * (__uint_as_float(ud[2 * e]) - dlt), p1 * (__uint_as_float(ud[2 * e + 1]) - dlt));
+        }
+        sm103::tmem_st16(tmem + lane_off + C::COL_S + q * 16, pk);  // dS over the first 64 columns of S
+      }
+      sm103::tmem_st_wait();
+      sm103::tc_fence_before();
+      sm103::mbar_arrive(bar(C::B_DSF));
+    }
+    if (ok) ok = __all_sync(0xffffffffu, wait_bounded(bar(C::B_QDONE), 0u, ab));
+    if (ok) {
+      sm103::tc_fence_after();
+      // dQ * scale -> bf16 into the idle Q tile (128-byte swizzle layout), then TMA.
+#pragma unroll
+      for (int q = 0; q < D / 32; ++q) {
+        uint32_t v[32];
+        sm103::tmem_ld32(tmem + lane_off + C::COL_DQ + q * 32, v);
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e)
+          pk[e] = sm103::pack_bf16x2(__uint_as_float(v[2 * e]) * p.scale, __uint_as_float(v[2 * e + 1]) * p.scale);
+        const uint32_t rowbase = sQ + uint32_t(q >> 1) * kSubTile + uint32_t(r) * 128u;
+#pragma unroll
+        for (int c4 = 0; c4 < 4; ++c4) {
+          const uint32_t chunk = uint32_t((q & 1) * 4 + c4);
+          sm103::st_shared_v4(rowbase + ((chunk ^ uint32_t(r & 7)) << 4), pk[4 * c4], pk[4 * c4 + 1], pk[4 * c4 + 2],
+                              pk[4 * c4 + 3]);
+        }
+      }
+      sm103::fence_proxy_async_smem();
+    }
+    ok = sm103::named_bar_and(1, BM, ok);
+    if (ok && r == 0) {
+      for (int kb = 0; kb < KB; ++kb) sm103::tma_store_3d(&p.tdq, sQ + kb * kSubTile, kb * 64, m0, bh);
+      sm103::bulk_commit();
+      sm103::bulk_wait_read0();
+    }
+  }
+  sm103::tc_fence_before();
+  __syncthreads();
+  if (warp == kBwdMmaWarp) {
+    sm103::tc_fence_after();
+    sm103::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// --------------------------------------------------------------- dK/dV kernel
+template <int D>
+struct CfgDkv {
+  static constexpr int KB = D / 64;
+  static constexpr uint32_t TILE = KB * kSubTile;
+  static constexpr int NSTAGE = 2;                         // (Q_i, dO_i, LSE, D) stages
+  static constexpr uint32_t OFF_VEC = 1024;                // [NSTAGE][2][128] fp32: LSE*log2e, D
+  static constexpr uint32_t OFF_K = 4096, OFF_V = OFF_K + TILE, OFF_ST = OFF_V + TILE;  // stage s: Q, dO
+  static constexpr uint32_t SMEM = OFF_ST + NSTAGE * 2 * TILE + 1024;
+  static_assert(SMEM <= 232448, "shared memory");
+  static_assert(OFF_VEC + NSTAGE * 2 * 128 * 4 <= OFF_K, "vector area");
+  static constexpr int B_KV = 0, B_SFULL = 1, B_SEMPTY = 1 + NSTAGE, B_SF = 1 + 2 * NSTAGE, B_PF = B_SF + 1,
+                       B_ACC = B_PF + 1, B_DONE = B_ACC + 1, NBAR = B_DONE + 1;
+  static constexpr uint32_t COL_S = 0, COL_DP = 128, COL_DV = 256, COL_DK = 256 + D;
+};
+
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dkdv_sm103(const __grid_constant__ BwdParams p) {
+  using C = CfgDkv<D>;
+  constexpr int KB = C::KB, NSTAGE = C::NSTAGE;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = sm103::smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* const sbase = smem_raw + (base - raw);
+  uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(sbase + 512);
+  volatile uint32_t* const abort_flag = reinterpret_cast<volatile uint32_t*>(sbase + 516);
+  float* const vec = reinterpret_cast<float*>(sbase + C::OFF_VEC);  // [stage][0: lse2, 1: D][128]
+  const uint32_t sK = base + C::OFF_K, sV = base + C::OFF_V, sST = base + C::OFF_ST;
+  auto bar = [base](int i) { return base + 8u * uint32_t(i); };
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  // Causal: key tiles seen by the most queries (the first ones) go first.
+  int kt, bh;
+  if (CAUSAL) {
+    kt = int(blockIdx.x / uint32_t(p.bh));
+    bh = int(blockIdx.x % uint32_t(p.bh));
+  } else {
+    kt = int(blockIdx.x % uint32_t(p.n_ktiles));
+    bh = int(blockIdx.x / uint32_t(p.n_ktiles));
+  }
+  const int n0 = kt * BN;
+  // Query tiles with a query that sees one of these keys (query i sees key n iff n <= i + kv_off).
+  const int it0 = CAUSAL ? max(0, n0 - p.kv_off) / BM : 0;
+  const int niter = max(0, p.n_qtiles - it0);
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < C::NBAR; ++i) {
+      uint32_t cnt = 1;
+      if (i >= C::B_SFULL && i < C::B_SFULL + NSTAGE) cnt = 32;  // the producer warp's lanes
+      if (i == C::B_PF) cnt = BM;
+      sm103::mbar_init(bar(i), cnt);
+    }
+    *abort_flag = 0u;
+    sm103::fence_mbar_init();
+  }
+  if (warp == kBwdMmaWarp) {
+    sm103::tmem_alloc(sm103::smem_u32(tmem_slot), kTmemCols);
+    sm103::tmem_relinquish();
+  }
+  sm103::tc_fence_before();
+  __syncthreads();
+  sm103::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const Abort ab{abort_flag, p.timeout_cycles};
+
+  if (warp == kBwdLoadWarp) {
+    // -------------------------------------------------------------- producer
+    if (lane == 0) {
+      sm103::mbar_arrive_expect_tx(bar(C::B_KV), 2u * C::TILE);
+      for (int kb = 0; kb < KB; ++kb) {
+        sm103::tma_load_3d(sK + kb * kSubTile, &p.tk, bar(C::B_KV), kb * 64, n0, bh);
+        sm103::tma_load_3d(sV + kb * kSubTile, &p.tv, bar(C::B_KV), kb * 64, n0, bh);
+      }
+    }
+    int issued = 0;
+    bool ok = true;
+    for (int it = 0; ok && it < niter; ++it) {
+      const int st = it % NSTAGE;
+      if (it >= NSTAGE && !(ok = warp_wait(bar(C::B_SEMPTY + st), uint32_t(it / NSTAGE - 1) & 1u, ab))) break;
+      const int i0 = (it0 + it) * BM;
+      // Per-query LSE (base 2) and D for this tile; queries past Nq get P = 0.
+#pragma unroll
+      for (int x = 0; x < 4; ++x) {
+        const int col = lane * 4 + x, i = i0 + col;
+        const bool live = i < p.Nq;
+        vec[(st * 2 + 0) * BM + col] = live ? p.lse[size_t(bh) * p.Nq + i] * 1.4426950408889634f : INFINITY;
+        vec[(st * 2 + 1) * BM + col] = live ? p.delta[size_t(bh) * p.Nq + i] : 0.f;
+      }
+      if (lane == 0) {
+        sm103::mbar_arrive_expect_tx(bar(C::B_SFULL + st), 2u * C::TILE);
+        const uint32_t sq = sST + uint32_t(st) * 2u * C::TILE, sdo = sq + C::TILE;
+        for (int kb = 0; kb < KB; ++kb) {
+          sm103::tma_load_3d(sq + kb * kSubTile, &p.tq, bar(C::B_SFULL + st), kb * 64, i0, bh);
+          sm103::tma_load_3d(sdo + kb * kSubTile, &p.tdo, bar(C::B_SFULL + st), kb * 64, i0, bh);
+        }
+      } else {
+        sm103::mbar_arrive(bar(C::B_SFULL + st));
+      }
+      ++issued;
+    }
+    if (lane == 0) {
+      drain_wait(bar(C::B_KV), 0u);
+      for (int t = issued > NSTAGE ? issued - NSTAGE : 0; t < issued; ++t)
+        drain_wait(bar(C::B_SFULL + t % NSTAGE), uint32_t(t / NSTAGE) & 1u);
+    }
+    __syncwarp();
+  } else if (warp == kBwdMmaWarp) {
+    // ------------------------------------------------------------- MMA issue
+    constexpr uint32_t kIdescS = sm103::idesc_bf16_f32(BM, BM, 0, 0);  // S^T, dP^T: both K-major
+    constexpr uint32_t kIdescA = sm103::idesc_bf16_f32(BM, D, 0, 1);   // P^T / dS^T from TMEM, B MN-major
+    const uint64_t dk_k = sm103::sdesc_sw128(sK, 16, 1024), dv_k = sm103::sdesc_sw128(sV, 16, 1024);
+    const uint64_t dst_k = sm103::sdesc_sw128(sST, 16, 1024), dst_mn = sm103::sdesc_sw128(sST, kSubTile, 1024);
+    bool ok = warp_wait(bar(C::B_KV), 0u, ab);
+    for (int it = 0; ok && it < niter; ++it) {
+      const int st = it % NSTAGE;
+      if (!(ok = warp_wait(bar(C::B_SFULL + st), uint32_t(it / NSTAGE) & 1u, ab))) break;
+      sm103::tc_fence_after();
+      const uint64_t soff = uint64_t(uint32_t(st) * 2u * (C::TILE >> 4));
+      const uint64_t q_k = dst_k + soff, do_k = dst_k + soff + (C::TILE >> 4);
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {  // S^T = K Q^T
+        const uint64_t off = uint64_t((uint32_t(kk >> 2) * kSubTile + uint32_t(kk & 3) * 32u) >> 4);
+        sm103::mma_ss_warp(tmem + C::COL_S, dk_k + off, q_k + off, kIdescS, kk > 0 ? 1u : 0u);
+      }
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {  // dP^T = V dO^T
+        const uint64_t off = uint64_t((uint32_t(kk >> 2) * kSubTile + uint32_t(kk & 3) * 32u) >> 4);
+        sm103::mma_ss_warp(tmem + C::COL_DP, dv_k + off, do_k + off, kIdescS, kk > 0 ? 1u : 0u);
+      }
+      sm103::mma_commit_warp(bar(C::B_SF));
+      if (!(ok = warp_wait(bar(C::B_PF), uint32_t(it) & 1u, ab))) break;
+      sm103::tc_fence_after();
+      const uint64_t q_mn = dst_mn + soff, do_mn = dst_mn + soff + (C::TILE >> 4);
+#pragma unroll
+      for (int kk = 0; kk < BM / 16; ++kk) {  // dV += P^T dO, dK += dS^T Q: 16 queries per MMA
+        const uint64_t off = uint64_t(kk * (2048 >> 4));
+        sm103::mma_ts_warp(tmem + C::COL_DV, tmem + C::COL_S + kk * 8, do_mn + off, kIdescA, (it > 0 || kk > 0) ? 1u : 0u);
+        sm103::mma_ts_warp(tmem + C::COL_DK, tmem + C::COL_DP + kk * 8, q_mn + off, kIdescA, (it > 0 || kk > 0) ? 1u : 0u);
+      }
+      sm103::mma_commit_warp(bar(C::B_SEMPTY + st));
+    }
+    sm103::mma_commit_warp(bar(C::B_ACC));
+    sm103::mma_commit_warp(bar(C::B_DONE));
+    drain_wait(bar(C::B_DONE), 0u);
+    __syncwarp();
+  } else {
+    // ----------------------------------------------------------- elementwise
+    const int r = threadIdx.x;
+    const int n = n0 + r;  // this thread's key
+    const uint32_t lane_off = uint32_t(warp * 32) << 16;
+    const uint64_t sl2x2 = sm103::f2_pack(p.scale_log2, p.scale_log2);
+    const bool key_live = n < p.Nk;
+    bool ok = true;
+    for (int it = 0; it < niter; ++it) {
+      const int st = it % NSTAGE;
+      if (!(ok = warp_wait(bar(C::B_SF), uint32_t(it) & 1u, ab))) break;
+      // The stage's LSE and D vectors were written by the producer lanes: wait on
+      // their barrier directly (already complete) to acquire those stores.
+      if (!(ok = warp_wait(bar(C::B_SFULL + st), uint32_t(it / NSTAGE) & 1u, ab))) break;
+      sm103::tc_fence_after();
+      const int i0 = (it0 + it) * BM;
+      // query column c sees this key iff n <= i0 + c + kv_off, i.e. c >= n - kv_off - i0
+      const int cmin = key_live ? (CAUSAL ? n - p.kv_off - i0 : 0) : BM;
+      const float2* lv = reinterpret_cast<const float2*>(vec + (st * 2 + 0) * BM);
+      const float2* dv = reinterpret_cast<const float2*>(vec + (st * 2 + 1) * BM);
+#pragma unroll
+      for (int q = 0; q < BM / 32; ++q) {
+        uint32_t us[32], ud[32];
+        sm103::tmem_ld32(tmem + lane_off + C::COL_S + q * 32, us);
+        sm103::tmem_ld32(tmem + lane_off + C::COL_DP + q * 32, ud);
+        uint32_t pp[16], pd[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const int c = q * 32 + 2 * e;
+          const float2 l2 = lv[c / 2], d2 = dv[c / 2];
+          const uint64_t t = sm103::f2_fma(sm103::f2_pack(__uint_as_float(us[2 * e]), __uint_as_float(us[2 * e + 1])),
+                                           sl2x2, sm103::f2_pack(-l2.x, -l2.y));
+          float t0, t1;
+          sm103::f2_unpack(t, t0, t1);
+          const float p0 = c < cmin ? 0.f : sm103::ex2_approx(t0);
+          const float p1 = c + 1 < cmin ? 0.f : sm103::ex2_approx(t1);
+          pp[e] = sm103::pack_bf16x2(p0, p1);
+          pd[e] = sm103::pack_bf16x2(p0 * (__uint_as_float(ud[2 * e]) - d2.x), p1 * (__uint_as_float(ud[2 * e + 1]) - d2.y));
+        }
+        sm103::tmem_st16(tmem + lane_off + C::COL_S + q * 16, pp);   // P^T over S^T
+        sm103::tmem_st16(tmem + lane_off + C::COL_DP + q * 16, pd);  // dS^T over dP^T
+      }
+      sm103::tmem_st_wait();
+      sm103::tc_fence_before();
+      sm103::mbar_arrive(bar(C::B_PF));
+    }
+    if (ok) ok = __all_sync(0xffffffffu, wait_bounded(bar(C::B_ACC), 0u, ab));
+    if (ok) {
+      sm103::tc_fence_after();
+      // dV -> bf16 into the idle V tile, dK * scale -> bf16 into the idle K tile.
+#pragma unroll
+      for (int w = 0; w < 2; ++w) {
+        const uint32_t col0 = w == 0 ? C::COL_DV : C::COL_DK;
+        const uint32_t stage = w == 0 ? sV : sK;
+        const float mul = w == 0 ? 1.f : p.scale;
+#pragma unroll
+        for (int q = 0; q < D / 32; ++q) {
+          uint32_t v[32];
+          sm103::tmem_ld32(tmem + lane_off + col0 + q * 32, v);
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            pk[e] = sm103::pack_bf16x2(__uint_as_float(v[2 * e]) * mul, __uint_as_float(v[2 * e + 1]) * mul);
+          const uint32_t rowbase = stage + uint32_t(q >> 1) * kSubTile + uint32_t(r) * 128u;
+#pragma unroll
+          for (int c4 = 0; c4 < 4; ++c4) {
+            const uint32_t chunk = uint32_t((q & 1) * 4 + c4);
+            sm103::st_shared_v4(rowbase + ((chunk ^ uint32_t(r & 7)) << 4), pk[4 * c4], pk[4 * c4 + 1], pk[4 * c4 + 2],
+                                pk[4 * c4 + 3]);
+          }
+        }
+      }
+      sm103::fence_proxy_async_smem();
+    }
+    ok = sm103::named_bar_and(1, BM, ok);
+    if (ok && r == 0) {
+      for (int kb = 0; kb < KB; ++kb) {
+        sm103::tma_store_3d(&p.tdv, sV + kb * kSubTile, kb * 64, n0, bh);
+        sm103::tma_store_3d(&p.tdk, sK + kb * kSubTile, kb * 64, n0, bh);
+      }
+      sm103::bulk_commit();
+      sm103::bulk_wait_read0();
+    }
+  }
+  sm103::tc_fence_before();
+  __syncthreads();
+  if (warp == kBwdMmaWarp) {
+    sm103::tc_fence_after();
+    sm103::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+}  // namespace attn

@@ -231,6 +231,8 @@ double attn_fwd_flops(int64_t B, int64_t H, int64_t N, int64_t D, int causal) {
   return causal ? 0.5 * f : f;
 }
 
+double attn_bwd_qk_flops(int64_t B, int64_t H, int64_t Nq, int64_t Nk, int64_t D, int causal);
+
 double attn_fwd_qk_flops(int64_t B, int64_t H, int64_t Nq, int64_t Nk, int64_t D, int causal) {
   // Visible (query, key) pairs: Nq * Nk, or for the bottom-right causal mask
   // (Nk >= Nq) sum over i of (i + 1 + Nk - Nq) = Nq * (Nk - Nq) + Nq (Nq + 1) / 2,
@@ -241,3 +243,8 @@ double attn_fwd_qk_flops(int64_t B, int64_t H, int64_t Nq, int64_t Nk, int64_t D
 }
 
 }  // extern "C"
+#include "attn_bwd_host.cuh"
+
+extern "C" double attn_bwd_qk_flops(int64_t B, int64_t H, int64_t Nq, int64_t Nk, int64_t D, int causal) {
+  return 2.5 * attn_fwd_qk_flops(B, H, Nq, Nk, D, causal);
+}
