@@ -4,7 +4,8 @@ Tolerance (per output X in dQ, dK, dV, and D): with u = 2^-9 the bf16 rounding
 bound, max|X - X_ref| <= 8u * max|X_ref| and mean|X - X_ref| <= 3u * mean|X_ref|.
 The outputs are rounded to bf16 once (<= u each), and P, dS and the forward's
 O (which D is computed from) enter the products in bf16; measured errors sit
-near 2.5u (max) and 1.2u (mean).
+near 2.5u (max) and 1.2u (mean).  The normalisers are floored at 1e-2 for
+references that are exactly zero (N = 1: one key gives P = 1 and dS = 0).
 """
 import math
 
@@ -55,7 +56,10 @@ def assert_grads_close(got, ref, what):
         g, r = got[n], ref[n]
         assert np.all(np.isfinite(g)), f"{what}: {n} has unwritten or non-finite entries"
         err = np.abs(g - r)
-        mx, mean = err.max() / np.abs(r).max(), err.mean() / np.abs(r).mean()
+        # Normalisers floored at 1e-2 (these problems' gradients are O(0.1-1)): with a
+        # single key the references dQ, dK are exactly 0 and the GPU's are rounding noise.
+        mx = err.max() / max(np.abs(r).max(), 1e-2)
+        mean = err.mean() / max(np.abs(r).mean(), 1e-2)
         assert mx <= MAX_REL and mean <= MEAN_REL, f"{what}: {n} max/max={mx:.2e} mean/mean={mean:.2e}"
 
 
