@@ -34,7 +34,7 @@ extern "C" {
 typedef enum {
   ATTN_OK = 0,
   ATTN_ERR_INVALID_ARG = 1, /* null/misaligned/overlapping pointer, bad size or scale */
-  ATTN_ERR_UNSUPPORTED = 2, /* valid request this build does not implement (head dim, device) */
+  ATTN_ERR_UNSUPPORTED = 2, /* valid request this build does not implement (head dim, lengths, device) */
   ATTN_ERR_CUDA = 3,        /* a CUDA runtime or driver call failed (launch, tensor map, ...) */
   ATTN_ERR_TIMEOUT = 4      /* a kernel pipeline wait exceeded its bound and the kernel gave up */
 } attn_status_t;
@@ -52,7 +52,10 @@ typedef enum {
  *           (a ragged last tile is masked).  B, H or N equal to 0 is an empty
  *           problem: ATTN_OK, nothing launched, and the pointers (which may
  *           then be null) are not examined.
- * D       : head dimension, 64 or 128 (others: ATTN_ERR_UNSUPPORTED).
+ * D       : head dimension, a multiple of 8 up to 128 (others:
+ *           ATTN_ERR_UNSUPPORTED).  Below 64 or 128 the computation runs at
+ *           that width with zero padding (the padding is never read from or
+ *           written to memory).
  * causal  : nonzero -> key j is visible to query i only when j <= i.
  * scale   : softmax scale applied to the logits, finite and > 0 (usually
  *           1/sqrt(D)).
@@ -60,7 +63,8 @@ typedef enum {
  *
  * The caller owns every buffer.  Argument errors return synchronously with
  * nothing launched: ATTN_ERR_INVALID_ARG, or ATTN_ERR_UNSUPPORTED for a head
- * dimension other than 64/128 or a device that is not sm_103.  A failed
+ * dimension that is not a multiple of 8 up to 128, or a device that is not
+ * sm_103.  A failed
  * launch returns ATTN_ERR_CUDA.  A kernel that hits a pipeline timeout does
  * not trap: it records ATTN_ERR_TIMEOUT in a device status word that
  * attn_last_status reports; its outputs are then unspecified.

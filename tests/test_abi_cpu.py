@@ -56,15 +56,23 @@ def test_bad_sizes_and_scale(lib):
 
 
 def test_unsupported_head_dims(lib):
-    for d in (16, 32, 96, 256):
+    for d in (4, 12, 100, 136, 192, 256):
         assert call(D=d) == pkg.ATTN_ERR_UNSUPPORTED
+
+
+def test_padded_head_dims_pass_validation(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    for d in (8, 32, 48, 96, 112):
+        assert call(D=d) == pkg.ATTN_ERR_CUDA  # past validation, stopped only by the missing device
 
 
 def test_empty_problem_is_a_no_op(lib):
     for kw in ({"B": 0}, {"H": 0}, {"N": 0}):
         assert call(**kw) == pkg.ATTN_OK
         assert call(q=None, k=None, v=None, o=None, lse=None, **kw) == pkg.ATTN_OK
-    assert call(B=0, D=96) == pkg.ATTN_ERR_UNSUPPORTED
+    assert call(B=0, D=100) == pkg.ATTN_ERR_UNSUPPORTED
     assert call(B=0, scale=-1.0) == pkg.ATTN_ERR_INVALID_ARG
 
 

@@ -107,3 +107,10 @@ def test_backward_argument_errors():
     assert pkg.attn_bwd_qk(x, x, x, x, f, x, *outs, torch.empty_like(f), 1, 1, 256, 128, 64, True, 0.125, s) \
         == pkg.ATTN_ERR_UNSUPPORTED  # causal with more queries than keys
     assert pkg.attn_last_status(s) == pkg.ATTN_OK
+
+
+@pytest.mark.parametrize("D", [8, 32, 96, 112])
+@pytest.mark.parametrize("causal", [False, True])
+def test_backward_padded_head_dims(D, causal):
+    got, ref = grads(1, 3, 300, 300, D, causal, seed=1700 + D)
+    assert_grads_close(got, ref, f"D={D} causal={causal}")

@@ -189,7 +189,7 @@ def test_boundary_errors_with_real_buffers():
     s = torch.cuda.current_stream()
     assert pkg.attn_fwd(q.data_ptr() + 2, q, q, o, lse, 1, 1, 255, 64, False, 0.125, s) == pkg.ATTN_ERR_INVALID_ARG
     assert pkg.attn_fwd(q, q, q, q, lse, 1, 1, 256, 64, False, 0.125, s) == pkg.ATTN_ERR_INVALID_ARG
-    assert pkg.attn_fwd(q, q, q, o, lse, 1, 1, 256, 96, False, 0.125, s) == pkg.ATTN_ERR_UNSUPPORTED
+    assert pkg.attn_fwd(q, q, q, o, lse, 1, 1, 256, 100, False, 0.125, s) == pkg.ATTN_ERR_UNSUPPORTED
     assert pkg.attn_last_status(s) == pkg.ATTN_OK
 
 
@@ -243,3 +243,15 @@ def test_fwd_wrapper_with_a_key_cache():
     o, lse = pkg.fwd(to_dev(q), to_dev(k), to_dev(v), causal=True)
     o_ref, lse_ref = oracle.attn_fwd(q, k, v, True, 0.125)
     assert_close(o_to_f64(o), lse.cpu().numpy().astype(np.float64), o_ref, lse_ref, "fwd() Nq=256 Nk=1500")
+
+
+@pytest.mark.parametrize("D", [8, 32, 48, 96, 112])
+@pytest.mark.parametrize("causal", [False, True])
+def test_padded_head_dims(D, causal, tiles_per_cta):
+    q, k, v = make_qkv(2, 3, 333, D, seed=1600 + D)
+    full_check(q, k, v, causal, 1.0 / math.sqrt(D), f"D={D} causal={causal} T={tiles_per_cta}")
+    qr, _, _ = make_qkv(1, 2, 100, D, seed=1601 + D)
+    _, kr, vr = make_qkv(1, 2, 450, D, seed=1602 + D)
+    o, lse = run_qk(qr, kr, vr, causal, 0.3)
+    o_ref, lse_ref = oracle.attn_fwd(qr, kr, vr, causal, 0.3)
+    assert_close(o, lse, o_ref, lse_ref, f"Nq=100 Nk=450 D={D} causal={causal}")

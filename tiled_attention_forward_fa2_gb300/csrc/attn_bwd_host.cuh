@@ -44,7 +44,7 @@ attn_status_t launch_bwd(const void* q, const void* k, const void* v, const void
                          int64_t Nq, int64_t Nk, int64_t D, int causal, float scale, void* stream) {
   if (B < 0 || H < 0 || Nq < 0 || Nk < 0 || D <= 0) return ATTN_ERR_INVALID_ARG;
   if (!(scale > 0.f) || !std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
-  if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
+  if (D > 128 || D % 8 != 0) return ATTN_ERR_UNSUPPORTED;
   if (B == 0 || H == 0 || (Nq == 0 && Nk == 0)) return ATTN_OK;  // nothing is read or written
   // Nq = 0 leaves dK = dV = 0 and Nk = 0 leaves rows without keys: neither is
   // produced by these kernels.
@@ -97,12 +97,13 @@ attn_status_t launch_bwd(const void* q, const void* k, const void* v, const void
   prm.bh = int(BH);
   prm.n_qtiles = int(n_qtiles);
   prm.n_ktiles = int(n_ktiles);
+  prm.d = int(D);
   prm.scale = scale;
   prm.scale_log2 = scale * 1.4426950408889634f;
   prm.timeout_cycles = timeout_cycles();
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t err;
-  if (D == 64)
+  if (D <= 64)  // padded to 64 or 128 as in the forward
     err = causal ? launch_bwd_kernels<64, true>(prm, st) : launch_bwd_kernels<64, false>(prm, st);
   else
     err = causal ? launch_bwd_kernels<128, true>(prm, st) : launch_bwd_kernels<128, false>(prm, st);

@@ -35,6 +35,7 @@ struct BwdParams {
   const float* lse;             // [B*H, Nq] natural log
   float* delta;                 // [B*H, Nq] D_i: written by the dQ kernel, read by the dK/dV kernel
   int Nq, Nk, kv_off, bh, n_qtiles, n_ktiles;
+  int d;                        // true head dim (<= the kernel's D; the rest is zero padding)
   float scale;                  // softmax scale
   float scale_log2;             // scale * log2(e)
   long long timeout_cycles;
@@ -174,11 +175,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dq_sm103(const __grid
     // D_i = dO_i . O_i and the row's LSE in base 2 (rows past Nq: P = 0).
     float dlt = 0.f, lse2 = INFINITY;
     if (row < p.Nq) {
-      const uint4* po = reinterpret_cast<const uint4*>(p.o + (size_t(bh) * p.Nq + row) * D);
-      const uint4* pd = reinterpret_cast<const uint4*>(p.dout + (size_t(bh) * p.Nq + row) * D);
+      const uint4* po = reinterpret_cast<const uint4*>(p.o + (size_t(bh) * p.Nq + row) * size_t(p.d));
+      const uint4* pd = reinterpret_cast<const uint4*>(p.dout + (size_t(bh) * p.Nq + row) * size_t(p.d));
       float a0 = 0.f, a1 = 0.f;
 #pragma unroll 4
-      for (int x = 0; x < D / 8; ++x) {
+      for (int x = 0; x < p.d / 8; ++x) {
         const uint4 uo = po[x], ud = pd[x];
         const uint32_t wo[4] = {uo.x, uo.y, uo.z, uo.w}, wd[4] = {ud.x, ud.y, ud.z, ud.w};
 #pragma unroll

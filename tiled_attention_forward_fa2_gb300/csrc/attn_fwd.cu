@@ -112,7 +112,7 @@ attn_status_t launch_fwd(const void* q, const void* k, const void* v, void* o, f
                          int64_t Nq, int64_t Nk, int64_t D, int causal, float scale, void* stream) {
   if (B < 0 || H < 0 || Nq < 0 || Nk < 0 || D <= 0) return ATTN_ERR_INVALID_ARG;
   if (!(scale > 0.f) || !std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
-  if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
+  if (D > 128 || D % 8 != 0) return ATTN_ERR_UNSUPPORTED;
   if (B == 0 || H == 0 || Nq == 0) return ATTN_OK;  // nothing is read or written
   // Query rows that see no key at all (Nk = 0, or causal with Nq > Nk) are not
   // produced by the kernel.
@@ -183,7 +183,10 @@ attn_status_t launch_fwd(const void* q, const void* k, const void* v, void* o, f
   const int64_t ctas = int64_t(prm.n_units) * BH;
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t err;
-  if (D == 64)
+  // Head dims below 64 or 128 run on that kernel: the tensor maps carry the true
+  // D, so TMA fills the missing columns with zeros on load (they add nothing to
+  // Q K^T, and P V gives zeros there) and leaves them out on store.
+  if (D <= 64)
     err = causal ? launch<64, true>(prm, ctas, st) : launch<64, false>(prm, ctas, st);
   else
     err = causal ? launch<128, true>(prm, ctas, st) : launch<128, false>(prm, ctas, st);
