@@ -83,16 +83,23 @@ def tiles_per_cta(request, monkeypatch):
     return int(request.param)
 
 
+@pytest.fixture(params=["0", "1"], ids=["one_unit_per_cta", "persistent"])
+def schedule(request, monkeypatch):
+    """Force the launcher's grid: one CTA per unit, or one CTA per SM walking the units."""
+    monkeypatch.setenv("ATTN_PERSISTENT", request.param)
+    return int(request.param)
+
+
 @pytest.mark.parametrize("D", [64, 128])
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("N", [1, 2, 17, 127, 128, 129, 200, 383, 640])
-def test_ragged_and_tiny_lengths(N, D, causal, tiles_per_cta):
+def test_ragged_and_tiny_lengths(N, D, causal, tiles_per_cta, schedule):
     q, k, v = make_qkv(2, 3, N, D, seed=500 + N + D)
     full_check(q, k, v, causal, 1.0 / math.sqrt(D), f"N={N} D={D} causal={causal} T={tiles_per_cta}")
 
 
 @pytest.mark.parametrize("D", [64, 128])
-def test_large_logits_stress_rescaling(D, tiles_per_cta):
+def test_large_logits_stress_rescaling(D, tiles_per_cta, schedule):
     # Q spread 8x: logits up to ~40 in magnitude; the running max moves often.
     q, k, v = make_qkv(1, 4, 1000, D, seed=77, q_std=8.0)
     for causal in (False, True):
@@ -100,10 +107,35 @@ def test_large_logits_stress_rescaling(D, tiles_per_cta):
 
 
 @pytest.mark.parametrize("name", SMALL)
-def test_workload_full_both_tilings(name, tiles_per_cta):
+def test_workload_full_both_tilings(name, tiles_per_cta, schedule):
     w = WORKLOADS[name]
     q, k, v = w.qkv()
     full_check(q, k, v, w.causal, w.scale, f"{name} T={tiles_per_cta}")
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("N", [640, 333])
+def test_many_units_per_cta(N, D, causal, tiles_per_cta, monkeypatch):
+    """Persistent grid with several units per CTA (B*H*units well above the SM
+    count): every unit's Q load, P V restart and epilogue reuse the buffers of
+    the unit before.  Heads of different lengths' worth of work in causal order."""
+    monkeypatch.setenv("ATTN_PERSISTENT", "1")
+    q, k, v = make_qkv(4, 100, N, D, seed=900 + N + D)
+    full_check(q, k, v, causal, 1.0 / math.sqrt(D), f"N={N} D={D} causal={causal} T={tiles_per_cta} persistent")
+
+
+def test_persistent_long_keys_sampled(monkeypatch):
+    """The bench shape forced onto the persistent grid: 1024 units over the SMs."""
+    monkeypatch.setenv("ATTN_PERSISTENT", "1")
+    w = WORKLOADS["b4h16n4096d128"]
+    q, k, v = w.qkv()
+    o, lse = run(q, k, v, w.causal, w.scale)
+    assert np.all(np.isfinite(o)) and np.all(np.isfinite(lse)), "unwritten or non-finite output"
+    bh, ri = sampled_rows(w.B * w.H, w.N, 512, w.seed + 1)
+    o_ref, lse_ref = oracle.attn_rows(q, k, v, w.causal, w.scale, bh, ri)
+    assert_close(o.reshape(w.B * w.H, w.N, w.D)[bh, ri], lse.reshape(w.B * w.H, w.N)[bh, ri], o_ref, lse_ref,
+                 "b4h16n4096d128 persistent")
 
 
 def test_identical_keys_give_mean_of_v():
@@ -221,7 +253,7 @@ def run_qk(q, k, v, causal, scale):
     (1, 1000, True), (1, 1000, False), (17, 300, True), (128, 4096, True), (200, 333, True),
     (300, 300, True), (700, 129, False), (1000, 77, False), (384, 2048, False),
 ])
-def test_queries_and_keys_of_different_lengths(Nq, Nk, causal, D, tiles_per_cta):
+def test_queries_and_keys_of_different_lengths(Nq, Nk, causal, D, tiles_per_cta, schedule):
     q, _, _ = make_qkv(2, 3, Nq, D, seed=900 + Nq)
     _, k, v = make_qkv(2, 3, Nk, D, seed=901 + Nk)
     scale = 1.0 / math.sqrt(D)
@@ -247,7 +279,7 @@ def test_fwd_wrapper_with_a_key_cache():
 
 @pytest.mark.parametrize("D", [8, 32, 48, 96, 112])
 @pytest.mark.parametrize("causal", [False, True])
-def test_padded_head_dims(D, causal, tiles_per_cta):
+def test_padded_head_dims(D, causal, tiles_per_cta, schedule):
     q, k, v = make_qkv(2, 3, 333, D, seed=1600 + D)
     full_check(q, k, v, causal, 1.0 / math.sqrt(D), f"D={D} causal={causal} T={tiles_per_cta}")
     qr, _, _ = make_qkv(1, 2, 100, D, seed=1601 + D)

@@ -56,7 +56,10 @@ std::mutex g_dev_mutex;
 
 template <int D, bool CAUSAL>
 cudaError_t opt_in_smem() {
-  return cudaFuncSetAttribute(attn::attn_fwd_sm103<D, CAUSAL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(attn::attn_fwd_sm103<D, CAUSAL, false>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, int(attn::Cfg<D>::SMEM));
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(attn::attn_fwd_sm103<D, CAUSAL, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               int(attn::Cfg<D>::SMEM));
 }
 
@@ -92,6 +95,13 @@ bool ranges_overlap(const void* a, uint64_t na, const void* b, uint64_t nb) {
   return x < y + nb && y < x + na;
 }
 
+// Key tiles (of 128) up to which the persistent grid is used.  It saves about
+// 3.5 us of launch, Q load and epilogue per unit and costs about 6 % of the
+// key loop's speed (1.55 us per key tile of a two-tile unit at D = 128): even
+// at about 38 tiles; measured on GB300, 32 tiles (N = 4096) still gains and
+// 128 (N = 16384) loses 6 %.
+constexpr int64_t kPersistMaxKeyTiles = 32;
+
 long long timeout_cycles() {
   // About two seconds at the GB300 clock; no legitimate wait comes near it.
   // ATTN_WAIT_LIMIT_CYCLES (read at every call) lowers it, e.g. to test the
@@ -102,8 +112,11 @@ long long timeout_cycles() {
 }
 
 template <int D, bool CAUSAL>
-cudaError_t launch(const attn::FwdParams& prm, int64_t ctas, cudaStream_t stream) {
-  attn::attn_fwd_sm103<D, CAUSAL><<<dim3(unsigned(ctas)), dim3(attn::kThreads), attn::Cfg<D>::SMEM, stream>>>(prm);
+cudaError_t launch(const attn::FwdParams& prm, int64_t ctas, bool persist, cudaStream_t stream) {
+  if (persist)
+    attn::attn_fwd_sm103<D, CAUSAL, true><<<dim3(unsigned(ctas)), dim3(attn::kThreads), attn::Cfg<D>::SMEM, stream>>>(prm);
+  else
+    attn::attn_fwd_sm103<D, CAUSAL, false><<<dim3(unsigned(ctas)), dim3(attn::kThreads), attn::Cfg<D>::SMEM, stream>>>(prm);
   return cudaGetLastError();
 }
 
@@ -180,16 +193,27 @@ attn_status_t launch_fwd(const void* q, const void* k, const void* v, void* o, f
   const char* wh = std::getenv("ATTN_TEST_WITHHOLD_KV");
   prm.withhold_kv = (wh && wh[0] == '1') ? 1 : 0;
 
-  const int64_t ctas = int64_t(prm.n_units) * BH;
+  prm.n_work = int(int64_t(prm.n_units) * BH);
+  // Short key ranges: a persistent grid (one CTA per SM taking every gridDim-th
+  // unit) overlaps each unit's Q load and epilogue with the previous unit's
+  // work.  Long ones: one CTA per unit, whose key loop runs faster (see the
+  // kernel) and whose launch cost is small beside the unit.
+  // ATTN_PERSISTENT=0|1 forces the choice (testing and tuning).
+  bool persist = n_ktiles <= kPersistMaxKeyTiles;
+  if (const char* e = std::getenv("ATTN_PERSISTENT")) {
+    if (e[0] == '0' && e[1] == 0) persist = false;
+    if (e[0] == '1' && e[1] == 0) persist = true;
+  }
+  const int64_t ctas = persist && prm.n_work > sms ? sms : prm.n_work;
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t err;
   // Head dims below 64 or 128 run on that kernel: the tensor maps carry the true
   // D, so TMA fills the missing columns with zeros on load (they add nothing to
   // Q K^T, and P V gives zeros there) and leaves them out on store.
   if (D <= 64)
-    err = causal ? launch<64, true>(prm, ctas, st) : launch<64, false>(prm, ctas, st);
+    err = causal ? launch<64, true>(prm, ctas, persist, st) : launch<64, false>(prm, ctas, persist, st);
   else
-    err = causal ? launch<128, true>(prm, ctas, st) : launch<128, false>(prm, ctas, st);
+    err = causal ? launch<128, true>(prm, ctas, persist, st) : launch<128, false>(prm, ctas, persist, st);
   return err == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 

@@ -11,11 +11,16 @@
 // Hardware mapping.  The pages' H100 design (wgmma into registers, TMA,
 // swizzled shared memory; "GPUの爆発的な性能向上", ja.news.hada.io topic 14783,
 // sections "WGMMA", "Shared memoryとbank conflict", "アドレス生成とTMA",
-// "Occupancyが隠してくれるコスト") is prior art.  Here a CTA owns T = 1 or 2
-// query tiles of 128 rows of one (batch, head) and streams that head's K and
-// V tiles once for both:
-//   warp 12      : TMA producer.  Q tiles once; K_j, V_j into a ring of
-//                  128-byte-swizzled shared-memory slots (full/empty mbarriers).
+// "Occupancyが隠してくれるコスト") is prior art.  The work is cut into units of
+// T = 1 or 2 query tiles of 128 rows of one (batch, head); a unit streams that
+// head's K and V tiles once for its tiles.  The grid is persistent: each CTA
+// (one per SM) takes units w = blockIdx.x, blockIdx.x + gridDim.x, ... and
+// every role runs through the same sequence, so one unit's epilogue and the
+// next unit's loads overlap the tensor-core work instead of a CTA launch.
+//   warp 12      : TMA producer.  Q tiles of each unit (into the tile's buffer
+//                  once the previous unit's last S MMA on it has finished);
+//                  K_j, V_j into a ring of 128-byte-swizzled shared-memory
+//                  slots (full/empty mbarriers).
 //   warp 13      : allocates the 512 TMEM columns; one thread issues tcgen05.mma:
 //                  S_i = Q_i K_j^T into TMEM buffer i, and O_i += P_i V_j with P_i
 //                  read back from TMEM (bf16, written over S_i).  The order
@@ -26,10 +31,10 @@
 //                  p = 2^(s*scale*log2e - m) with packed fp32x2 math, P -> TMEM,
 //                  running sum.  The reference max m only moves when a row's max
 //                  grows by more than 2^8; rescale factors go to TMEM for the
-//                  correction warps; the LSE is written at the end.
+//                  correction warps; 1/l goes to shared memory; LSE to global.
 //   warpgroup 2  : (warps 8..11) correction: O_i *= alpha in TMEM between PV
 //                  steps (skipped when no row of the warp moved its max);
-//                  epilogue O_i / l -> bf16 -> swizzled shared memory -> TMA store.
+//                  epilogue O_i / l -> bf16 -> swizzled staging tile -> TMA store.
 // Every barrier wait is bounded: on expiry the kernel records a timeout in a
 // device status word, the other roles see a shared abort flag, in-flight TMA
 // copies and MMAs are drained, TMEM is freed and the CTA returns.
@@ -52,9 +57,10 @@ constexpr uint32_t kSubTile = 128u * 128u;  // 128 rows x 64 bf16 (one 128-B swi
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleLog2 = 8.0f;        // move the reference max only when it grows by > 2^8
 constexpr int kStatusTimeout = 4;           // value of ATTN_ERR_TIMEOUT
-// Register split (setmaxnreg): 2 x 128 softmax threads at 176, 128 correction
-// threads at 80, 128 load/MMA/idle threads at 80 = 65536 = 512 threads x 128.
-constexpr uint32_t kRegSoftmax = 176, kRegCorr = 80, kRegOther = 80;
+// Register split (setmaxnreg): 2 x 128 softmax threads at 168, 128 correction
+// threads at 96, 128 load/MMA/idle threads at 80 = 65536 = 512 threads x 128
+// (each the smallest count at which its role compiles without spills).
+constexpr uint32_t kRegSoftmax = 168, kRegCorr = 96, kRegOther = 80;
 static_assert(2 * 128 * kRegSoftmax + 128 * kRegCorr + 128 * kRegOther == kThreads * 128, "register split");
 
 struct FwdParams {
@@ -64,8 +70,9 @@ struct FwdParams {
   int kv_off;                  // Nk - Nq: causal key j is visible to query i iff j <= i + kv_off
   int bh;                      // B*H
   int n_qtiles, n_ktiles;      // ceil(Nq / 128), ceil(Nk / 128)
-  int tiles_per_cta;           // T = 1 or 2 query tiles per CTA
-  int n_units;                 // ceil(n_qtiles / T): CTAs per (batch, head)
+  int tiles_per_cta;           // T = 1 or 2 query tiles per unit
+  int n_units;                 // ceil(n_qtiles / T): units per (batch, head)
+  int n_work;                  // n_units * B*H: units of the whole problem
   float scale_log2;            // scale * log2(e)
   long long timeout_cycles;
   int withhold_kv;             // test hook: nonzero -> no K/V loads are issued, so the pipeline waits run out
@@ -76,31 +83,71 @@ struct Cfg {
   static_assert(D == 64 || D == 128, "head dim");
   static constexpr int KB = D / 64;                      // 64-column sub-tiles per tile
   static constexpr uint32_t TILE = KB * kSubTile;        // bytes of one 128 x D bf16 tile
-  static constexpr int NSLOT = D == 128 ? 5 : 10;        // K/V ring slots (one tile each)
-  static constexpr uint32_t OFF_Q = 1024;                // first 1 KB: barriers and flags
-  static constexpr uint32_t OFF_KV = OFF_Q + 2 * TILE;
+  static constexpr int NSLOT = D == 128 ? 4 : 11;        // K/V ring slots (one tile each)
+  static constexpr uint32_t OFF_INVL = 1024;             // [2][128] fp32: 1/l of each row of tile i
+  static constexpr uint32_t OFF_Q = 2048;                // Q_0, Q_1
+  static constexpr uint32_t OFF_STG = OFF_Q + 2 * TILE;  // O staging tile of the TMA store
+  static constexpr uint32_t OFF_KV = OFF_STG + TILE;
   static constexpr uint32_t USED = OFF_KV + NSLOT * TILE;
   static constexpr uint32_t SMEM = USED + 1024;          // + slack to align the base to 1 KB
   static_assert(SMEM <= 232448, "shared memory");
-  // barrier slots
-  static constexpr int B_Q = 0, B_FULL = 1, B_EMPTY = 1 + NSLOT;
-  static constexpr int B_SF = 1 + 2 * NSLOT;  // [2] scores of tile i ready (MMA commit)
-  static constexpr int B_PF = B_SF + 2;       // [2] P of tile i in TMEM (128 softmax threads)
-  static constexpr int B_AR = B_PF + 2;       // [2] per-step rescale factor in TMEM (128 softmax threads)
-  static constexpr int B_OR = B_AR + 2;       // [2] O of tile i rescaled (128 correction threads)
-  static constexpr int B_OF = B_OR + 2;       // [2] O_i += P_i V_j finished (MMA commit)
-  // [2] final 1/l in TMEM (128 softmax threads).  Kept apart from B_AR: the
-  // final hand-off follows the last step's factor without waiting for the
-  // correction warps, so on one barrier it could run two phases ahead of them.
+  // barrier slots ([2]: one per query tile of the unit)
+  static constexpr int B_Q = 0;                  // [2] Q_i landed (TMA bytes)
+  static constexpr int B_QE = 2;                 // [2] last S MMA on Q_i of the unit finished (MMA commit)
+  static constexpr int B_FULL = 4, B_EMPTY = 4 + NSLOT;
+  static constexpr int B_SF = 4 + 2 * NSLOT;     // [2] scores of tile i ready (MMA commit)
+  static constexpr int B_PF = B_SF + 2;          // [2] P of tile i in TMEM (128 softmax threads)
+  static constexpr int B_AR = B_PF + 2;          // [2] per-step rescale factor in TMEM (128 softmax threads)
+  static constexpr int B_OR = B_AR + 2;          // [2] O of tile i rescaled (128 correction threads)
+  static constexpr int B_OF = B_OR + 2;          // [2] O_i += P_i V_j finished (MMA commit)
+  // [2] final 1/l in shared memory (128 softmax threads).  Kept apart from
+  // B_AR: the final hand-off follows the last step's factor without waiting
+  // for the correction warps, so on one barrier it could run two phases ahead.
   static constexpr int B_FIN = B_OF + 2;
-  static constexpr int B_DONE = B_FIN + 2;
+  static constexpr int B_OE = B_FIN + 2;         // [2] epilogue has read O_i and 1/l (128 correction threads)
+  static constexpr int B_DONE = B_OE + 2;
   static constexpr int NBAR = B_DONE + 1;
   static_assert(NBAR * 8 <= 512, "barrier area");
   // TMEM columns
   static constexpr uint32_t COL_S = 0;     // S_i at COL_S + 128 i (P_i over its first 64 columns)
   static constexpr uint32_t COL_O = 256;   // O_i at COL_O + D i
-  static constexpr uint32_t COL_ALPHA = 64, COL_INVL = 65;  // inside S_i, above P_i
+  static constexpr uint32_t COL_ALPHA = 64;  // inside S_i, above P_i
+  __host__ __device__ static constexpr bool count128(int b) {  // barriers completed by 128 thread arrivals
+    return (b >= B_PF && b < B_OR + 2) || (b >= B_FIN && b < B_OE + 2);
+  }
 };
+
+// The unit a CTA works on: query tiles t0 (and t0 + 1), key tiles nk0 (nk1)
+// visited by them; nk1 = 0 when the unit has one tile.  Causal: heaviest units
+// first (longest-processing-time order over all heads).  Full: the units of one
+// head are adjacent, so CTAs working at the same time share its K and V in L2.
+struct Unit {
+  int t0, bh, nk0, nk1;
+  __device__ __forceinline__ int nk() const { return max(nk0, nk1); }
+};
+
+template <bool CAUSAL>
+__device__ __forceinline__ Unit unit_of(const FwdParams& p, int w) {
+  Unit u;
+  int unit;
+  if (CAUSAL) {
+    unit = p.n_units - 1 - w / p.bh;
+    u.bh = w % p.bh;
+  } else {
+    unit = w % p.n_units;
+    u.bh = w / p.n_units;
+  }
+  u.t0 = unit * p.tiles_per_cta;
+  // Causal: key tiles up to the one of the tile's last query row (past Nq: row Nq-1).
+  auto tiles = [&](int t) {
+    if (!CAUSAL) return p.n_ktiles;
+    const int last_row = min(t * BM + BM - 1, p.Nq - 1);
+    return min(p.n_ktiles, (last_row + p.kv_off) / BN + 1);
+  };
+  u.nk0 = tiles(u.t0);
+  u.nk1 = (p.tiles_per_cta == 2 && u.t0 + 1 < p.n_qtiles) ? tiles(u.t0 + 1) : 0;
+  return u;
+}
 
 __device__ int g_attn_status;  // 0 or kStatusTimeout; read and cleared by the host
 
@@ -148,7 +195,7 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const A
   return __all_sync(0xffffffffu, wait_bounded(bar, parity, ab));
 }
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool PERSIST>
 __global__ void __launch_bounds__(kThreads, 1) attn_fwd_sm103(const __grid_constant__ FwdParams p) {
   using C = Cfg<D>;
   constexpr int KB = C::KB;
@@ -160,42 +207,31 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_sm103(const __grid_const
   uint8_t* const sbase = smem_raw + (base - raw);
   uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(sbase + 512);
   volatile uint32_t* const abort_flag = reinterpret_cast<volatile uint32_t*>(sbase + 516);
-  const uint32_t sQ = base + C::OFF_Q;   // Q_i at sQ + i * TILE (later: O_i staging)
-  const uint32_t sKV = base + C::OFF_KV; // slot s at sKV + s * TILE
+  float* const invl = reinterpret_cast<float*>(sbase + C::OFF_INVL);  // [2][128]
+  const uint32_t sQ = base + C::OFF_Q;      // Q_i at sQ + i * TILE
+  const uint32_t sStg = base + C::OFF_STG;  // O staging tile
+  const uint32_t sKV = base + C::OFF_KV;    // slot s at sKV + s * TILE
   auto bar = [base](int i) { return base + 8u * uint32_t(i); };
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-
-  // Work of this CTA.  Causal: heaviest units first (longest-processing-time
-  // order across all heads).  Full: the units of one head are adjacent so its
-  // K and V stay hot in L2.
-  const int T = p.tiles_per_cta;
-  int unit, bh;
-  if (CAUSAL) {
-    unit = p.n_units - 1 - int(blockIdx.x / uint32_t(p.bh));
-    bh = int(blockIdx.x % uint32_t(p.bh));
-  } else {
-    unit = int(blockIdx.x % uint32_t(p.n_units));
-    bh = int(blockIdx.x / uint32_t(p.n_units));
-  }
-  const int t0 = unit * T;
-  // Key tiles visited by query tile 0 and 1 (0 when the CTA has one tile).
-  // Causal: up to the key tile of the tile's last query row (past Nq: row Nq-1).
-  auto causal_tiles = [&](int t) {
-    const int last_row = min(t * BM + BM - 1, p.Nq - 1);
-    return min(p.n_ktiles, (last_row + p.kv_off) / BN + 1);
-  };
-  const int nk0 = CAUSAL ? causal_tiles(t0) : p.n_ktiles;
-  const int nk1 = T == 2 ? (CAUSAL ? causal_tiles(t0 + 1) : p.n_ktiles) : 0;
-  const int nk = max(nk0, nk1);
+  // Units of this CTA: round k takes unit k G + c for even k and k G + (G - 1 - c)
+  // for odd k (G = gridDim.x, c = blockIdx.x).  Units are numbered heaviest
+  // first when causal, so the snake order pairs heavy and light rounds and the
+  // CTAs' totals stay level.
+  // Without PERSIST the grid has one CTA per unit and every loop over units
+  // below runs once; the compiler then lays the MMA warp's key loop out as a
+  // single loop, which keeps its issue rate (about 6 % more throughput on long
+  // key ranges than the same loop nested in a unit loop).
+  const int w0 = int(blockIdx.x), dw = int(gridDim.x);
+  auto work = [w0, dw](int k) { return k * dw + ((k & 1) ? dw - 1 - w0 : w0); };
+  // Rounds of units per CTA; the bound is written as k < kRounds (not k == 0):
+  // the compiler only collapses the loops for the former.
+  constexpr int kRounds = PERSIST ? 0x7fffffff : 1;
+  auto more = [&](int k) { return work(k) < p.n_work; };
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < C::NBAR; ++i) {
-      uint32_t cnt = 1;
-      if ((i >= C::B_PF && i < C::B_OR + 2) || i == C::B_FIN || i == C::B_FIN + 1) cnt = BM;  // 128 threads
-      sm103::mbar_init(bar(i), cnt);
-    }
+    for (int i = 0; i < C::NBAR; ++i) sm103::mbar_init(bar(i), C::count128(i) ? uint32_t(BM) : 1u);
     *abort_flag = 0u;
     sm103::fence_mbar_init();
   }
@@ -215,29 +251,52 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_sm103(const __grid_const
   const uint32_t tmem = *tmem_slot;
   const Abort ab{abort_flag, p.timeout_cycles};
 
+  // Phase bookkeeping.  Every role walks the same units; per query tile i it
+  // counts the units that used tile i (phases of B_Q, B_QE, B_FIN, B_OE) and
+  // their key steps (B_SF, B_PF, B_OF).  Each unit has one rescale step fewer
+  // than key steps (j >= 1: B_AR, B_OR), so those number steps - units.
   if (warp >= kLoadWarp) {
     sm103::regs_decrease<kRegOther>();
     if (warp == kLoadWarp) {
       // ---------------------------------------------------------- producer
       if (lane == 0) {
-        sm103::mbar_arrive_expect_tx(bar(C::B_Q), uint32_t(T) * C::TILE);
-        for (int i = 0; i < T; ++i)
-          for (int kb = 0; kb < KB; ++kb)
-            sm103::tma_load_3d(sQ + i * C::TILE + kb * kSubTile, &p.tq, bar(C::B_Q), kb * 64, (t0 + i) * BM, bh);
-        int c = 0;  // loads issued; K_j is load 2j, V_j load 2j+1
+        int c = 0;            // K/V loads issued; K_j of a unit is load cb + 2j, V_j load cb + 2j + 1
+        int nq0 = 0, nq1 = 0;  // Q loads issued into buffer 0 / 1
         bool ok = true;
-        for (int j = 0; ok && !p.withhold_kv && j < nk; ++j) {
-          for (int kv = 0; kv < 2; ++kv, ++c) {
-            const int s = c % NSLOT;
-            if (c >= NSLOT && !(ok = wait_bounded(bar(C::B_EMPTY + s), uint32_t(c / NSLOT - 1) & 1u, ab))) break;
-            sm103::mbar_arrive_expect_tx(bar(C::B_FULL + s), C::TILE);
-            const CUtensorMap* map = kv == 0 ? &p.tk : &p.tv;
+        for (int k = 0; k < kRounds && ok && more(k); ++k) {
+          const Unit u = unit_of<CAUSAL>(p, work(k));
+          // Buffer i is free once the previous unit's last S MMA reading it has finished.
+          auto load_q = [&](int i, int nq) -> bool {
+            if (nq > 0 && !wait_bounded(bar(C::B_QE + i), uint32_t(nq - 1) & 1u, ab)) return false;
+            sm103::mbar_arrive_expect_tx(bar(C::B_Q + i), C::TILE);
             for (int kb = 0; kb < KB; ++kb)
-              sm103::tma_load_3d(sKV + s * C::TILE + kb * kSubTile, map, bar(C::B_FULL + s), kb * 64, j * BN, bh);
+              sm103::tma_load_3d(sQ + i * C::TILE + kb * kSubTile, &p.tq, bar(C::B_Q + i), kb * 64,
+                                 (u.t0 + i) * BM, u.bh);
+            return true;
+          };
+          if (!(ok = load_q(0, nq0))) break;
+          ++nq0;
+          if (u.nk1 > 0) {
+            if (!(ok = load_q(1, nq1))) break;
+            ++nq1;
+          }
+          const int nk = u.nk();
+          for (int j = 0; ok && !p.withhold_kv && j < nk; ++j) {
+            for (int kv = 0; kv < 2; ++kv, ++c) {
+              const int s = c % NSLOT;
+              if (c >= NSLOT && !(ok = wait_bounded(bar(C::B_EMPTY + s), uint32_t(c / NSLOT - 1) & 1u, ab))) break;
+              sm103::mbar_arrive_expect_tx(bar(C::B_FULL + s), C::TILE);
+              const CUtensorMap* map = kv == 0 ? &p.tk : &p.tv;
+              for (int kb = 0; kb < KB; ++kb)
+                sm103::tma_load_3d(sKV + s * C::TILE + kb * kSubTile, map, bar(C::B_FULL + s), kb * 64, j * BN, u.bh);
+            }
           }
         }
         // Drain: no copy may land in shared memory after this CTA has left.
-        drain_wait(bar(C::B_Q), 0u);
+        // Earlier Q loads and ring loads before the last NSLOT were consumed
+        // (waited on) before their buffers were reused.
+        if (nq0 > 0) drain_wait(bar(C::B_Q + 0), uint32_t(nq0 - 1) & 1u);
+        if (nq1 > 0) drain_wait(bar(C::B_Q + 1), uint32_t(nq1 - 1) & 1u);
         for (int t = c > NSLOT ? c - NSLOT : 0; t < c; ++t) drain_wait(bar(C::B_FULL + t % NSLOT), uint32_t(t / NSLOT) & 1u);
       }
       __syncwarp();
@@ -247,59 +306,95 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_sm103(const __grid_const
       // lane issues each tcgen05.mma and tcgen05.commit.
       constexpr uint32_t kIdescS = sm103::idesc_bf16_f32(BM, BN, 0, 0);  // Q, K both K-major
       constexpr uint32_t kIdescO = sm103::idesc_bf16_f32(BM, D, 0, 1);   // P K-major, V MN-major
-      // Descriptors are built once; moving an operand by `off` bytes adds off >> 4
-      // to the start-address field (no carry: shared addresses stay below 256 KB).
-      const uint64_t desc_q = sm103::sdesc_sw128(sQ, 16, 1024);         // K-major Q tiles
-      const uint64_t desc_k = sm103::sdesc_sw128(sKV, 16, 1024);        // K-major K slots
-      const uint64_t desc_v = sm103::sdesc_sw128(sKV, kSubTile, 1024);  // MN-major V slots
-      auto slot_off = [](int c) { return uint64_t(uint32_t(c % NSLOT) * (C::TILE >> 4)); };
+      // Descriptors (low words) are built once; moving an operand by `off` bytes
+      // adds off >> 4 to the start-address field (no carry: shared addresses stay
+      // below 256 KB).
+      const uint32_t hi = sm103::kSdescHi;
+      const uint32_t desc_q = sm103::sdesc_sw128_lo(sQ, 16);         // K-major Q tiles
+      const uint32_t desc_k = sm103::sdesc_sw128_lo(sKV, 16);        // K-major K slots
+      const uint32_t desc_v = sm103::sdesc_sw128_lo(sKV, kSubTile);  // MN-major V slots
+      auto slot_off = [](int c) { return uint32_t(c % NSLOT) * (C::TILE >> 4); };
       auto wait_full = [&](int c) { return warp_wait(bar(C::B_FULL + c % NSLOT), uint32_t(c / NSLOT) & 1u, ab); };
       auto release = [&](int c) { sm103::mma_commit_warp(bar(C::B_EMPTY + c % NSLOT)); };
-      auto issue_s = [&](int i, int j) {
-        const uint64_t dk = desc_k + slot_off(2 * j), dq = desc_q + uint64_t(uint32_t(i) * (C::TILE >> 4));
-        const uint32_t dS = tmem + C::COL_S + uint32_t(i) * BN;
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {  // 16 of the head dim per MMA
-          const uint64_t off = uint64_t((uint32_t(kk >> 2) * kSubTile + uint32_t(kk & 3) * 32u) >> 4);
-          sm103::mma_ss_warp(dS, dq + off, dk + off, kIdescS, kk > 0 ? 1u : 0u);
+      // Loop-carried state is kept to three words: the MMA issue path relies on
+      // its descriptors staying in uniform registers.  ph bits: 0/1 = parity of
+      // the units tile 0/1 had (B_Q, B_OE), 2/3 = parity of their key steps
+      // (B_PF), 4/5 = parity of their rescale steps (B_OR), 6/7 = tile 0/1 had a
+      // unit before.
+      uint32_t cb = 0;  // ring index of the current unit's K_0
+      uint32_t ph = 0;
+      bool ok = true;
+      for (int k = 0; k < kRounds && ok && more(k); ++k) {
+        int nk0, nk1;
+        {
+          const Unit u = unit_of<CAUSAL>(p, work(k));
+          nk0 = u.nk0;
+          nk1 = u.nk1;
         }
-        sm103::mma_commit_warp(bar(C::B_SF + i));
-      };
-      auto issue_pv = [&](int i, int j) -> bool {
-        if (!warp_wait(bar(C::B_PF + i), uint32_t(j) & 1u, ab)) return false;
-        if (j > 0 && !warp_wait(bar(C::B_OR + i), uint32_t(j - 1) & 1u, ab)) return false;
-        sm103::tc_fence_after();
-        const uint64_t dv = desc_v + slot_off(2 * j + 1);
-        const uint32_t aP = tmem + C::COL_S + uint32_t(i) * BN;
-        const uint32_t dO = tmem + C::COL_O + uint32_t(i) * D;
+        const int nk = max(nk0, nk1);
+        auto issue_s = [&](int i, int j) {
+          const uint32_t dk = desc_k + slot_off(int(cb) + 2 * j), dq = desc_q + uint32_t(i) * (C::TILE >> 4);
+          const uint32_t dS = tmem + C::COL_S + uint32_t(i) * BN;
 #pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk)  // 16 keys per MMA: 8 TMEM columns of P, 16 rows of V
-          sm103::mma_ts_warp(dO, aP + kk * 8, dv + uint64_t(kk * (2048 >> 4)), kIdescO, (j > 0 || kk > 0) ? 1u : 0u);
-        sm103::mma_commit_warp(bar(C::B_OF + i));
-        return true;
-      };
-      bool ok = warp_wait(bar(C::B_Q), 0u, ab) && wait_full(0);
-      if (ok) {
+          for (int kk = 0; kk < D / 16; ++kk) {  // 16 of the head dim per MMA
+            const uint32_t off = (uint32_t(kk >> 2) * kSubTile + uint32_t(kk & 3) * 32u) >> 4;
+            sm103::mma_ss_warp_lo(dS, dq + off, dk + off, kIdescS, kk > 0 ? 1u : 0u, hi);
+          }
+          sm103::mma_commit_warp(bar(C::B_SF + i));
+          if (j == (i == 0 ? nk0 : nk1) - 1) sm103::mma_commit_warp(bar(C::B_QE + i));  // Q_i no longer read
+        };
+        auto issue_pv = [&](int i, int j) -> bool {
+          if (!warp_wait(bar(C::B_PF + i), ((ph >> (2 + i)) ^ uint32_t(j)) & 1u, ab)) return false;
+          if (j > 0) {
+            if (!warp_wait(bar(C::B_OR + i), ((ph >> (4 + i)) ^ uint32_t(j - 1)) & 1u, ab)) return false;
+          } else if ((ph >> (6 + i)) & 1u) {
+            // The first P V of a unit overwrites O_i: the previous unit's epilogue must have read it.
+            if (!warp_wait(bar(C::B_OE + i), ((ph >> i) & 1u) ^ 1u, ab)) return false;
+          }
+          sm103::tc_fence_after();
+          const uint32_t dv = desc_v + slot_off(int(cb) + 2 * j + 1);
+          const uint32_t aP = tmem + C::COL_S + uint32_t(i) * BN;
+          const uint32_t dO = tmem + C::COL_O + uint32_t(i) * D;
+#pragma unroll
+          for (int kk = 0; kk < BN / 16; ++kk)  // 16 keys per MMA: 8 TMEM columns of P, 16 rows of V
+            sm103::mma_ts_warp_lo(dO, aP + kk * 8, dv + uint32_t(kk * (2048 >> 4)), kIdescO, (j > 0 || kk > 0) ? 1u : 0u, hi);
+          sm103::mma_commit_warp(bar(C::B_OF + i));
+          return true;
+        };
+        ok = warp_wait(bar(C::B_Q + 0), ph & 1u, ab) && wait_full(int(cb));
+        if (!ok) break;
         sm103::tc_fence_after();
         issue_s(0, 0);
-        if (nk1 > 0) issue_s(1, 0);
-        release(0);
-      }
-      for (int j = 0; ok && j < nk; ++j) {
-        const bool next = j + 1 < nk;
-        if (next && !(ok = wait_full(2 * j + 2))) break;
-        if (!(ok = wait_full(2 * j + 1))) break;
-        sm103::tc_fence_after();
-        if (j < nk0) {
-          if (!(ok = issue_pv(0, j))) break;
-          if (j + 1 < nk0) issue_s(0, j + 1);
+        if (nk1 > 0) {
+          if (!(ok = warp_wait(bar(C::B_Q + 1), (ph >> 1) & 1u, ab))) break;
+          sm103::tc_fence_after();
+          issue_s(1, 0);
         }
-        if (j < nk1) {
-          if (!(ok = issue_pv(1, j))) break;
-          if (j + 1 < nk1) issue_s(1, j + 1);
+        release(int(cb));
+        for (int j = 0; ok && j < nk; ++j) {
+          const bool next = j + 1 < nk;
+          if (next && !(ok = wait_full(int(cb) + 2 * j + 2))) break;
+          if (!(ok = wait_full(int(cb) + 2 * j + 1))) break;
+          sm103::tc_fence_after();
+          if (j < nk0) {
+            if (!(ok = issue_pv(0, j))) break;
+            if (j + 1 < nk0) issue_s(0, j + 1);
+          }
+          if (j < nk1) {
+            if (!(ok = issue_pv(1, j))) break;
+            if (j + 1 < nk1) issue_s(1, j + 1);
+          }
+          release(int(cb) + 2 * j + 1);
+          if (next) release(int(cb) + 2 * j + 2);
         }
-        release(2 * j + 1);
-        if (next) release(2 * j + 2);
+        cb += 2u * uint32_t(nk);
+        // Tile i: units +1, steps + nk_i, rescale steps + nk_i - 1.
+        ph ^= 0x01u | (uint32_t(nk0 & 1) << 2) | (uint32_t((nk0 - 1) & 1) << 4);
+        ph |= 0x40u;
+        if (nk1 > 0) {
+          ph ^= 0x02u | (uint32_t(nk1 & 1) << 3) | (uint32_t((nk1 - 1) & 1) << 5);
+          ph |= 0x80u;
+        }
       }
       // Every MMA must be finished before TMEM is freed.
       sm103::mma_commit_warp(bar(C::B_DONE));
@@ -311,29 +406,38 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_sm103(const __grid_const
     sm103::regs_increase<kRegSoftmax>();
     const int i = warp >> 2;            // query tile of this warpgroup
     const int r = threadIdx.x & 127;    // row within the tile = TMEM lane
-    const int nki = i == 0 ? nk0 : nk1;
-    if (nki > 0) {
-      const uint32_t lane_off = uint32_t((warp & 3) * 32) << 16;
-      const uint32_t tS = tmem + lane_off + C::COL_S + uint32_t(i) * BN;
-      const int row = (t0 + i) * BM + r;
-      const float sl2 = p.scale_log2;
-      const uint64_t sl2x2 = sm103::f2_pack(sl2, sl2);
+    const uint32_t lane_off = uint32_t((warp & 3) * 32) << 16;
+    const uint32_t tS = tmem + lane_off + C::COL_S + uint32_t(i) * BN;
+    const float sl2 = p.scale_log2;
+    const uint64_t sl2x2 = sm103::f2_pack(sl2, sl2);
+    // Phase word (kept small: this role runs at the register limit): bit 0 =
+    // parity of this tile's earlier key steps (B_SF), bit 1 = parity of its
+    // earlier units (B_OE), bit 2 = an earlier unit exists.
+    uint32_t ph = 0;
+    bool ok = true;
+    for (int k = 0; k < kRounds && ok && more(k); ++k) {
+      int nki, diag;  // key steps; causal: last visible key of this row (row + Nk - Nq)
+      {
+        const Unit u = unit_of<CAUSAL>(p, work(k));
+        nki = i == 0 ? u.nk0 : u.nk1;
+        diag = (u.t0 + i) * BM + r + p.kv_off;
+      }
+      if (nki == 0) continue;
       float m_ref = 0.f;  // reference max (base 2) the exponents are taken against
       float l_run = 0.f;  // running sum of p (fp32, before the bf16 rounding of P)
-      bool ok = true;
       for (int j = 0; j < nki; ++j) {
-        if (!(ok = warp_wait(bar(C::B_SF + i), uint32_t(j) & 1u, ab))) break;
+        if (!(ok = warp_wait(bar(C::B_SF + i), (ph ^ uint32_t(j)) & 1u, ab))) break;
         sm103::tc_fence_after();
         float s[BN];
         {
-          uint32_t u[BN];
-          sm103::tmem_ld128(tS, u);
+          uint32_t uu[BN];
+          sm103::tmem_ld128(tS, uu);
 #pragma unroll
-          for (int c = 0; c < BN; ++c) s[c] = __uint_as_float(u[c]);
+          for (int c = 0; c < BN; ++c) s[c] = __uint_as_float(uu[c]);
         }
         // Masks: keys past N, and keys after the query row when causal.
         int lim = min(BN - 1, p.Nk - 1 - j * BN);
-        if (CAUSAL) lim = min(lim, row + p.kv_off - j * BN);
+        if (CAUSAL) lim = min(lim, diag - j * BN);
         if (lim < BN - 1) {
 #pragma unroll
           for (int c = 0; c < BN; ++c) s[c] = c > lim ? -INFINITY : s[c];
@@ -395,85 +499,106 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_sm103(const __grid_const
         sm103::tc_fence_before();
         sm103::mbar_arrive(bar(C::B_PF + i));
       }
-      if (ok) {
-        // 1/l for the correction warps' epilogue; LSE from here.
-        sm103::tmem_st1(tS + C::COL_INVL, __float_as_uint(1.f / l_run));
-        sm103::tmem_st_wait();
-        sm103::tc_fence_before();
-        sm103::mbar_arrive(bar(C::B_FIN + i));
-        if (row < p.Nq) p.lse[size_t(bh) * size_t(p.Nq) + size_t(row)] = (m_ref + log2f(l_run)) * 0.6931471805599453f;
+      if (!ok) break;
+      // 1/l for the epilogue, once it has read the previous unit's value; LSE from here.
+      if ((ph & 4u) && !(ok = warp_wait(bar(C::B_OE + i), ((ph >> 1) & 1u) ^ 1u, ab))) break;
+      invl[i * BM + r] = 1.f / l_run;
+      sm103::mbar_arrive(bar(C::B_FIN + i));
+      {
+        const Unit u = unit_of<CAUSAL>(p, work(k));
+        const int row = (u.t0 + i) * BM + r;
+        if (row < p.Nq) p.lse[size_t(u.bh) * size_t(p.Nq) + size_t(row)] = (m_ref + log2f(l_run)) * 0.6931471805599453f;
       }
+      ph = ((ph ^ uint32_t(nki)) & 1u) | ((ph ^ 2u) & 2u) | 4u;
     }
   } else {
     // ------------------------------------------------- correction, epilogue
     sm103::regs_decrease<kRegCorr>();
     const int r = threadIdx.x & 127;
     const uint32_t lane_off = uint32_t((warp & 3) * 32) << 16;
+    int nu0 = 0, nu1 = 0, ns0 = 0, ns1 = 0;  // as in the MMA warp
     bool ok = true;
-    for (int j = 1; ok && j < nk; ++j) {
-      for (int i = 0; i < T; ++i) {
-        if (j >= (i == 0 ? nk0 : nk1)) continue;
-        const uint32_t tS = tmem + lane_off + C::COL_S + uint32_t(i) * BN;
-        const uint32_t tO = tmem + lane_off + C::COL_O + uint32_t(i) * D;
-        if (!(ok = warp_wait(bar(C::B_AR + i), uint32_t(j - 1) & 1u, ab))) break;
-        sm103::tc_fence_after();
-        const float alpha = __uint_as_float(sm103::tmem_ld1(tS + C::COL_ALPHA));
-        if (!(ok = warp_wait(bar(C::B_OF + i), uint32_t(j - 1) & 1u, ab))) break;
-        sm103::tc_fence_after();
-        if (__any_sync(0xffffffffu, alpha != 1.f)) {
+    for (int k = 0; k < kRounds && more(k); ++k) {
+      const Unit u = unit_of<CAUSAL>(p, work(k));
+      const int nk = u.nk();
+      for (int j = 1; ok && j < nk; ++j) {
+#pragma unroll 1
+        for (int i = 0; i < 2; ++i) {
+          if (j >= (i == 0 ? u.nk0 : u.nk1)) continue;
+          const uint32_t tS = tmem + lane_off + C::COL_S + uint32_t(i) * BN;
+          const uint32_t tO = tmem + lane_off + C::COL_O + uint32_t(i) * D;
+          if (!(ok = warp_wait(bar(C::B_AR + i), uint32_t((i == 0 ? ns0 - nu0 : ns1 - nu1) + j - 1) & 1u, ab))) break;
+          sm103::tc_fence_after();
+          const float alpha = __uint_as_float(sm103::tmem_ld1(tS + C::COL_ALPHA));
+          if (!(ok = warp_wait(bar(C::B_OF + i), uint32_t((i == 0 ? ns0 : ns1) + j - 1) & 1u, ab))) break;
+          sm103::tc_fence_after();
+          if (__any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll
-          for (int q = 0; q < D / 32; ++q) {
-            uint32_t v[32];
-            sm103::tmem_ld32(tO + q * 32, v);
+            for (int q = 0; q < D / 32; ++q) {
+              uint32_t v[32];
+              sm103::tmem_ld32(tO + q * 32, v);
 #pragma unroll
-            for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
-            sm103::tmem_st32(tO + q * 32, v);
+              for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
+              sm103::tmem_st32(tO + q * 32, v);
+            }
+            sm103::tmem_st_wait();
           }
-          sm103::tmem_st_wait();
+          sm103::tc_fence_before();
+          sm103::mbar_arrive(bar(C::B_OR + i));
         }
-        sm103::tc_fence_before();
-        sm103::mbar_arrive(bar(C::B_OR + i));
       }
-    }
-    // Epilogue.  The four warps agree (reduction barrier) before touching the
-    // shared staging tile, so a warp that gave up on a wait cannot leave the
-    // others stuck at the named barrier below.
-    for (int i = 0; i < T; ++i) {
-      const int nki = i == 0 ? nk0 : nk1;
-      const uint32_t tS = tmem + lane_off + C::COL_S + uint32_t(i) * BN;
-      const uint32_t tO = tmem + lane_off + C::COL_O + uint32_t(i) * D;
-      if (ok) ok = warp_wait(bar(C::B_FIN + i), 0u, ab);
-      if (ok) ok = warp_wait(bar(C::B_OF + i), uint32_t(nki - 1) & 1u, ab);
-      ok = sm103::named_bar_and(1, 128, ok);
+      // Epilogue.  The four warps agree (reduction barrier) before touching the
+      // shared staging tile, so a warp that gave up on a wait cannot leave the
+      // others stuck at the named barrier below.  Tile 0 is in every unit, so the
+      // warps meet at least once per unit.
+#pragma unroll 1
+      for (int i = 0; i < 2; ++i) {
+        const int nki = i == 0 ? u.nk0 : u.nk1;
+        if (nki == 0) continue;
+        const uint32_t tO = tmem + lane_off + C::COL_O + uint32_t(i) * D;
+        if (ok) ok = warp_wait(bar(C::B_FIN + i), uint32_t(i == 0 ? nu0 : nu1) & 1u, ab);
+        if (ok) ok = warp_wait(bar(C::B_OF + i), uint32_t((i == 0 ? ns0 : ns1) + nki - 1) & 1u, ab);
+        if (r == 0) sm103::bulk_wait_read0();  // the previous store has read the staging tile
+        ok = sm103::named_bar_and(1, 128, ok);
+        if (!ok) break;
+        sm103::tc_fence_after();
+        const float inv_l = invl[i * BM + r];
+        // O_i / l -> bf16 into the staging tile, laid out as TMA's 128-byte
+        // swizzle expects: row r at 128 r, 16-byte chunk c at ((c ^ (r & 7)) * 16).
+#pragma unroll
+        for (int q = 0; q < D / 32; ++q) {
+          uint32_t v[32];
+          sm103::tmem_ld32(tO + q * 32, v);
+          if (q == D / 32 - 1) {
+            // O_i and 1/l are in registers: the next unit may overwrite both.
+            sm103::tc_fence_before();
+            sm103::mbar_arrive(bar(C::B_OE + i));
+          }
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            pk[e] = sm103::pack_bf16x2(__uint_as_float(v[2 * e]) * inv_l, __uint_as_float(v[2 * e + 1]) * inv_l);
+          const uint32_t rowbase = sStg + uint32_t(q >> 1) * kSubTile + uint32_t(r) * 128u;
+#pragma unroll
+          for (int c4 = 0; c4 < 4; ++c4) {
+            const uint32_t chunk = uint32_t((q & 1) * 4 + c4);
+            sm103::st_shared_v4(rowbase + ((chunk ^ uint32_t(r & 7)) << 4), pk[4 * c4], pk[4 * c4 + 1],
+                                pk[4 * c4 + 2], pk[4 * c4 + 3]);
+          }
+        }
+        sm103::fence_proxy_async_smem();
+        sm103::named_bar_sync(1, 128);
+        if (r == 0) {
+          for (int kb = 0; kb < KB; ++kb) sm103::tma_store_3d(&p.to, sStg + kb * kSubTile, kb * 64, (u.t0 + i) * BM, u.bh);
+          sm103::bulk_commit();
+        }
+      }
       if (!ok) break;
-      sm103::tc_fence_after();
-      const int m0 = (t0 + i) * BM;
-      if (m0 >= p.Nq) continue;  // a second tile wholly past Nq: nothing to store
-      const float inv_l = __uint_as_float(sm103::tmem_ld1(tS + C::COL_INVL));
-      // O_i / l -> bf16 into the (now idle) Q_i tile, laid out as TMA's 128-byte
-      // swizzle expects: row r at 128 r, 16-byte chunk c at ((c ^ (r & 7)) * 16).
-      const uint32_t stage = sQ + uint32_t(i) * C::TILE;
-#pragma unroll
-      for (int q = 0; q < D / 32; ++q) {
-        uint32_t v[32];
-        sm103::tmem_ld32(tO + q * 32, v);
-        uint32_t pk[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e)
-          pk[e] = sm103::pack_bf16x2(__uint_as_float(v[2 * e]) * inv_l, __uint_as_float(v[2 * e + 1]) * inv_l);
-        const uint32_t rowbase = stage + uint32_t(q >> 1) * kSubTile + uint32_t(r) * 128u;
-#pragma unroll
-        for (int c4 = 0; c4 < 4; ++c4) {
-          const uint32_t chunk = uint32_t((q & 1) * 4 + c4);
-          sm103::st_shared_v4(rowbase + ((chunk ^ uint32_t(r & 7)) << 4), pk[4 * c4], pk[4 * c4 + 1],
-                              pk[4 * c4 + 2], pk[4 * c4 + 3]);
-        }
-      }
-      sm103::fence_proxy_async_smem();
-      sm103::named_bar_sync(1, 128);
-      if (r == 0) {
-        for (int kb = 0; kb < KB; ++kb) sm103::tma_store_3d(&p.to, stage + kb * kSubTile, kb * 64, m0, bh);
-        sm103::bulk_commit();
+      ++nu0;
+      ns0 += u.nk0;
+      if (u.nk1 > 0) {
+        ++nu1;
+        ns1 += u.nk1;
       }
     }
     if (r == 0) sm103::bulk_wait_read0();  // the stores have read shared memory
