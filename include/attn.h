@@ -93,6 +93,39 @@ attn_status_t attn_fwd_qk(const void* q, const void* k, const void* v, void* o, 
                           float scale, void* stream);
 
 /*
+ * attn_fwd_from_host -- attn_fwd_qk for inputs and outputs in host memory.
+ *
+ * q_host, k_host, v_host : host (or device) pointers, the layouts of attn_fwd_qk's
+ *           q, k, v.  Read.
+ * o_host, lse_host : host (or device) pointers, the layouts of o and lse.  Written.
+ * q, k, v, o, lse : device buffers of the full sizes with attn_fwd_qk's rules
+ *           (alignment, no overlap); owned by the caller, used as the staging
+ *           area (q, k, v receive the inputs; o, lse hold the results).
+ * Other arguments as attn_fwd_qk (Nq = Nk for the square problem).
+ *
+ * The work is enqueued behind everything already on `stream` and the call
+ * returns; synchronising `stream` waits for all of it, host outputs included.
+ * The heads are processed in up to 8 chunks: the host-to-device copy of one
+ * chunk, the kernel on the previous one and the device-to-host copy of the one
+ * before overlap (two copy streams and a set of events, created once per device
+ * and reused; this is the GB300 counterpart of the pages' advice to keep the
+ * copy engines and the SMs busy at the same time, "GPUの爆発的な性能向上",
+ * ja.news.hada.io topic 14783, section "アドレス生成とTMA").  Host buffers
+ * should be pinned (page-locked) for the copies to run asynchronously; pageable
+ * ones give the same results with less overlap.  The host buffers must stay
+ * valid until the work completes.  Results are bit-identical to attn_fwd_qk on
+ * the same device inputs.  Errors: the argument checks of attn_fwd_qk run before
+ * anything is enqueued (plus ATTN_ERR_INVALID_ARG for a null host pointer); a
+ * failed copy or launch returns ATTN_ERR_CUDA, with earlier chunks possibly
+ * enqueued; timeouts through attn_last_status.  Calls from several host threads
+ * are serialised while they enqueue.
+ */
+attn_status_t attn_fwd_from_host(const void* q_host, const void* k_host, const void* v_host,
+                                 void* o_host, float* lse_host, void* q, void* k, void* v, void* o,
+                                 float* lse, int64_t B, int64_t H, int64_t Nq, int64_t Nk,
+                                 int64_t D, int causal, float scale, void* stream);
+
+/*
  * attn_bwd -- enqueue the backward of attn_fwd on `stream`: the gradients of
  * sum(dO * O) with respect to Q, K and V.
  *

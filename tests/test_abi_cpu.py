@@ -130,3 +130,28 @@ def test_qk_flops(lib):
     assert pkg.attn_fwd_qk_flops(2, 3, 256, 256, 64, False) == pkg.attn_fwd_flops(2, 3, 256, 64, False)
     assert pkg.attn_fwd_qk_flops(1, 1, 100, 300, 64, False) == 4.0 * 100 * 300 * 64
     assert pkg.attn_fwd_qk_flops(1, 1, 100, 300, 64, True) == 4.0 * (100 * 200 + 0.5 * 100 * 100) * 64
+
+
+def call_host(Nq=100, Nk=300, causal=0, **kw):
+    args = dict(qh=A16 + 512 * MB, kh=A16 + 576 * MB, vh=A16 + 640 * MB, oh=A16 + 704 * MB, lh=A16 + 768 * MB,
+                q=A16, k=A16 + 64 * MB, v=A16 + 128 * MB, o=A16 + 192 * MB, lse=A16 + 256 * MB,
+                B=1, H=2, D=64, scale=0.125)
+    args.update(kw)
+    a = args
+    return pkg.attn_fwd_from_host(a["qh"], a["kh"], a["vh"], a["oh"], a["lh"], a["q"], a["k"], a["v"], a["o"],
+                                  a["lse"], a["B"], a["H"], Nq, Nk, a["D"], causal, a["scale"], None)
+
+
+def test_from_host_validation(lib):
+    for kw in ("qh", "kh", "vh", "oh", "lh", "q", "k", "v", "o", "lse"):
+        assert call_host(**{kw: None}) == pkg.ATTN_ERR_INVALID_ARG, kw
+    assert call_host(scale=0.0) == pkg.ATTN_ERR_INVALID_ARG
+    assert call_host(D=100) == pkg.ATTN_ERR_UNSUPPORTED
+    assert call_host(Nq=300, Nk=100, causal=1) == pkg.ATTN_ERR_UNSUPPORTED
+    assert call_host(o=A16 + 64 * MB) == pkg.ATTN_ERR_INVALID_ARG  # device o overlaps device k
+    assert call_host(Nq=0, qh=None, kh=None, vh=None, oh=None, lh=None, q=None, k=None, v=None, o=None,
+                     lse=None) == pkg.ATTN_OK
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert call_host() == pkg.ATTN_ERR_CUDA  # valid request, no device: nothing enqueued

@@ -19,6 +19,7 @@ from ._binding import (  # noqa: F401
     attn_bwd_qk_flops,
     attn_fwd,
     attn_fwd_flops,
+    attn_fwd_from_host,
     attn_fwd_qk,
     attn_fwd_qk_flops,
     attn_last_status,
@@ -83,3 +84,44 @@ def bwd(q, k, v, o, lse, do, causal: bool = False, scale: float | None = None, s
     if st != ATTN_OK:
         raise AttnError(st)
     return dq, dk, dv, delta
+
+
+def fwd_from_host(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None, device_buffers=None,
+                  stream=None):
+    """Forward for bf16 CPU tensors q [B, H, Nq, D], k, v [B, H, Nk, D] (pin them for overlapped copies).
+
+    ``device_buffers`` = (q, k, v, o, lse) CUDA tensors of the same shapes (o like q,
+    lse fp32 [B, H, Nq]) are the staging area; allocated on the current device when
+    omitted.  Returns ``(out, lse)`` CPU tensors, filled once ``stream`` (default:
+    torch's current stream) has been synchronised.  Keep q, k, v (and the device
+    buffers) alive until then: the copies run asynchronously, and torch's
+    pinned-memory cache may hand a freed block to another tensor at once.
+    """
+    import torch
+
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if t.dtype != torch.bfloat16 or t.is_cuda or t.dim() != 4 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous bf16 CPU tensor [B, H, N, D]")
+    B, H, Nq, D = q.shape
+    Nk = k.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    pin = q.is_pinned()
+    if out is None:
+        out = torch.empty(q.shape, dtype=torch.bfloat16, pin_memory=pin)
+    if lse is None:
+        lse = torch.empty((B, H, Nq), dtype=torch.float32, pin_memory=pin)
+    if device_buffers is None:
+        dev = torch.device("cuda", torch.cuda.current_device())
+        device_buffers = (torch.empty(q.shape, dtype=torch.bfloat16, device=dev),
+                          torch.empty(k.shape, dtype=torch.bfloat16, device=dev),
+                          torch.empty(v.shape, dtype=torch.bfloat16, device=dev),
+                          torch.empty(q.shape, dtype=torch.bfloat16, device=dev),
+                          torch.empty((B, H, Nq), dtype=torch.float32, device=dev))
+    qd, kd, vd, od, ld = device_buffers
+    if stream is None:
+        stream = torch.cuda.current_stream(qd.device)
+    st = attn_fwd_from_host(q, k, v, out, lse, qd, kd, vd, od, ld, B, H, Nq, Nk, D, causal, scale, stream)
+    if st != ATTN_OK:
+        raise AttnError(st)
+    return out, lse

@@ -48,6 +48,8 @@ def library() -> ctypes.CDLL:
             lib.attn_bwd_qk.restype = ctypes.c_int
             lib.attn_bwd_qk_flops.argtypes = [I64, I64, I64, I64, I64, ctypes.c_int]
             lib.attn_bwd_qk_flops.restype = ctypes.c_double
+            lib.attn_fwd_from_host.argtypes = [P] * 10 + [I64, I64, I64, I64, I64, ctypes.c_int, ctypes.c_float, P]
+            lib.attn_fwd_from_host.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -114,3 +116,11 @@ def attn_bwd_qk(q, k, v, o, lse, dout, dq, dk, dv, delta, B: int, H: int, Nq: in
 
 def attn_bwd_qk_flops(B: int, H: int, Nq: int, Nk: int, D: int, causal: bool) -> float:
     return library().attn_bwd_qk_flops(int(B), int(H), int(Nq), int(Nk), int(D), int(bool(causal)))
+
+
+def attn_fwd_from_host(q_host, k_host, v_host, o_host, lse_host, q, k, v, o, lse, B: int, H: int, Nq: int, Nk: int,
+                       D: int, causal: bool, scale: float, stream) -> int:
+    """Call ``attn_fwd_from_host`` (host inputs and outputs, copies overlapped with the kernels)."""
+    a = [_addr(x) for x in (q_host, k_host, v_host, o_host, lse_host, q, k, v, o, lse)]
+    return library().attn_fwd_from_host(*a, int(B), int(H), int(Nq), int(Nk), int(D), int(bool(causal)),
+                                        float(scale), _stream(stream))

@@ -121,8 +121,10 @@ cudaError_t launch(const attn::FwdParams& prm, int64_t ctas, bool persist, cudaS
 }
 
 // Shared launcher of attn_fwd and attn_fwd_qk: Q, O [B*H, Nq, D]; K, V [B*H, Nk, D].
+// With check_only it validates the arguments and the device and returns.
 attn_status_t launch_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int64_t B, int64_t H,
-                         int64_t Nq, int64_t Nk, int64_t D, int causal, float scale, void* stream) {
+                         int64_t Nq, int64_t Nk, int64_t D, int causal, float scale, void* stream,
+                         bool check_only = false) {
   if (B < 0 || H < 0 || Nq < 0 || Nk < 0 || D <= 0) return ATTN_ERR_INVALID_ARG;
   if (!(scale > 0.f) || !std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
   if (D > 128 || D % 8 != 0) return ATTN_ERR_UNSUPPORTED;
@@ -154,7 +156,7 @@ attn_status_t launch_fwd(const void* q, const void* k, const void* v, void* o, f
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_CUDA;
   const attn_status_t ready = prepare_device(dev);
-  if (ready != ATTN_OK) return ready;
+  if (ready != ATTN_OK || check_only) return ready;
   const EncodeTiledFn enc = encode_fn();
   if (!enc) return ATTN_ERR_CUDA;
 
@@ -271,6 +273,7 @@ double attn_fwd_qk_flops(int64_t B, int64_t H, int64_t Nq, int64_t Nk, int64_t D
 
 }  // extern "C"
 #include "attn_bwd_host.cuh"
+#include "attn_host_pipeline.cuh"
 
 extern "C" double attn_bwd_qk_flops(int64_t B, int64_t H, int64_t Nq, int64_t Nk, int64_t D, int causal) {
   return 2.5 * attn_fwd_qk_flops(B, H, Nq, Nk, D, causal);
