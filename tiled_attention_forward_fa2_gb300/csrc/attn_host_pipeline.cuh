@@ -11,12 +11,30 @@
 
 namespace {
 
-constexpr int kPipeChunks = 8;  // chunks of heads per call (fewer when B*H is smaller)
+constexpr int kPipeChunksMax = 32;  // events held per device
+
+// Chunks of heads per call.  A chunk's kernel lasts at least as long as its
+// longest unit (all key tiles of two query tiles: ~1.55 us per key tile at
+// D = 128, ~0.8 at D <= 64, measured on GB300), so more chunks only help while
+// each chunk's upload (~200 GB/s over the host link, measured both for the copy
+// engines and for SM loads) still takes longer than that; at most 8 (measured:
+// the bench shape, 32-key-tile units, is best at 8; causal N = 16384, 128-tile
+// units, at 4 -- 816 against 620 TFLOP/s end to end at 8).  ATTN_PIPE_CHUNKS=
+// 1..32 (read at every call) overrides the choice (tuning).
+int pipe_chunks(uint64_t in_bytes, int64_t n_ktiles, int64_t D) {
+  const char* e = std::getenv("ATTN_PIPE_CHUNKS");
+  const int x = e ? std::atoi(e) : 0;
+  if (x >= 1 && x <= kPipeChunksMax) return x;
+  const double unit_us = double(n_ktiles) * (D <= 64 ? 0.8 : 1.55);
+  const double upload_us = double(in_bytes) / 200e3;  // 200 GB/s = 200e3 bytes per us
+  const double n = upload_us / unit_us;
+  return n >= 8.0 ? 8 : (n >= 1.0 ? int(n) : 1);
+}
 
 struct HostPipe {
   cudaStream_t up = nullptr, down = nullptr;
   cudaEvent_t start = nullptr, done = nullptr;
-  cudaEvent_t in[kPipeChunks] = {}, out[kPipeChunks] = {};
+  cudaEvent_t in[kPipeChunksMax] = {}, out[kPipeChunksMax] = {};
   bool ready = false;
 };
 HostPipe g_pipe[kMaxDevices];
@@ -32,7 +50,7 @@ attn_status_t pipe_ready(int dev) {
       cudaStreamCreateWithFlags(&hp.down, cudaStreamNonBlocking) != cudaSuccess ||
       cudaEventCreateWithFlags(&hp.start, ev) != cudaSuccess || cudaEventCreateWithFlags(&hp.done, ev) != cudaSuccess)
     return ATTN_ERR_CUDA;
-  for (int c = 0; c < kPipeChunks; ++c)
+  for (int c = 0; c < kPipeChunksMax; ++c)
     if (cudaEventCreateWithFlags(&hp.in[c], ev) != cudaSuccess || cudaEventCreateWithFlags(&hp.out[c], ev) != cudaSuccess)
       return ATTN_ERR_CUDA;
   hp.ready = true;
@@ -58,8 +76,9 @@ extern "C" attn_status_t attn_fwd_from_host(const void* q_host, const void* k_ho
   HostPipe& hp = g_pipe[dev];
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int64_t BH = B * H;
-  const int n = int(BH < kPipeChunks ? BH : kPipeChunks);
   const uint64_t q_row = uint64_t(Nq) * uint64_t(D) * 2u, kv_row = uint64_t(Nk) * uint64_t(D) * 2u;
+  const int chunks = pipe_chunks(uint64_t(BH) * (q_row + 2u * kv_row), (Nk + attn::BN - 1) / attn::BN, D);
+  const int n = int(BH < chunks ? BH : chunks);
   const uint64_t l_row = uint64_t(Nq) * 4u;
   auto at = [](const void* p, uint64_t off) { return static_cast<const uint8_t*>(p) + off; };
   auto atw = [](void* p, uint64_t off) { return static_cast<uint8_t*>(p) + off; };
