@@ -83,19 +83,22 @@ struct Cfg {
   static_assert(D == 64 || D == 128, "head dim");
   static constexpr int KB = D / 64;                      // 64-column sub-tiles per tile
   static constexpr uint32_t TILE = KB * kSubTile;        // bytes of one 128 x D bf16 tile
-  static constexpr int NSLOT = D == 128 ? 4 : 11;        // K/V ring slots (one tile each)
+  // Q buffers per query tile: at D = 64 two, so a unit's Q loads while the unit
+  // before still reads the other (short units would otherwise wait for it).
+  static constexpr int NQB = D == 64 ? 2 : 1;
+  static constexpr int NSLOT = D == 128 ? 4 : 9;         // K/V ring slots (one tile each)
   static constexpr uint32_t OFF_INVL = 1024;             // [2][128] fp32: 1/l of each row of tile i
-  static constexpr uint32_t OFF_Q = 2048;                // Q_0, Q_1
-  static constexpr uint32_t OFF_STG = OFF_Q + 2 * TILE;  // O staging tile of the TMA store
+  static constexpr uint32_t OFF_Q = 2048;                      // Q buffer i * NQB + b of tile i
+  static constexpr uint32_t OFF_STG = OFF_Q + 2 * NQB * TILE;  // O staging tile of the TMA store
   static constexpr uint32_t OFF_KV = OFF_STG + TILE;
   static constexpr uint32_t USED = OFF_KV + NSLOT * TILE;
   static constexpr uint32_t SMEM = USED + 1024;          // + slack to align the base to 1 KB
   static_assert(SMEM <= 232448, "shared memory");
   // barrier slots ([2]: one per query tile of the unit)
-  static constexpr int B_Q = 0;                  // [2] Q_i landed (TMA bytes)
-  static constexpr int B_QE = 2;                 // [2] last S MMA on Q_i of the unit finished (MMA commit)
-  static constexpr int B_FULL = 4, B_EMPTY = 4 + NSLOT;
-  static constexpr int B_SF = 4 + 2 * NSLOT;     // [2] scores of tile i ready (MMA commit)
+  static constexpr int B_Q = 0;                  // [2 NQB] Q buffer landed (TMA bytes)
+  static constexpr int B_QE = 2 * NQB;           // [2 NQB] last S MMA on the buffer finished (MMA commit)
+  static constexpr int B_FULL = 4 * NQB, B_EMPTY = 4 * NQB + NSLOT;
+  static constexpr int B_SF = 4 * NQB + 2 * NSLOT;  // [2] scores of tile i ready (MMA commit)
   static constexpr int B_PF = B_SF + 2;          // [2] P of tile i in TMEM (128 softmax threads)
   static constexpr int B_AR = B_PF + 2;          // [2] per-step rescale factor in TMEM (128 softmax threads)
   static constexpr int B_OR = B_AR + 2;          // [2] O of tile i rescaled (128 correction threads)
@@ -208,7 +211,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_sm103(const __grid_const
   uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(sbase + 512);
   volatile uint32_t* const abort_flag = reinterpret_cast<volatile uint32_t*>(sbase + 516);
   float* const invl = reinterpret_cast<float*>(sbase + C::OFF_INVL);  // [2][128]
-  const uint32_t sQ = base + C::OFF_Q;      // Q_i at sQ + i * TILE
+  const uint32_t sQ = base + C::OFF_Q;      // Q buffer qi = i * NQB + b at sQ + qi * TILE
   const uint32_t sStg = base + C::OFF_STG;  // O staging tile
   const uint32_t sKV = base + C::OFF_KV;    // slot s at sKV + s * TILE
   auto bar = [base](int i) { return base + 8u * uint32_t(i); };
@@ -261,16 +264,18 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_sm103(const __grid_const
       // ---------------------------------------------------------- producer
       if (lane == 0) {
         int c = 0;            // K/V loads issued; K_j of a unit is load cb + 2j, V_j load cb + 2j + 1
-        int nq0 = 0, nq1 = 0;  // Q loads issued into buffer 0 / 1
+        int nq0 = 0, nq1 = 0;  // Q loads issued for tile 0 / 1 (the n-th into buffer n % NQB)
         bool ok = true;
         for (int k = 0; k < kRounds && ok && more(k); ++k) {
           const Unit u = unit_of<CAUSAL>(p, work(k));
-          // Buffer i is free once the previous unit's last S MMA reading it has finished.
+          // A buffer is free once the last S MMA of the unit that used it before
+          // (NQB loads ago) has finished.
           auto load_q = [&](int i, int nq) -> bool {
-            if (nq > 0 && !wait_bounded(bar(C::B_QE + i), uint32_t(nq - 1) & 1u, ab)) return false;
-            sm103::mbar_arrive_expect_tx(bar(C::B_Q + i), C::TILE);
+            const int qi = i * C::NQB + nq % C::NQB;
+            if (nq >= C::NQB && !wait_bounded(bar(C::B_QE + qi), uint32_t(nq / C::NQB - 1) & 1u, ab)) return false;
+            sm103::mbar_arrive_expect_tx(bar(C::B_Q + qi), C::TILE);
             for (int kb = 0; kb < KB; ++kb)
-              sm103::tma_load_3d(sQ + i * C::TILE + kb * kSubTile, &p.tq, bar(C::B_Q + i), kb * 64,
+              sm103::tma_load_3d(sQ + qi * C::TILE + kb * kSubTile, &p.tq, bar(C::B_Q + qi), kb * 64,
                                  (u.t0 + i) * BM, u.bh);
             return true;
           };
@@ -295,8 +300,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_sm103(const __grid_const
         // Drain: no copy may land in shared memory after this CTA has left.
         // Earlier Q loads and ring loads before the last NSLOT were consumed
         // (waited on) before their buffers were reused.
-        if (nq0 > 0) drain_wait(bar(C::B_Q + 0), uint32_t(nq0 - 1) & 1u);
-        if (nq1 > 0) drain_wait(bar(C::B_Q + 1), uint32_t(nq1 - 1) & 1u);
+        for (int t = nq0 > C::NQB ? nq0 - C::NQB : 0; t < nq0; ++t)
+          drain_wait(bar(C::B_Q + t % C::NQB), uint32_t(t / C::NQB) & 1u);
+        for (int t = nq1 > C::NQB ? nq1 - C::NQB : 0; t < nq1; ++t)
+          drain_wait(bar(C::B_Q + C::NQB + t % C::NQB), uint32_t(t / C::NQB) & 1u);
         for (int t = c > NSLOT ? c - NSLOT : 0; t < c; ++t) drain_wait(bar(C::B_FULL + t % NSLOT), uint32_t(t / NSLOT) & 1u);
       }
       __syncwarp();
@@ -316,13 +323,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_sm103(const __grid_const
       auto slot_off = [](int c) { return uint32_t(c % NSLOT) * (C::TILE >> 4); };
       auto wait_full = [&](int c) { return warp_wait(bar(C::B_FULL + c % NSLOT), uint32_t(c / NSLOT) & 1u, ab); };
       auto release = [&](int c) { sm103::mma_commit_warp(bar(C::B_EMPTY + c % NSLOT)); };
-      // Loop-carried state is kept to three words: the MMA issue path relies on
-      // its descriptors staying in uniform registers.  ph bits: 0/1 = parity of
-      // the units tile 0/1 had (B_Q, B_OE), 2/3 = parity of their key steps
-      // (B_PF), 4/5 = parity of their rescale steps (B_OR), 6/7 = tile 0/1 had a
-      // unit before.
+      // nu0/nu1: units tile 0/1 had (B_Q / B_QE buffer and phase, B_OE); ph bits
+      // 2/3 = parity of their key steps (B_PF), 4/5 = parity of their rescale
+      // steps (B_OR).
       uint32_t cb = 0;  // ring index of the current unit's K_0
       uint32_t ph = 0;
+      int nu0 = 0, nu1 = 0;
       bool ok = true;
       for (int k = 0; k < kRounds && ok && more(k); ++k) {
         int nk0, nk1;
@@ -333,7 +339,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_sm103(const __grid_const
         }
         const int nk = max(nk0, nk1);
         auto issue_s = [&](int i, int j) {
-          const uint32_t dk = desc_k + slot_off(int(cb) + 2 * j), dq = desc_q + uint32_t(i) * (C::TILE >> 4);
+          const int qi = i * C::NQB + (i == 0 ? nu0 : nu1) % C::NQB;
+          const uint32_t dk = desc_k + slot_off(int(cb) + 2 * j), dq = desc_q + uint32_t(qi) * (C::TILE >> 4);
           const uint32_t dS = tmem + C::COL_S + uint32_t(i) * BN;
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {  // 16 of the head dim per MMA
@@ -341,15 +348,15 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_sm103(const __grid_const
             sm103::mma_ss_warp_lo(dS, dq + off, dk + off, kIdescS, kk > 0 ? 1u : 0u, hi);
           }
           sm103::mma_commit_warp(bar(C::B_SF + i));
-          if (j == (i == 0 ? nk0 : nk1) - 1) sm103::mma_commit_warp(bar(C::B_QE + i));  // Q_i no longer read
+          if (j == (i == 0 ? nk0 : nk1) - 1) sm103::mma_commit_warp(bar(C::B_QE + qi));  // Q buffer no longer read
         };
         auto issue_pv = [&](int i, int j) -> bool {
           if (!warp_wait(bar(C::B_PF + i), ((ph >> (2 + i)) ^ uint32_t(j)) & 1u, ab)) return false;
           if (j > 0) {
             if (!warp_wait(bar(C::B_OR + i), ((ph >> (4 + i)) ^ uint32_t(j - 1)) & 1u, ab)) return false;
-          } else if ((ph >> (6 + i)) & 1u) {
+          } else if ((i == 0 ? nu0 : nu1) > 0) {
             // The first P V of a unit overwrites O_i: the previous unit's epilogue must have read it.
-            if (!warp_wait(bar(C::B_OE + i), ((ph >> i) & 1u) ^ 1u, ab)) return false;
+            if (!warp_wait(bar(C::B_OE + i), uint32_t((i == 0 ? nu0 : nu1) - 1) & 1u, ab)) return false;
           }
           sm103::tc_fence_after();
           const uint32_t dv = desc_v + slot_off(int(cb) + 2 * j + 1);
@@ -361,12 +368,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_sm103(const __grid_const
           sm103::mma_commit_warp(bar(C::B_OF + i));
           return true;
         };
-        ok = warp_wait(bar(C::B_Q + 0), ph & 1u, ab) && wait_full(int(cb));
+        ok = warp_wait(bar(C::B_Q + nu0 % C::NQB), uint32_t(nu0 / C::NQB) & 1u, ab) && wait_full(int(cb));
         if (!ok) break;
         sm103::tc_fence_after();
         issue_s(0, 0);
         if (nk1 > 0) {
-          if (!(ok = warp_wait(bar(C::B_Q + 1), (ph >> 1) & 1u, ab))) break;
+          if (!(ok = warp_wait(bar(C::B_Q + C::NQB + nu1 % C::NQB), uint32_t(nu1 / C::NQB) & 1u, ab))) break;
           sm103::tc_fence_after();
           issue_s(1, 0);
         }
@@ -389,11 +396,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_sm103(const __grid_const
         }
         cb += 2u * uint32_t(nk);
         // Tile i: units +1, steps + nk_i, rescale steps + nk_i - 1.
-        ph ^= 0x01u | (uint32_t(nk0 & 1) << 2) | (uint32_t((nk0 - 1) & 1) << 4);
-        ph |= 0x40u;
+        ph ^= (uint32_t(nk0 & 1) << 2) | (uint32_t((nk0 - 1) & 1) << 4);
+        ++nu0;
         if (nk1 > 0) {
-          ph ^= 0x02u | (uint32_t(nk1 & 1) << 3) | (uint32_t((nk1 - 1) & 1) << 5);
-          ph |= 0x80u;
+          ph ^= (uint32_t(nk1 & 1) << 3) | (uint32_t((nk1 - 1) & 1) << 5);
+          ++nu1;
         }
       }
       // Every MMA must be finished before TMEM is freed.
