@@ -56,15 +56,30 @@ def test_bad_sizes_and_scale(lib):
 
 
 def test_unsupported_head_dims(lib):
-    for d in (4, 12, 100, 136, 192, 256):
+    for d in (4, 12, 100, 260, 264, 512):
         assert call(D=d) == pkg.ATTN_ERR_UNSUPPORTED
+
+
+def call_bwd(D=64, **kw):
+    a = dict(q=A16, k=A16 + 64 * MB, v=A16 + 128 * MB, o=A16 + 192 * MB, lse=A16 + 256 * MB, dout=A16 + 320 * MB,
+             dq=A16 + 384 * MB, dk=A16 + 448 * MB, dv=A16 + 512 * MB, delta=A16 + 576 * MB)
+    a.update(kw)
+    return pkg.attn_bwd(a["q"], a["k"], a["v"], a["o"], a["lse"], a["dout"], a["dq"], a["dk"], a["dv"], a["delta"],
+                        1, 2, 256, D, 0, 0.125, None)
+
+
+def test_backward_head_dims(lib):
+    """The backward stops at D = 128 (its kernels' TMEM and shared-memory budgets)."""
+    for d in (4, 100, 136, 192, 256):
+        assert call_bwd(D=d) == pkg.ATTN_ERR_UNSUPPORTED
+    assert call_bwd(D=64, dq=None) == pkg.ATTN_ERR_INVALID_ARG
 
 
 def test_padded_head_dims_pass_validation(lib):
     import torch
     if torch.cuda.is_available():
         pytest.skip("a GPU is present")
-    for d in (8, 32, 48, 96, 112):
+    for d in (8, 32, 48, 96, 112, 136, 192, 200, 256):
         assert call(D=d) == pkg.ATTN_ERR_CUDA  # past validation, stopped only by the missing device
 
 

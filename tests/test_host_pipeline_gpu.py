@@ -53,6 +53,7 @@ def qkv_qk(B, H, Nq, Nk, D, seed):
     (1, 3, 333, 333, 128, True),     # fewer heads than chunks, ragged
     (2, 10, 640, 640, 64, False),    # 20 heads in 8 chunks of 2 or 3
     (3, 7, 200, 1000, 128, True),    # queries against a longer key cache
+    (2, 5, 300, 300, 256, True),     # the D = 256 kernel
 ])
 def test_matches_device_call_exactly(B, H, Nq, Nk, D, causal, pin):
     q, k, v = qkv_qk(B, H, Nq, Nk, D, seed=31 + B * H + Nq)

@@ -287,3 +287,38 @@ def test_padded_head_dims(D, causal, tiles_per_cta, schedule):
     o, lse = run_qk(qr, kr, vr, causal, 0.3)
     o_ref, lse_ref = oracle.attn_fwd(qr, kr, vr, causal, 0.3)
     assert_close(o, lse, o_ref, lse_ref, f"Nq=100 Nk=450 D={D} causal={causal}")
+
+
+@pytest.mark.parametrize("D", [136, 192, 256])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("N", [1, 127, 300, 640])
+def test_wide_head_dims(N, D, causal):
+    """Head dims above 128 run on the D = 256 kernel (one query tile per CTA, zero padding below 256)."""
+    q, k, v = make_qkv(2, 3, N, D, seed=1300 + N + D)
+    full_check(q, k, v, causal, 1.0 / math.sqrt(D), f"N={N} D={D} causal={causal}")
+
+
+@pytest.mark.parametrize("Nq,Nk,causal", [(100, 700, True), (384, 129, False), (513, 1000, True)])
+def test_wide_head_dims_queries_and_keys_of_different_lengths(Nq, Nk, causal):
+    D = 256
+    q = make_qkv(2, 2, Nq, D, seed=1400 + Nq)[0]
+    _, k, v = make_qkv(2, 2, Nk, D, seed=1500 + Nk)
+    qd, kd, vd = to_dev(q), to_dev(k), to_dev(v)
+    o = torch.full_like(qd, float("nan"))
+    lse = torch.full((2, 2, Nq), float("nan"), dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream()
+    assert pkg.attn_fwd_qk(qd, kd, vd, o, lse, 2, 2, Nq, Nk, D, causal, 0.0625, stream) == pkg.ATTN_OK
+    assert pkg.attn_last_status(stream) == pkg.ATTN_OK
+    o_ref, lse_ref = oracle.attn_fwd(q, k, v, causal, 0.0625)
+    assert_close(o_to_f64(o), lse.cpu().numpy().astype(np.float64), o_ref, lse_ref, f"D=256 Nq={Nq} Nk={Nk}")
+
+
+def test_wide_head_dims_large_logits_and_many_tiles():
+    """D = 256, Q spread 4x, 2048 keys (16 key steps through the two-slot ring), causal and not."""
+    q, k, v = make_qkv(1, 4, 2048, 256, seed=1600, q_std=4.0)
+    for causal in (False, True):
+        o, lse = run(q, k, v, causal, 1.0 / 16)
+        bh, ri = sampled_rows(4, 2048, 256, 1601)
+        o_ref, lse_ref = oracle.attn_rows(q, k, v, causal, 1.0 / 16, bh, ri)
+        assert_close(o.reshape(4, 2048, 256)[bh, ri], lse.reshape(4, 2048)[bh, ri], o_ref, lse_ref,
+                     f"D=256 N=2048 q_std=4 causal={causal}")

@@ -59,8 +59,10 @@ cudaError_t opt_in_smem() {
   cudaError_t e = cudaFuncSetAttribute(attn::attn_fwd_sm103<D, CAUSAL, false>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, int(attn::Cfg<D>::SMEM));
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(attn::attn_fwd_sm103<D, CAUSAL, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              int(attn::Cfg<D>::SMEM));
+  if constexpr (attn::Cfg<D>::STAGE_IN_Q) return cudaSuccess;  // one-unit grid only
+  else
+    return cudaFuncSetAttribute(attn::attn_fwd_sm103<D, CAUSAL, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                int(attn::Cfg<D>::SMEM));
 }
 
 attn_status_t prepare_device(int dev) {
@@ -78,7 +80,8 @@ attn_status_t prepare_device(int dev) {
       } else if (major != 10 || minor != 3) {
         st = 2;
       } else if (opt_in_smem<64, false>() != cudaSuccess || opt_in_smem<64, true>() != cudaSuccess ||
-                 opt_in_smem<128, false>() != cudaSuccess || opt_in_smem<128, true>() != cudaSuccess) {
+                 opt_in_smem<128, false>() != cudaSuccess || opt_in_smem<128, true>() != cudaSuccess ||
+                 opt_in_smem<256, false>() != cudaSuccess || opt_in_smem<256, true>() != cudaSuccess) {
         st = 3;
       } else {
         st = 1;
@@ -113,10 +116,14 @@ long long timeout_cycles() {
 
 template <int D, bool CAUSAL>
 cudaError_t launch(const attn::FwdParams& prm, int64_t ctas, bool persist, cudaStream_t stream) {
-  if (persist)
-    attn::attn_fwd_sm103<D, CAUSAL, true><<<dim3(unsigned(ctas)), dim3(attn::kThreads), attn::Cfg<D>::SMEM, stream>>>(prm);
-  else
-    attn::attn_fwd_sm103<D, CAUSAL, false><<<dim3(unsigned(ctas)), dim3(attn::kThreads), attn::Cfg<D>::SMEM, stream>>>(prm);
+  if constexpr (!attn::Cfg<D>::STAGE_IN_Q) {
+    if (persist) {
+      attn::attn_fwd_sm103<D, CAUSAL, true><<<dim3(unsigned(ctas)), dim3(attn::kThreads), attn::Cfg<D>::SMEM,
+                                               stream>>>(prm);
+      return cudaGetLastError();
+    }
+  }
+  attn::attn_fwd_sm103<D, CAUSAL, false><<<dim3(unsigned(ctas)), dim3(attn::kThreads), attn::Cfg<D>::SMEM, stream>>>(prm);
   return cudaGetLastError();
 }
 
@@ -127,7 +134,7 @@ attn_status_t launch_fwd(const void* q, const void* k, const void* v, void* o, f
                          bool check_only = false) {
   if (B < 0 || H < 0 || Nq < 0 || Nk < 0 || D <= 0) return ATTN_ERR_INVALID_ARG;
   if (!(scale > 0.f) || !std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
-  if (D > 128 || D % 8 != 0) return ATTN_ERR_UNSUPPORTED;
+  if (D > 256 || D % 8 != 0) return ATTN_ERR_UNSUPPORTED;
   if (B == 0 || H == 0 || Nq == 0) return ATTN_OK;  // nothing is read or written
   // Query rows that see no key at all (Nk = 0, or causal with Nq > Nk) are not
   // produced by the kernel.
@@ -178,6 +185,7 @@ attn_status_t launch_fwd(const void* q, const void* k, const void* v, void* o, f
     if (e[0] == '1' && e[1] == 0) T = 1;
     if (e[0] == '2' && e[1] == 0) T = 2;
   }
+  if (D > 128) T = 1;  // the D = 256 kernel holds one query tile (TMEM)
   prm.lse = lse;
   prm.Nq = int(Nq);
   prm.Nk = int(Nk);
@@ -206,16 +214,19 @@ attn_status_t launch_fwd(const void* q, const void* k, const void* v, void* o, f
     if (e[0] == '0' && e[1] == 0) persist = false;
     if (e[0] == '1' && e[1] == 0) persist = true;
   }
+  if (D > 128) persist = false;  // the D = 256 kernel stages O in its Q buffer
   const int64_t ctas = persist && prm.n_work > sms ? sms : prm.n_work;
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t err;
-  // Head dims below 64 or 128 run on that kernel: the tensor maps carry the true
+  // Head dims below 64, 128 or 256 run on that kernel: the tensor maps carry the true
   // D, so TMA fills the missing columns with zeros on load (they add nothing to
   // Q K^T, and P V gives zeros there) and leaves them out on store.
   if (D <= 64)
     err = causal ? launch<64, true>(prm, ctas, persist, st) : launch<64, false>(prm, ctas, persist, st);
-  else
+  else if (D <= 128)
     err = causal ? launch<128, true>(prm, ctas, persist, st) : launch<128, false>(prm, ctas, persist, st);
+  else
+    err = causal ? launch<256, true>(prm, ctas, persist, st) : launch<256, false>(prm, ctas, persist, st);
   return err == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 

@@ -80,17 +80,24 @@ struct FwdParams {
 
 template <int D>
 struct Cfg {
-  static_assert(D == 64 || D == 128, "head dim");
+  static_assert(D == 64 || D == 128 || D == 256, "head dim");
   static constexpr int KB = D / 64;                      // 64-column sub-tiles per tile
   static constexpr uint32_t TILE = KB * kSubTile;        // bytes of one 128 x D bf16 tile
+  // Query tiles per unit at most: at D = 256 one (S 128 + O 256 TMEM columns;
+  // a second tile would need 768).
+  static constexpr int MAXT = D == 256 ? 1 : 2;
   // Q buffers per query tile: at D = 64 two, so a unit's Q loads while the unit
   // before still reads the other (short units would otherwise wait for it).
   static constexpr int NQB = D == 64 ? 2 : 1;
-  static constexpr int NSLOT = D == 128 ? 4 : 9;         // K/V ring slots (one tile each)
+  // K/V ring slots (one tile each): 2 at D = 256 (one key step ahead).
+  static constexpr int NSLOT = D == 256 ? 2 : (D == 128 ? 4 : 9);
+  // At D = 256 the epilogue stages O in the Q buffer (free once the unit's
+  // last S MMA has finished), so that kernel runs one unit per CTA.
+  static constexpr bool STAGE_IN_Q = D == 256;
   static constexpr uint32_t OFF_INVL = 1024;             // [2][128] fp32: 1/l of each row of tile i
-  static constexpr uint32_t OFF_Q = 2048;                      // Q buffer i * NQB + b of tile i
-  static constexpr uint32_t OFF_STG = OFF_Q + 2 * NQB * TILE;  // O staging tile of the TMA store
-  static constexpr uint32_t OFF_KV = OFF_STG + TILE;
+  static constexpr uint32_t OFF_Q = 2048;                // Q buffer i * NQB + b of tile i
+  static constexpr uint32_t OFF_STG = STAGE_IN_Q ? OFF_Q : OFF_Q + MAXT * NQB * TILE;  // O staging tile
+  static constexpr uint32_t OFF_KV = OFF_Q + MAXT * NQB * TILE + (STAGE_IN_Q ? 0u : TILE);
   static constexpr uint32_t USED = OFF_KV + NSLOT * TILE;
   static constexpr uint32_t SMEM = USED + 1024;          // + slack to align the base to 1 KB
   static_assert(SMEM <= 232448, "shared memory");
@@ -201,6 +208,7 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const A
 template <int D, bool CAUSAL, bool PERSIST>
 __global__ void __launch_bounds__(kThreads, 1) attn_fwd_sm103(const __grid_constant__ FwdParams p) {
   using C = Cfg<D>;
+  static_assert(!(PERSIST && C::STAGE_IN_Q), "O staged in the Q buffer: one unit per CTA");
   constexpr int KB = C::KB;
   constexpr int NSLOT = C::NSLOT;
 
@@ -312,6 +320,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_sm103(const __grid_const
       // The whole warp runs this loop with warp-uniform values; one elected
       // lane issues each tcgen05.mma and tcgen05.commit.
       constexpr uint32_t kIdescS = sm103::idesc_bf16_f32(BM, BN, 0, 0);  // Q, K both K-major
+      // S's MMAs fully unrolled up to D = 128; at D = 256 four at a time (fewer
+      // hoisted descriptor offsets: this warp runs at 88 registers).
+      constexpr int kUnrollS = D / 16 <= 8 ? D / 16 : 4;
       constexpr uint32_t kIdescO = sm103::idesc_bf16_f32(BM, D, 0, 1);   // P K-major, V MN-major
       // Descriptors (low words) are built once; moving an operand by `off` bytes
       // adds off >> 4 to the start-address field (no carry: shared addresses stay
@@ -342,7 +353,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_sm103(const __grid_const
           const int qi = i * C::NQB + (i == 0 ? nu0 : nu1) % C::NQB;
           const uint32_t dk = desc_k + slot_off(int(cb) + 2 * j), dq = desc_q + uint32_t(qi) * (C::TILE >> 4);
           const uint32_t dS = tmem + C::COL_S + uint32_t(i) * BN;
-#pragma unroll
+#pragma unroll(kUnrollS)
           for (int kk = 0; kk < D / 16; ++kk) {  // 16 of the head dim per MMA
             const uint32_t off = (uint32_t(kk >> 2) * kSubTile + uint32_t(kk & 3) * 32u) >> 4;
             sm103::mma_ss_warp_lo(dS, dq + off, dk + off, kIdescS, kk > 0 ? 1u : 0u, hi);
