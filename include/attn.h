@@ -52,9 +52,9 @@ typedef enum {
  *           (a ragged last tile is masked).  B, H or N equal to 0 is an empty
  *           problem: ATTN_OK, nothing launched, and the pointers (which may
  *           then be null) are not examined.
- * D       : head dimension, a multiple of 8 up to 128 (others:
- *           ATTN_ERR_UNSUPPORTED).  Below 64 or 128 the computation runs at
- *           that width with zero padding (the padding is never read from or
+ * D       : head dimension, a multiple of 8 up to 256 (others:
+ *           ATTN_ERR_UNSUPPORTED).  Below 64, 128 or 256 the computation runs
+ *           at that width with zero padding (the padding is never read from or
  *           written to memory).
  * causal  : nonzero -> key j is visible to query i only when j <= i.
  * scale   : softmax scale applied to the logits, finite and > 0 (usually
@@ -63,7 +63,7 @@ typedef enum {
  *
  * The caller owns every buffer.  Argument errors return synchronously with
  * nothing launched: ATTN_ERR_INVALID_ARG, or ATTN_ERR_UNSUPPORTED for a head
- * dimension that is not a multiple of 8 up to 128, or a device that is not
+ * dimension that is not a multiple of 8 up to 256, or a device that is not
  * sm_103.  A failed
  * launch returns ATTN_ERR_CUDA.  A kernel that hits a pipeline timeout does
  * not trap: it records ATTN_ERR_TIMEOUT in a device status word that
@@ -135,8 +135,8 @@ attn_status_t attn_fwd_from_host(const void* q_host, const void* k_host, const v
  * D_i = sum_d dO_id O_id, which the chain rule through the softmax needs
  * (ds_ij = p_ij (dp_ij - D_i)); returned so that no scratch memory is needed.
  * Outputs must not overlap each other or any input.  Same sizes, alignment
- * (16 bytes for bf16 tensors, 4 for fp32), scale and head-dim rules as
- * attn_fwd.  The pages call the backward an order of magnitude harder than
+ * (16 bytes for bf16 tensors, 4 for fp32) and scale rules as attn_fwd; head
+ * dims a multiple of 8 up to 128 (ATTN_ERR_UNSUPPORTED above).  The pages call the backward an order of magnitude harder than
  * the forward ("GPUの爆発的な性能向上", ja.news.hada.io topic 14783) without a
  * formula; the math is the chain rule written out in oracle/attn_oracle_bwd.c
  * and the kernels' header comment.  Two kernels are enqueued (dQ and D first,
