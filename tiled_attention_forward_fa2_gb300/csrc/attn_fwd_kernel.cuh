@@ -73,6 +73,7 @@ struct FwdParams {
   int tiles_per_cta;           // T = 1 or 2 query tiles per unit
   int n_units;                 // ceil(n_qtiles / T): units per (batch, head)
   int n_work;                  // n_units * B*H: units of the whole problem
+  int lpt;                     // causal: nonzero -> heaviest units first over all heads, else a head's units adjacent
   float scale_log2;            // scale * log2(e)
   long long timeout_cycles;
   int withhold_kv;             // test hook: nonzero -> no K/V loads are issued, so the pipeline waits run out
@@ -128,9 +129,10 @@ struct Cfg {
 };
 
 // The unit a CTA works on: query tiles t0 (and t0 + 1), key tiles nk0 (nk1)
-// visited by them; nk1 = 0 when the unit has one tile.  Causal: heaviest units
-// first (longest-processing-time order over all heads).  Full: the units of one
-// head are adjacent, so CTAs working at the same time share its K and V in L2.
+// visited by them; nk1 = 0 when the unit has one tile.  Causal with units of
+// very different lengths (p.lpt): heaviest units first (longest-processing-time
+// order over all heads).  Otherwise the units of one head are adjacent, so CTAs
+// working at the same time share its K and V in L2.
 struct Unit {
   int t0, bh, nk0, nk1;
   __device__ __forceinline__ int nk() const { return max(nk0, nk1); }
@@ -140,7 +142,7 @@ template <bool CAUSAL>
 __device__ __forceinline__ Unit unit_of(const FwdParams& p, int w) {
   Unit u;
   int unit;
-  if (CAUSAL) {
+  if (CAUSAL && p.lpt) {
     unit = p.n_units - 1 - w / p.bh;
     u.bh = w % p.bh;
   } else {
