@@ -28,11 +28,19 @@ def _lib():
     pkg.library()
 
 
+def sampled(B, H, N, n, seed):
+    rng = np.random.default_rng(seed)
+    return rng.integers(0, B * H, n).astype(np.int64), rng.integers(0, N, n).astype(np.int64)
+
+
+@pytest.mark.parametrize("D,persist", [(64, "1"), (64, "0"), (128, "1"), (128, "0"), (256, "0")])
 @pytest.mark.parametrize("tiles", ["1", "2"])
-def test_wait_timeout_is_reported_and_device_stays_usable(tiles, monkeypatch):
+def test_wait_timeout_is_reported_and_device_stays_usable(tiles, D, persist, monkeypatch):
+    """320 heads: on the persistent grid every CTA holds about four units when the wait runs out."""
     monkeypatch.setenv("ATTN_TILES_PER_CTA", tiles)
-    B, H, N, D = 1, 4, 512, 64
-    q, k, v = make_qkv(B, H, N, D, seed=90)
+    monkeypatch.setenv("ATTN_PERSISTENT", persist)
+    B, H, N = 1, 320, 512
+    q, k, v = make_qkv(B, H, N, D, seed=90 + D)
     qd, kd, vd = to_dev(q), to_dev(k), to_dev(v)
     o = torch.empty_like(qd)
     lse = torch.empty((B, H, N), device="cuda")
@@ -48,5 +56,8 @@ def test_wait_timeout_is_reported_and_device_stays_usable(tiles, monkeypatch):
     monkeypatch.delenv("ATTN_TEST_WITHHOLD_KV")
     assert pkg.attn_fwd(qd, kd, vd, o, lse, B, H, N, D, True, 0.125, s) == pkg.ATTN_OK
     assert pkg.attn_last_status(s) == pkg.ATTN_OK
-    o_ref, lse_ref = oracle.attn_fwd(q, k, v, True, 0.125)
-    assert_close(o_to_f64(o), lse.cpu().numpy().astype(np.float64), o_ref, lse_ref, "after a timeout")
+    bh, ri = sampled(B, H, N, 2048, 91)
+    o_ref, lse_ref = oracle.attn_rows(q, k, v, True, 0.125, bh, ri)
+    of = o_to_f64(o).reshape(B * H, N, D)[bh, ri]
+    lf = lse.cpu().numpy().astype(np.float64).reshape(B * H, N)[bh, ri]
+    assert_close(of, lf, o_ref, lse_ref, f"after a timeout D={D} persistent={persist} T={tiles}")
