@@ -10,8 +10,11 @@
 // Two kernels, launched in this order on one stream; neither needs scratch
 // memory (D is an output):
 //   attn_bwd_dq_sm103  : one CTA per 128-query tile.  D_i from O and dO, then
-//       per key tile S = Q K^T and dP = dO V^T into TMEM, dS (bf16) over S,
-//       dQ += dS K with dS read from TMEM; dQ stored with TMA.
+//       per key tile S = Q K^T (into one of two TMEM buffers, alternating) and
+//       dP = dO V^T into TMEM, dS (bf16) over S, dQ += dS K with dS read from
+//       TMEM; dQ stored with TMA.  The elementwise warps take dP into
+//       registers first and release its columns, so the next key tile's S and
+//       dP are computed while they work on this one's dS.
 //   attn_bwd_dkdv_sm103: one CTA per 128-key tile, transposed: per query tile
 //       S^T = K Q^T and dP^T = V dO^T, P^T and dS^T (bf16) over them, then
 //       dV += P^T dO and dK += dS^T Q; the per-query LSE and D reach every
@@ -46,19 +49,30 @@ template <int D>
 struct CfgDq {
   static constexpr int KB = D / 64;
   static constexpr uint32_t TILE = KB * kSubTile;
-  static constexpr int NSLOT = D == 128 ? 4 : 8;   // K/V ring (K_j, V_j alternate)
+  // Separate rings for K and V, sized to how long each tile is needed: K_j
+  // until dQ_j (the end of step j), V_j only until dP_j.  Three K slots and two
+  // V slots give every load a whole step of lead (one four-slot ring left the
+  // MMA warp waiting ~1760 cycles a step for K/V).
+  static constexpr int NK = D == 128 ? 3 : 5, NV = D == 128 ? 2 : 3;
+  static constexpr int NSLOT = NK + NV;            // K slots, then V slots
   static constexpr uint32_t OFF_Q = 1024, OFF_DO = OFF_Q + TILE, OFF_KV = OFF_DO + TILE;
   static constexpr uint32_t SMEM = OFF_KV + NSLOT * TILE + 1024;
   static_assert(SMEM <= 232448, "shared memory");
+  // B_SF: S_j and dP_j in TMEM (MMA commit); B_DPR: dP_j in the elementwise
+  // warps' registers (128 arrivals); B_DSF[j & 1]: dS_j in TMEM (128 arrivals).
+  // Two dS barriers: S_{j+1} is issued before the MMA warp waits for dS_j, so
+  // on a single barrier dS_{j+1} could complete a phase the MMA warp had not
+  // yet seen; dS_{j+2} needs S_{j+2}, which is only issued after that wait.
   static constexpr int B_Q = 0, B_FULL = 1, B_EMPTY = 1 + NSLOT, B_SF = 1 + 2 * NSLOT, B_DSF = B_SF + 1,
-                       B_QDONE = B_DSF + 1, B_DONE = B_QDONE + 1, NBAR = B_DONE + 1;
-  static constexpr uint32_t COL_S = 0, COL_DP = 128, COL_DQ = 256;  // dS (bf16) over S's first 64 columns
+                       B_DPR = B_DSF + 2, B_QDONE = B_DPR + 1, B_DONE = B_QDONE + 1, NBAR = B_DONE + 1;
+  // S_j at COL_S + 128 (j & 1), dS_j (bf16) over its first 64 columns.
+  static constexpr uint32_t COL_S = 0, COL_DP = 256, COL_DQ = 384;
 };
 
 template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dq_sm103(const __grid_constant__ BwdParams p) {
   using C = CfgDq<D>;
-  constexpr int KB = C::KB, NSLOT = C::NSLOT;
+  constexpr int KB = C::KB, NK = C::NK, NV = C::NV;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = sm103::smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -82,7 +96,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dq_sm103(const __grid
   const int nk = CAUSAL ? min(p.n_ktiles, (min(m0 + BM - 1, p.Nq - 1) + p.kv_off) / BN + 1) : p.n_ktiles;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < C::NBAR; ++i) sm103::mbar_init(bar(i), i == C::B_DSF ? uint32_t(BM) : 1u);
+    for (int i = 0; i < C::NBAR; ++i)
+      sm103::mbar_init(bar(i), (i == C::B_DSF || i == C::B_DSF + 1 || i == C::B_DPR) ? uint32_t(BM) : 1u);
     *abort_flag = 0u;
     sm103::fence_mbar_init();
   }
@@ -103,20 +118,26 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dq_sm103(const __grid
         sm103::tma_load_3d(sQ + kb * kSubTile, &p.tq, bar(C::B_Q), kb * 64, m0, bh);
         sm103::tma_load_3d(sDO + kb * kSubTile, &p.tdo, bar(C::B_Q), kb * 64, m0, bh);
       }
-      int c = 0;
+      int ck = 0, cv = 0;  // K and V loads issued
       bool ok = true;
+      auto load = [&](int j, bool is_k) -> bool {
+        const int n = is_k ? NK : NV, s = (is_k ? 0 : NK) + j % n;
+        if (j >= n && !wait_bounded(bar(C::B_EMPTY + s), uint32_t(j / n - 1) & 1u, ab)) return false;
+        sm103::mbar_arrive_expect_tx(bar(C::B_FULL + s), C::TILE);
+        for (int kb = 0; kb < KB; ++kb)
+          sm103::tma_load_3d(sKV + s * C::TILE + kb * kSubTile, is_k ? &p.tk : &p.tv, bar(C::B_FULL + s), kb * 64,
+                             j * BN, bh);
+        return true;
+      };
       for (int j = 0; ok && j < nk; ++j) {
-        for (int kv = 0; kv < 2; ++kv, ++c) {
-          const int s = c % NSLOT;
-          if (c >= NSLOT && !(ok = wait_bounded(bar(C::B_EMPTY + s), uint32_t(c / NSLOT - 1) & 1u, ab))) break;
-          sm103::mbar_arrive_expect_tx(bar(C::B_FULL + s), C::TILE);
-          const CUtensorMap* map = kv == 0 ? &p.tk : &p.tv;
-          for (int kb = 0; kb < KB; ++kb)
-            sm103::tma_load_3d(sKV + s * C::TILE + kb * kSubTile, map, bar(C::B_FULL + s), kb * 64, j * BN, bh);
-        }
+        if (!(ok = load(j, true))) break;
+        ++ck;
+        if (!(ok = load(j, false))) break;
+        ++cv;
       }
       drain_wait(bar(C::B_Q), 0u);
-      for (int t = c > NSLOT ? c - NSLOT : 0; t < c; ++t) drain_wait(bar(C::B_FULL + t % NSLOT), uint32_t(t / NSLOT) & 1u);
+      for (int t = ck > NK ? ck - NK : 0; t < ck; ++t) drain_wait(bar(C::B_FULL + t % NK), uint32_t(t / NK) & 1u);
+      for (int t = cv > NV ? cv - NV : 0; t < cv; ++t) drain_wait(bar(C::B_FULL + NK + t % NV), uint32_t(t / NV) & 1u);
     }
     __syncwarp();
   } else if (warp == kBwdMmaWarp) {
@@ -124,15 +145,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dq_sm103(const __grid
     constexpr uint32_t kIdescQ = sm103::idesc_bf16_f32(BM, D, 0, 1);   // dS from TMEM, K MN-major
     const uint64_t dq_k = sm103::sdesc_sw128(sQ, 16, 1024), ddo_k = sm103::sdesc_sw128(sDO, 16, 1024);
     const uint64_t dkv_k = sm103::sdesc_sw128(sKV, 16, 1024), dkv_mn = sm103::sdesc_sw128(sKV, kSubTile, 1024);
-    auto slot_off = [](int c) { return uint64_t(uint32_t(c % NSLOT) * (C::TILE >> 4)); };
-    auto wait_full = [&](int c) { return warp_wait(bar(C::B_FULL + c % NSLOT), uint32_t(c / NSLOT) & 1u, ab); };
-    auto release = [&](int c) { sm103::mma_commit_warp(bar(C::B_EMPTY + c % NSLOT)); };
-    auto issue_s_dp = [&](int j) {  // S = Q K_j^T, dP = dO V_j^T
-      const uint64_t dk = dkv_k + slot_off(2 * j), dv = dkv_k + slot_off(2 * j + 1);
+    // Ring slot of K_j (kv = 0) or V_j (kv = 1), its fill phase, and release.
+    auto slot = [](int j, int kv) { return kv == 0 ? j % NK : NK + j % NV; };
+    auto slot_off = [&](int j, int kv) { return uint64_t(uint32_t(slot(j, kv)) * (C::TILE >> 4)); };
+    auto wait_full = [&](int j, int kv) {
+      return warp_wait(bar(C::B_FULL + slot(j, kv)), uint32_t(j / (kv == 0 ? NK : NV)) & 1u, ab);
+    };
+    auto release = [&](int j, int kv) { sm103::mma_commit_warp(bar(C::B_EMPTY + slot(j, kv))); };
+    auto issue_s_dp = [&](int j) {  // S = Q K_j^T (buffer j & 1), dP = dO V_j^T
+      const uint64_t dk = dkv_k + slot_off(j, 0), dv = dkv_k + slot_off(j, 1);
+      const uint32_t dS = tmem + C::COL_S + uint32_t(j & 1) * BN;
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint64_t off = uint64_t((uint32_t(kk >> 2) * kSubTile + uint32_t(kk & 3) * 32u) >> 4);
-        sm103::mma_ss_warp(tmem + C::COL_S, dq_k + off, dk + off, kIdescS, kk > 0 ? 1u : 0u);
+        sm103::mma_ss_warp(dS, dq_k + off, dk + off, kIdescS, kk > 0 ? 1u : 0u);
       }
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
@@ -140,27 +166,31 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dq_sm103(const __grid
         sm103::mma_ss_warp(tmem + C::COL_DP, ddo_k + off, dv + off, kIdescS, kk > 0 ? 1u : 0u);
       }
       sm103::mma_commit_warp(bar(C::B_SF));
-      release(2 * j + 1);  // V_j is done with
+      release(j, 1);  // V_j is done with
     };
-    bool ok = warp_wait(bar(C::B_Q), 0u, ab) && wait_full(0) && wait_full(1);
+    bool ok = warp_wait(bar(C::B_Q), 0u, ab) && wait_full(0, 0) && wait_full(0, 1);
     if (ok) {
       sm103::tc_fence_after();
       issue_s_dp(0);
     }
     for (int j = 0; ok && j < nk; ++j) {
-      if (!(ok = warp_wait(bar(C::B_DSF), uint32_t(j) & 1u, ab))) break;
-      sm103::tc_fence_after();
-      const uint64_t dkmn = dkv_mn + slot_off(2 * j);
-#pragma unroll
-      for (int kk = 0; kk < BN / 16; ++kk)  // dQ += dS K_j: 16 keys per MMA
-        sm103::mma_ts_warp(tmem + C::COL_DQ, tmem + C::COL_S + kk * 8, dkmn + uint64_t(kk * (2048 >> 4)), kIdescQ,
-                           (j > 0 || kk > 0) ? 1u : 0u);
-      release(2 * j);  // K_j is done with
       if (j + 1 < nk) {
-        if (!(ok = wait_full(2 * j + 2) && wait_full(2 * j + 3))) break;
+        // S_{j+1} goes to the other buffer (its dS_{j-1} was read by the dQ MMA
+        // issued before); dP_{j+1} once dP_j has left TMEM.
+        if (!(ok = wait_full(j + 1, 0) && wait_full(j + 1, 1))) break;
+        if (!(ok = warp_wait(bar(C::B_DPR), uint32_t(j) & 1u, ab))) break;
         sm103::tc_fence_after();
         issue_s_dp(j + 1);
       }
+      if (!(ok = warp_wait(bar(C::B_DSF + (j & 1)), uint32_t(j >> 1) & 1u, ab))) break;
+      sm103::tc_fence_after();
+      const uint64_t dkmn = dkv_mn + slot_off(j, 0);
+      const uint32_t aS = tmem + C::COL_S + uint32_t(j & 1) * BN;
+#pragma unroll
+      for (int kk = 0; kk < BN / 16; ++kk)  // dQ += dS K_j: 16 keys per MMA
+        sm103::mma_ts_warp(tmem + C::COL_DQ, aS + kk * 8, dkmn + uint64_t(kk * (2048 >> 4)), kIdescQ,
+                           (j > 0 || kk > 0) ? 1u : 0u);
+      release(j, 0);  // K_j is done with
     }
     sm103::mma_commit_warp(bar(C::B_QDONE));
     sm103::mma_commit_warp(bar(C::B_DONE));
@@ -199,11 +229,21 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dq_sm103(const __grid
       sm103::tc_fence_after();
       int lim = min(BN - 1, p.Nk - 1 - j * BN);
       if (CAUSAL) lim = min(lim, row + p.kv_off - j * BN);
+      // dP_j - D into registers, then its TMEM columns go back to the MMA warp.
+      float dpd[BN];
+      {
+        uint32_t ud[BN];
+        sm103::tmem_ld128(tmem + lane_off + C::COL_DP, ud);
+#pragma unroll
+        for (int c = 0; c < BN; ++c) dpd[c] = __uint_as_float(ud[c]) - dlt;
+      }
+      sm103::tc_fence_before();
+      sm103::mbar_arrive(bar(C::B_DPR));
+      const uint32_t tS = tmem + lane_off + C::COL_S + uint32_t(j & 1) * BN;
 #pragma unroll
       for (int q = 0; q < BN / 32; ++q) {
-        uint32_t us[32], ud[32];
-        sm103::tmem_ld32(tmem + lane_off + C::COL_S + q * 32, us);
-        sm103::tmem_ld32(tmem + lane_off + C::COL_DP + q * 32, ud);
+        uint32_t us[32];
+        sm103::tmem_ld32(tS + q * 32, us);
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
@@ -213,13 +253,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dq_sm103(const __grid
           const int c = q * 32 + 2 * e;
           const float p0 = c > lim ? 0.f : sm103::ex2_approx(t0);
           const float p1 = c + 1 > lim ? 0.f : sm103::ex2_approx(t1);
-          pk[e] = sm103::pack_bf16x2(p0 * (__uint_as_float(ud[2 * e]) - dlt), p1 * (__uint_as_float(ud[2 * e + 1]) - dlt));
+          pk[e] = sm103::pack_bf16x2(p0 * dpd[c], p1 * dpd[c + 1]);
         }
-        sm103::tmem_st16(tmem + lane_off + C::COL_S + q * 16, pk);  // dS over the first 64 columns of S
+        sm103::tmem_st16(tS + q * 16, pk);  // dS over the first 64 columns of S_j
       }
       sm103::tmem_st_wait();
       sm103::tc_fence_before();
-      sm103::mbar_arrive(bar(C::B_DSF));
+      sm103::mbar_arrive(bar(C::B_DSF + (j & 1)));
     }
     if (ok) ok = __all_sync(0xffffffffu, wait_bounded(bar(C::B_QDONE), 0u, ab));
     if (ok) {
