@@ -15,10 +15,12 @@
 //       TMEM; dQ stored with TMA.  The elementwise warps take dP into
 //       registers first and release its columns, so the next key tile's S and
 //       dP are computed while they work on this one's dS.
-//   attn_bwd_dkdv_sm103: one CTA per 128-key tile, transposed: per query tile
-//       S^T = K Q^T and dP^T = V dO^T, P^T and dS^T (bf16) over them, then
-//       dV += P^T dO and dK += dS^T Q; the per-query LSE and D reach every
-//       thread through shared memory; dK, dV stored with TMA.
+//   attn_bwd_dkdv_sm103: one CTA per 128-key tile, transposed: per half of a
+//       query tile (64 queries) S^T = K Q^T and dP^T = V dO^T into one of two
+//       TMEM buffers, P^T and dS^T (bf16) over them, then dV += P^T dO and
+//       dK += dS^T Q; the next half's S^T and dP^T are computed while the
+//       elementwise warps work on this one.  The per-query LSE and D reach
+//       every thread through shared memory; dK, dV stored with TMA.
 // Warp roles as in the forward: warps 0-3 elementwise (thread = TMEM lane =
 // row), warp 4 TMA producer, warp 5 TMEM allocation and warp-uniform MMA issue.
 // Every wait is bounded (see wait_bounded in attn_fwd_kernel.cuh).
@@ -309,9 +311,14 @@ struct CfgDkv {
   static constexpr uint32_t SMEM = OFF_ST + NSTAGE * 2 * TILE + 1024;
   static_assert(SMEM <= 232448, "shared memory");
   static_assert(OFF_VEC + NSTAGE * 2 * 128 * 4 <= OFF_K, "vector area");
-  static constexpr int B_KV = 0, B_SFULL = 1, B_SEMPTY = 1 + NSTAGE, B_SF = 1 + 2 * NSTAGE, B_PF = B_SF + 1,
-                       B_ACC = B_PF + 1, B_DONE = B_ACC + 1, NBAR = B_DONE + 1;
-  static constexpr uint32_t COL_S = 0, COL_DP = 128, COL_DV = 256, COL_DK = 256 + D;
+  // Half steps h (64 queries): S^T and dP^T in buffer h & 1 (B_SF[h & 1], MMA
+  // commit), P^T and dS^T written over them (B_PF[h & 1], 128 arrivals).
+  static constexpr int HQ = 64;                            // queries per half step
+  static constexpr int B_KV = 0, B_SFULL = 1, B_SEMPTY = 1 + NSTAGE, B_SF = 1 + 2 * NSTAGE, B_PF = B_SF + 2,
+                       B_ACC = B_PF + 2, B_DONE = B_ACC + 1, NBAR = B_DONE + 1;
+  // Buffer b: S^T at 128 b, dP^T at 128 b + 64 (64 columns each; P^T, dS^T
+  // bf16 over their first 32).
+  static constexpr uint32_t COL_S = 0, COL_DP = 64, COL_DV = 256, COL_DK = 256 + D;
 };
 
 template <int D, bool CAUSAL>
@@ -346,8 +353,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dkdv_sm103(const __gr
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::NBAR; ++i) {
       uint32_t cnt = 1;
-      if (i >= C::B_SFULL && i < C::B_SFULL + NSTAGE) cnt = 32;  // the producer warp's lanes
-      if (i == C::B_PF) cnt = BM;
+      // the producer warp's 32 lanes (vectors written) + lane 0's expect-tx arrival
+      if (i >= C::B_SFULL && i < C::B_SFULL + NSTAGE) cnt = 33;
+      if (i == C::B_PF || i == C::B_PF + 1) cnt = BM;
       sm103::mbar_init(bar(i), cnt);
     }
     *abort_flag = 0u;
@@ -376,16 +384,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dkdv_sm103(const __gr
     bool ok = true;
     for (int it = 0; ok && it < niter; ++it) {
       const int st = it % NSTAGE;
-      if (it >= NSTAGE && !(ok = warp_wait(bar(C::B_SEMPTY + st), uint32_t(it / NSTAGE - 1) & 1u, ab))) break;
       const int i0 = (it0 + it) * BM;
-      // Per-query LSE (base 2) and D for this tile; queries past Nq get P = 0.
+      // Per-query LSE (base 2) and D for this tile (queries past Nq get P = 0),
+      // read before the stage is free so the loads overlap the wait; the tile
+      // copies go out first once it is free.
+      float lse4[4], d4[4];
 #pragma unroll
       for (int x = 0; x < 4; ++x) {
-        const int col = lane * 4 + x, i = i0 + col;
+        const int i = i0 + lane * 4 + x;
         const bool live = i < p.Nq;
-        vec[(st * 2 + 0) * BM + col] = live ? p.lse[size_t(bh) * p.Nq + i] * 1.4426950408889634f : INFINITY;
-        vec[(st * 2 + 1) * BM + col] = live ? p.delta[size_t(bh) * p.Nq + i] : 0.f;
+        lse4[x] = live ? p.lse[size_t(bh) * p.Nq + i] * 1.4426950408889634f : INFINITY;
+        d4[x] = live ? p.delta[size_t(bh) * p.Nq + i] : 0.f;
       }
+      if (it >= NSTAGE && !(ok = warp_wait(bar(C::B_SEMPTY + st), uint32_t(it / NSTAGE - 1) & 1u, ab))) break;
       if (lane == 0) {
         sm103::mbar_arrive_expect_tx(bar(C::B_SFULL + st), 2u * C::TILE);
         const uint32_t sq = sST + uint32_t(st) * 2u * C::TILE, sdo = sq + C::TILE;
@@ -393,9 +404,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dkdv_sm103(const __gr
           sm103::tma_load_3d(sq + kb * kSubTile, &p.tq, bar(C::B_SFULL + st), kb * 64, i0, bh);
           sm103::tma_load_3d(sdo + kb * kSubTile, &p.tdo, bar(C::B_SFULL + st), kb * 64, i0, bh);
         }
-      } else {
-        sm103::mbar_arrive(bar(C::B_SFULL + st));
       }
+#pragma unroll
+      for (int x = 0; x < 4; ++x) {
+        vec[(st * 2 + 0) * BM + lane * 4 + x] = lse4[x];
+        vec[(st * 2 + 1) * BM + lane * 4 + x] = d4[x];
+      }
+      sm103::mbar_arrive(bar(C::B_SFULL + st));  // releases this lane's vector stores
       ++issued;
     }
     if (lane == 0) {
@@ -406,38 +421,58 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dkdv_sm103(const __gr
     __syncwarp();
   } else if (warp == kBwdMmaWarp) {
     // ------------------------------------------------------------- MMA issue
-    constexpr uint32_t kIdescS = sm103::idesc_bf16_f32(BM, BM, 0, 0);  // S^T, dP^T: both K-major
-    constexpr uint32_t kIdescA = sm103::idesc_bf16_f32(BM, D, 0, 1);   // P^T / dS^T from TMEM, B MN-major
+    constexpr uint32_t kIdescS = sm103::idesc_bf16_f32(BM, C::HQ, 0, 0);  // S^T, dP^T: both K-major
+    constexpr uint32_t kIdescA = sm103::idesc_bf16_f32(BM, D, 0, 1);      // P^T / dS^T from TMEM, B MN-major
     const uint64_t dk_k = sm103::sdesc_sw128(sK, 16, 1024), dv_k = sm103::sdesc_sw128(sV, 16, 1024);
     const uint64_t dst_k = sm103::sdesc_sw128(sST, 16, 1024), dst_mn = sm103::sdesc_sw128(sST, kSubTile, 1024);
-    bool ok = warp_wait(bar(C::B_KV), 0u, ab);
-    for (int it = 0; ok && it < niter; ++it) {
-      const int st = it % NSTAGE;
-      if (!(ok = warp_wait(bar(C::B_SFULL + st), uint32_t(it / NSTAGE) & 1u, ab))) break;
-      sm103::tc_fence_after();
-      const uint64_t soff = uint64_t(uint32_t(st) * 2u * (C::TILE >> 4));
+    constexpr uint64_t kHalf = uint64_t((C::HQ * 128u) >> 4);  // 64 rows of a 128-byte-row tile
+    // S^T and dP^T of half step h into buffer h & 1.
+    auto issue_s = [&](int h) {
+      const int it = h >> 1, st = it % NSTAGE;
+      const uint64_t soff = uint64_t(uint32_t(st) * 2u * (C::TILE >> 4)) + uint64_t(h & 1) * kHalf;
       const uint64_t q_k = dst_k + soff, do_k = dst_k + soff + (C::TILE >> 4);
+      const uint32_t buf = tmem + uint32_t(h & 1) * 128u;
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {  // S^T = K Q^T
         const uint64_t off = uint64_t((uint32_t(kk >> 2) * kSubTile + uint32_t(kk & 3) * 32u) >> 4);
-        sm103::mma_ss_warp(tmem + C::COL_S, dk_k + off, q_k + off, kIdescS, kk > 0 ? 1u : 0u);
+        sm103::mma_ss_warp(buf + C::COL_S, dk_k + off, q_k + off, kIdescS, kk > 0 ? 1u : 0u);
       }
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {  // dP^T = V dO^T
         const uint64_t off = uint64_t((uint32_t(kk >> 2) * kSubTile + uint32_t(kk & 3) * 32u) >> 4);
-        sm103::mma_ss_warp(tmem + C::COL_DP, dv_k + off, do_k + off, kIdescS, kk > 0 ? 1u : 0u);
+        sm103::mma_ss_warp(buf + C::COL_DP, dv_k + off, do_k + off, kIdescS, kk > 0 ? 1u : 0u);
       }
-      sm103::mma_commit_warp(bar(C::B_SF));
-      if (!(ok = warp_wait(bar(C::B_PF), uint32_t(it) & 1u, ab))) break;
+      sm103::mma_commit_warp(bar(C::B_SF + (h & 1)));
+    };
+    const int nh = 2 * niter;
+    bool ok = warp_wait(bar(C::B_KV), 0u, ab) && (nh == 0 || warp_wait(bar(C::B_SFULL), 0u, ab));
+    if (ok && nh > 0) {
       sm103::tc_fence_after();
-      const uint64_t q_mn = dst_mn + soff, do_mn = dst_mn + soff + (C::TILE >> 4);
-#pragma unroll
-      for (int kk = 0; kk < BM / 16; ++kk) {  // dV += P^T dO, dK += dS^T Q: 16 queries per MMA
-        const uint64_t off = uint64_t(kk * (2048 >> 4));
-        sm103::mma_ts_warp(tmem + C::COL_DV, tmem + C::COL_S + kk * 8, do_mn + off, kIdescA, (it > 0 || kk > 0) ? 1u : 0u);
-        sm103::mma_ts_warp(tmem + C::COL_DK, tmem + C::COL_DP + kk * 8, q_mn + off, kIdescA, (it > 0 || kk > 0) ? 1u : 0u);
+      issue_s(0);
+    }
+    for (int h = 0; ok && h < nh; ++h) {
+      const int it = h >> 1, st = it % NSTAGE;
+      if (h + 1 < nh) {
+        // The other buffer's P^T, dS^T (half step h - 1) were read by MMAs issued before.
+        if (((h + 1) & 1) == 0) {
+          const int it1 = (h + 1) >> 1;
+          if (!(ok = warp_wait(bar(C::B_SFULL + it1 % NSTAGE), uint32_t(it1 / NSTAGE) & 1u, ab))) break;
+          sm103::tc_fence_after();
+        }
+        issue_s(h + 1);
       }
-      sm103::mma_commit_warp(bar(C::B_SEMPTY + st));
+      if (!(ok = warp_wait(bar(C::B_PF + (h & 1)), uint32_t(h >> 1) & 1u, ab))) break;
+      sm103::tc_fence_after();
+      const uint64_t soff = uint64_t(uint32_t(st) * 2u * (C::TILE >> 4)) + uint64_t(h & 1) * kHalf;
+      const uint64_t q_mn = dst_mn + soff, do_mn = dst_mn + soff + (C::TILE >> 4);
+      const uint32_t buf = tmem + uint32_t(h & 1) * 128u;
+#pragma unroll
+      for (int kk = 0; kk < C::HQ / 16; ++kk) {  // dV += P^T dO, dK += dS^T Q: 16 queries per MMA
+        const uint64_t off = uint64_t(kk * (2048 >> 4));
+        sm103::mma_ts_warp(tmem + C::COL_DV, buf + C::COL_S + kk * 8, do_mn + off, kIdescA, (h > 0 || kk > 0) ? 1u : 0u);
+        sm103::mma_ts_warp(tmem + C::COL_DK, buf + C::COL_DP + kk * 8, q_mn + off, kIdescA, (h > 0 || kk > 0) ? 1u : 0u);
+      }
+      if (h & 1) sm103::mma_commit_warp(bar(C::B_SEMPTY + st));  // both halves of the stage are done with
     }
     sm103::mma_commit_warp(bar(C::B_ACC));
     sm103::mma_commit_warp(bar(C::B_DONE));
@@ -451,43 +486,46 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dkdv_sm103(const __gr
     const uint64_t sl2x2 = sm103::f2_pack(p.scale_log2, p.scale_log2);
     const bool key_live = n < p.Nk;
     bool ok = true;
-    for (int it = 0; it < niter; ++it) {
-      const int st = it % NSTAGE;
-      if (!(ok = warp_wait(bar(C::B_SF), uint32_t(it) & 1u, ab))) break;
+    for (int h = 0; h < 2 * niter; ++h) {
+      const int it = h >> 1, st = it % NSTAGE, hf = h & 1;
+      if (!(ok = warp_wait(bar(C::B_SF + hf), uint32_t(h >> 1) & 1u, ab))) break;
       // The stage's LSE and D vectors were written by the producer lanes: wait on
       // their barrier directly (already complete) to acquire those stores.
       if (!(ok = warp_wait(bar(C::B_SFULL + st), uint32_t(it / NSTAGE) & 1u, ab))) break;
       sm103::tc_fence_after();
-      const int i0 = (it0 + it) * BM;
+      const int i0 = (it0 + it) * BM + hf * C::HQ;
       // query column c sees this key iff n <= i0 + c + kv_off, i.e. c >= n - kv_off - i0
-      const int cmin = key_live ? (CAUSAL ? n - p.kv_off - i0 : 0) : BM;
-      const float2* lv = reinterpret_cast<const float2*>(vec + (st * 2 + 0) * BM);
-      const float2* dv = reinterpret_cast<const float2*>(vec + (st * 2 + 1) * BM);
+      const int cmin = key_live ? (CAUSAL ? n - p.kv_off - i0 : 0) : C::HQ;
+      const float2* lv = reinterpret_cast<const float2*>(vec + (st * 2 + 0) * BM + hf * C::HQ);
+      const float2* dv = reinterpret_cast<const float2*>(vec + (st * 2 + 1) * BM + hf * C::HQ);
+      const uint32_t tS = tmem + lane_off + uint32_t(hf) * 128u + C::COL_S, tDP = tS + (C::COL_DP - C::COL_S);
+      // S^T and dP^T are adjacent: one load of 128 columns, one wait.
+      static_assert(C::COL_DP == C::COL_S + C::HQ && 2 * C::HQ == 128, "S^T, dP^T adjacent");
+      uint32_t u[128];
+      sm103::tmem_ld128(tS, u);
 #pragma unroll
-      for (int q = 0; q < BM / 32; ++q) {
-        uint32_t us[32], ud[32];
-        sm103::tmem_ld32(tmem + lane_off + C::COL_S + q * 32, us);
-        sm103::tmem_ld32(tmem + lane_off + C::COL_DP + q * 32, ud);
+      for (int q = 0; q < C::HQ / 32; ++q) {
         uint32_t pp[16], pd[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
           const int c = q * 32 + 2 * e;
           const float2 l2 = lv[c / 2], d2 = dv[c / 2];
-          const uint64_t t = sm103::f2_fma(sm103::f2_pack(__uint_as_float(us[2 * e]), __uint_as_float(us[2 * e + 1])),
-                                           sl2x2, sm103::f2_pack(-l2.x, -l2.y));
+          const uint64_t t = sm103::f2_fma(sm103::f2_pack(__uint_as_float(u[c]), __uint_as_float(u[c + 1])), sl2x2,
+                                           sm103::f2_pack(-l2.x, -l2.y));
           float t0, t1;
           sm103::f2_unpack(t, t0, t1);
           const float p0 = c < cmin ? 0.f : sm103::ex2_approx(t0);
           const float p1 = c + 1 < cmin ? 0.f : sm103::ex2_approx(t1);
           pp[e] = sm103::pack_bf16x2(p0, p1);
-          pd[e] = sm103::pack_bf16x2(p0 * (__uint_as_float(ud[2 * e]) - d2.x), p1 * (__uint_as_float(ud[2 * e + 1]) - d2.y));
+          pd[e] = sm103::pack_bf16x2(p0 * (__uint_as_float(u[C::HQ + c]) - d2.x),
+                                     p1 * (__uint_as_float(u[C::HQ + c + 1]) - d2.y));
         }
-        sm103::tmem_st16(tmem + lane_off + C::COL_S + q * 16, pp);   // P^T over S^T
-        sm103::tmem_st16(tmem + lane_off + C::COL_DP + q * 16, pd);  // dS^T over dP^T
+        sm103::tmem_st16(tS + q * 16, pp);   // P^T over S^T (its first 32 columns)
+        sm103::tmem_st16(tDP + q * 16, pd);  // dS^T over dP^T
       }
       sm103::tmem_st_wait();
       sm103::tc_fence_before();
-      sm103::mbar_arrive(bar(C::B_PF));
+      sm103::mbar_arrive(bar(C::B_PF + hf));
     }
     if (ok) ok = __all_sync(0xffffffffu, wait_bounded(bar(C::B_ACC), 0u, ab));
     if (ok) {
