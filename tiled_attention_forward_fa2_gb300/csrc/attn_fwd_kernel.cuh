@@ -12,15 +12,17 @@
 // swizzled shared memory; "GPUの爆発的な性能向上", ja.news.hada.io topic 14783,
 // sections "WGMMA", "Shared memoryとbank conflict", "アドレス生成とTMA",
 // "Occupancyが隠してくれるコスト") is prior art.  The work is cut into units of
-// T = 1 or 2 query tiles of 128 rows of one (batch, head); a unit streams that
-// head's K and V tiles once for its tiles.  The grid is persistent: each CTA
-// (one per SM) takes units w = blockIdx.x, blockIdx.x + gridDim.x, ... and
-// every role runs through the same sequence, so one unit's epilogue and the
-// next unit's loads overlap the tensor-core work instead of a CTA launch.
-//   warp 12      : TMA producer.  Q tiles of each unit (into the tile's buffer
-//                  once the previous unit's last S MMA on it has finished);
-//                  K_j, V_j into a ring of 128-byte-swizzled shared-memory
-//                  slots (full/empty mbarriers).
+// T = 1 or 2 query tiles of 128 rows of one (batch, head) (T = 1 at D = 256);
+// a unit streams that head's K and V tiles once for its tiles.  With PERSIST
+// the grid has one CTA per SM, each taking its units in snake order, and every
+// role runs through the same sequence, so one unit's epilogue and the next
+// unit's loads overlap the tensor-core work instead of a CTA launch; without
+// it (long key ranges, D = 256) each CTA runs one unit.
+//   warp 12      : TMA producer.  Q tiles of each unit (into a buffer of the
+//                  tile once the last S MMA of the unit that used it before has
+//                  finished; two buffers per tile at D = 64); K_j, V_j into a
+//                  ring of 128-byte-swizzled shared-memory slots (full/empty
+//                  mbarriers).
 //   warp 13      : allocates the 512 TMEM columns; one thread issues tcgen05.mma:
 //                  S_i = Q_i K_j^T into TMEM buffer i, and O_i += P_i V_j with P_i
 //                  read back from TMEM (bf16, written over S_i).  The order
