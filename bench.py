@@ -421,8 +421,8 @@ def run_ours(args, w):
     roofline["traffic"] = traffic
     roofline["algorithmic_bytes"] = alg_bytes
     roofline["flop_per_byte"] = flops / alg_bytes
-    # The launcher's grid rule: persistent up to 32 key tiles at D <= 128.
-    persist = (w.n_keys + 127) // 128 <= 32 and w.D <= 128
+    # The launcher's grid rule: persistent at D <= 64, and up to 32 key tiles at D <= 128.
+    persist = w.D <= 64 or ((w.n_keys + 127) // 128 <= 32 and w.D <= 128)
     dk = 64 if w.D <= 64 else (128 if w.D <= 128 else 256)
     roofline["kernel"] = f"attn_fwd_sm103<{dk},{str(w.causal).lower()},{'persistent' if persist else 'one unit per CTA'}>"
     cpu = None
