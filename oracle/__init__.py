@@ -86,6 +86,12 @@ class Oracle:
             lib.oracle_attn_bwd_f64.argtypes = args
             lib.oracle_attn_bwd.restype = I
             lib.oracle_attn_bwd_f64.restype = I
+            lib.oracle_attn_bwd_rows.argtypes = [P, P, P, P, I64, I64, I64, I64, I, ctypes.c_double, P, P, I64, P,
+                                                 P, I]
+            lib.oracle_attn_bwd_keys.argtypes = [P, P, P, P, I64, I64, I64, I64, I, ctypes.c_double, I64, P, I64,
+                                                 P, P, I]
+            lib.oracle_attn_bwd_rows.restype = I
+            lib.oracle_attn_bwd_keys.restype = I
         self._lib = lib
         self.path = libpath
 
@@ -170,8 +176,43 @@ def _bwd_methods(cls):
         arr = [np.ascontiguousarray(x, dtype=np.float64) for x in (q, k, v, do)]
         return _bwd_call(self._lib.oracle_attn_bwd_f64, *arr, causal, scale, nthreads)
 
+    def attn_bwd_rows(self, q, k, v, do, causal: bool, scale: float, bh_idx, row_idx, nthreads: int = 0):
+        """dQ rows [R, D] and D [R] for the query rows (bh_idx[r], row_idx[r]) only."""
+        q, k, v, do = _bits(q), _bits(k), _bits(v), _bits(do)
+        B, H, Nq, Nk, D = self._shapes(q, k, v)
+        bh = np.ascontiguousarray(bh_idx, dtype=np.int64)
+        ri = np.ascontiguousarray(row_idx, dtype=np.int64)
+        if bh.shape != ri.shape or bh.ndim != 1 or do.shape != q.shape:
+            raise ValueError("bh_idx, row_idx 1-D of one length; do shaped like q")
+        dq = np.empty((bh.shape[0], D), dtype=np.float64)
+        delta = np.empty((bh.shape[0],), dtype=np.float64)
+        rc = self._lib.oracle_attn_bwd_rows(_ptr(q), _ptr(k), _ptr(v), _ptr(do), B * H, Nq, Nk, D,
+                                            int(bool(causal)), float(scale), _ptr(bh), _ptr(ri), bh.shape[0],
+                                            _ptr(dq), _ptr(delta), int(nthreads))
+        if rc != 0:
+            raise RuntimeError("oracle_attn_bwd_rows failed (bad index?)")
+        return dq, delta
+
+    def attn_bwd_keys(self, q, k, v, do, causal: bool, scale: float, bh: int, key_idx, nthreads: int = 0):
+        """dK and dV rows [R, D] for the keys key_idx[r] of slice bh (b * H + h) only."""
+        q, k, v, do = _bits(q), _bits(k), _bits(v), _bits(do)
+        B, H, Nq, Nk, D = self._shapes(q, k, v)
+        kj = np.ascontiguousarray(key_idx, dtype=np.int64)
+        if kj.ndim != 1 or do.shape != q.shape:
+            raise ValueError("key_idx 1-D; do shaped like q")
+        dk = np.empty((kj.shape[0], D), dtype=np.float64)
+        dv = np.empty((kj.shape[0], D), dtype=np.float64)
+        rc = self._lib.oracle_attn_bwd_keys(_ptr(q), _ptr(k), _ptr(v), _ptr(do), B * H, Nq, Nk, D,
+                                            int(bool(causal)), float(scale), int(bh), _ptr(kj), kj.shape[0],
+                                            _ptr(dk), _ptr(dv), int(nthreads))
+        if rc != 0:
+            raise RuntimeError("oracle_attn_bwd_keys failed (bad index?)")
+        return dk, dv
+
     cls.attn_bwd = attn_bwd
     cls.attn_bwd_f64 = attn_bwd_f64
+    cls.attn_bwd_rows = attn_bwd_rows
+    cls.attn_bwd_keys = attn_bwd_keys
     return cls
 
 
@@ -180,6 +221,14 @@ _bwd_methods(Oracle)
 
 def attn_bwd(q, k, v, do, causal: bool, scale: float, nthreads: int = 0):
     return default().attn_bwd(q, k, v, do, causal, scale, nthreads)
+
+
+def attn_bwd_rows(q, k, v, do, causal: bool, scale: float, bh_idx, row_idx, nthreads: int = 0):
+    return default().attn_bwd_rows(q, k, v, do, causal, scale, bh_idx, row_idx, nthreads)
+
+
+def attn_bwd_keys(q, k, v, do, causal: bool, scale: float, bh: int, key_idx, nthreads: int = 0):
+    return default().attn_bwd_keys(q, k, v, do, causal, scale, bh, key_idx, nthreads)
 
 
 def default() -> Oracle:

@@ -178,3 +178,209 @@ int oracle_attn_bwd(const uint16_t *q, const uint16_t *k, const uint16_t *v, con
     free(vd);
     return rc;
 }
+
+/* ------------------------------------------------------------------------
+ * Sampled outputs of the same backward, for problems too large for the full
+ * computation (each value is computed on its own, by the formulas above).
+ */
+
+/* Row statistics of query row i of one slice: visible keys n_vis, max m,
+ * sum l (of exp(s - m)); s, scratch of Nk doubles, receives the scores. */
+static int64_t row_scores(const double *qi, const double *kb, int64_t i, int64_t Nq, int64_t Nk, int64_t D,
+                          int causal, double scale, double *s, double *m_out, double *l_out) {
+    int64_t n_vis = Nk, j, d;
+    if (causal) {
+        n_vis = i + (Nk - Nq) + 1;
+        if (n_vis > Nk) n_vis = Nk;
+        if (n_vis < 0) n_vis = 0;
+    }
+    double m = -INFINITY, l = 0.0;
+    for (j = 0; j < n_vis; ++j) {
+        double a = 0.0;
+        for (d = 0; d < D; ++d) a += qi[d] * kb[j * D + d];
+        s[j] = scale * a;
+        if (s[j] > m) m = s[j];
+    }
+    for (j = 0; j < n_vis; ++j) l += exp(s[j] - m);
+    *m_out = m;
+    *l_out = l;
+    return n_vis;
+}
+
+static void widen_slice(const uint16_t *src, double *dst, int64_t n) {
+    for (int64_t x = 0; x < n; ++x) dst[x] = widen_bf16_b(src[x]);
+}
+
+/* dQ and D for the rows (bh_idx[r], row_idx[r]): dq_out [R*D], delta_out [R].
+ * Inputs as oracle_attn_bwd (bf16 bit patterns, [BH, N, D]). */
+int oracle_attn_bwd_rows(const uint16_t *q, const uint16_t *k, const uint16_t *v, const uint16_t *dout,
+                         int64_t BH, int64_t Nq, int64_t Nk, int64_t D, int causal, double scale,
+                         const int64_t *bh_idx, const int64_t *row_idx, int64_t R, double *dq_out,
+                         double *delta_out, int nthreads) {
+    if (!q || !k || !v || !dout || !bh_idx || !row_idx || !dq_out || !delta_out) return -1;
+    if (BH < 1 || Nq < 1 || Nk < 1 || D < 1 || R < 0) return -1;
+    for (int64_t r = 0; r < R; ++r)
+        if (bh_idx[r] < 0 || bh_idx[r] >= BH || row_idx[r] < 0 || row_idx[r] >= Nq) return -1;
+    int failed = 0;
+    const int nt = nthreads_or_all(nthreads);
+    (void)nt;
+#pragma omp parallel num_threads(nt) reduction(| : failed)
+    {
+        double *s = (double *)malloc(sizeof(double) * (size_t)Nk);
+        double *qi = (double *)malloc(sizeof(double) * (size_t)D);
+        double *doi = (double *)malloc(sizeof(double) * (size_t)D);
+        double *kj = (double *)malloc(sizeof(double) * (size_t)D);
+        double *vj = (double *)malloc(sizeof(double) * (size_t)D);
+        if (!s || !qi || !doi || !kj || !vj) {
+            failed = 1;
+        } else {
+            int64_t r;
+#pragma omp for schedule(dynamic, 1)
+            for (r = 0; r < R; ++r) {
+                const int64_t bh = bh_idx[r], i = row_idx[r];
+                widen_slice(q + (bh * Nq + i) * D, qi, D);
+                widen_slice(dout + (bh * Nq + i) * D, doi, D);
+                const uint16_t *kb = k + bh * Nk * D, *vb = v + bh * Nk * D;
+                double *dqr = dq_out + r * D;
+                int64_t j, d;
+                for (d = 0; d < D; ++d) dqr[d] = 0.0;
+                int64_t n_vis = Nk;
+                if (causal) {
+                    n_vis = i + (Nk - Nq) + 1;
+                    if (n_vis > Nk) n_vis = Nk;
+                    if (n_vis < 0) n_vis = 0;
+                }
+                if (n_vis == 0) {
+                    delta_out[r] = 0.0;
+                    continue;
+                }
+                double m = -INFINITY, l = 0.0;
+                for (j = 0; j < n_vis; ++j) {
+                    widen_slice(kb + j * D, kj, D);
+                    double a = 0.0;
+                    for (d = 0; d < D; ++d) a += qi[d] * kj[d];
+                    s[j] = scale * a;
+                    if (s[j] > m) m = s[j];
+                }
+                for (j = 0; j < n_vis; ++j) l += exp(s[j] - m);
+                /* D_i = sum_j p_ij dp_ij, then dq_i = scale sum_j p_ij (dp_ij - D_i) k_j */
+                double dl = 0.0;
+                for (j = 0; j < n_vis; ++j) {
+                    widen_slice(vb + j * D, vj, D);
+                    double a = 0.0;
+                    for (d = 0; d < D; ++d) a += doi[d] * vj[d];
+                    const double p = exp(s[j] - m) / l;
+                    dl += p * a;
+                    s[j] = a;  /* keep dp_ij; p is recomputed below from the stored max */
+                }
+                delta_out[r] = dl;
+                /* second pass: recompute the scores for p (s now holds dp) */
+                for (j = 0; j < n_vis; ++j) {
+                    widen_slice(kb + j * D, kj, D);
+                    double a = 0.0;
+                    for (d = 0; d < D; ++d) a += qi[d] * kj[d];
+                    const double p = exp(scale * a - m) / l;
+                    const double ds = p * (s[j] - dl);
+                    for (d = 0; d < D; ++d) dqr[d] += scale * ds * kj[d];
+                }
+            }
+        }
+        free(s);
+        free(qi);
+        free(doi);
+        free(kj);
+        free(vj);
+    }
+    return failed ? -1 : 0;
+}
+
+/* dK and dV for the keys key_idx[r] of slice bh: dk_out, dv_out [R*D].  The
+ * slice's per-row max, sum and D are computed once (the whole slice's scores),
+ * then each key's gradients from all the queries that see it. */
+int oracle_attn_bwd_keys(const uint16_t *q, const uint16_t *k, const uint16_t *v, const uint16_t *dout,
+                         int64_t BH, int64_t Nq, int64_t Nk, int64_t D, int causal, double scale, int64_t bh,
+                         const int64_t *key_idx, int64_t R, double *dk_out, double *dv_out, int nthreads) {
+    if (!q || !k || !v || !dout || !key_idx || !dk_out || !dv_out) return -1;
+    if (BH < 1 || Nq < 1 || Nk < 1 || D < 1 || R < 0 || bh < 0 || bh >= BH) return -1;
+    for (int64_t r = 0; r < R; ++r)
+        if (key_idx[r] < 0 || key_idx[r] >= Nk) return -1;
+    double *qd = (double *)malloc(sizeof(double) * (size_t)(Nq * D));
+    double *dod = (double *)malloc(sizeof(double) * (size_t)(Nq * D));
+    double *kd = (double *)malloc(sizeof(double) * (size_t)(Nk * D));
+    double *vd = (double *)malloc(sizeof(double) * (size_t)(Nk * D));
+    double *mrow = (double *)malloc(sizeof(double) * (size_t)Nq);
+    double *lrow = (double *)malloc(sizeof(double) * (size_t)Nq);
+    double *drow = (double *)malloc(sizeof(double) * (size_t)Nq);
+    int failed = !qd || !dod || !kd || !vd || !mrow || !lrow || !drow;
+    const int nt = nthreads_or_all(nthreads);
+    (void)nt;
+    if (!failed) {
+        widen_slice(q + bh * Nq * D, qd, Nq * D);
+        widen_slice(dout + bh * Nq * D, dod, Nq * D);
+        widen_slice(k + bh * Nk * D, kd, Nk * D);
+        widen_slice(v + bh * Nk * D, vd, Nk * D);
+#pragma omp parallel num_threads(nt) reduction(| : failed)
+        {
+            double *s = (double *)malloc(sizeof(double) * (size_t)Nk);
+            if (!s) {
+                failed = 1;
+            } else {
+                int64_t i;
+#pragma omp for schedule(dynamic, 16)
+                for (i = 0; i < Nq; ++i) {
+                    double m, l;
+                    const int64_t n_vis = row_scores(qd + i * D, kd, i, Nq, Nk, D, causal, scale, s, &m, &l);
+                    mrow[i] = m;
+                    lrow[i] = l;
+                    double dl = 0.0;
+                    for (int64_t j = 0; j < n_vis; ++j) {
+                        double a = 0.0;
+                        for (int64_t d = 0; d < D; ++d) a += dod[i * D + d] * vd[j * D + d];
+                        dl += exp(s[j] - m) / l * a;
+                    }
+                    drow[i] = dl;
+                }
+            }
+            free(s);
+        }
+    }
+    if (!failed) {
+        int64_t r;
+#pragma omp parallel for num_threads(nt) schedule(dynamic, 1)
+        for (r = 0; r < R; ++r) {
+            const int64_t j = key_idx[r];
+            double *dkr = dk_out + r * D, *dvr = dv_out + r * D;
+            for (int64_t d = 0; d < D; ++d) {
+                dkr[d] = 0.0;
+                dvr[d] = 0.0;
+            }
+            /* queries that see key j: all, or i >= j - (Nk - Nq) when causal */
+            int64_t i0 = 0;
+            if (causal) {
+                i0 = j - (Nk - Nq);
+                if (i0 < 0) i0 = 0;
+            }
+            for (int64_t i = i0; i < Nq; ++i) {
+                double a = 0.0, b = 0.0;
+                for (int64_t d = 0; d < D; ++d) {
+                    a += qd[i * D + d] * kd[j * D + d];
+                    b += dod[i * D + d] * vd[j * D + d];
+                }
+                const double p = exp(scale * a - mrow[i]) / lrow[i];
+                const double ds = p * (b - drow[i]);
+                for (int64_t d = 0; d < D; ++d) {
+                    dvr[d] += p * dod[i * D + d];
+                    dkr[d] += scale * ds * qd[i * D + d];
+                }
+            }
+        }
+    }
+    free(qd);
+    free(dod);
+    free(kd);
+    free(vd);
+    free(mrow);
+    free(lrow);
+    free(drow);
+    return failed ? -1 : 0;
+}

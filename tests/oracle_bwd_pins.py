@@ -5,7 +5,9 @@
 * closed forms and invariants of the softmax chain rule: identical keys give
   dQ = 0; the key gradients of a head sum to zero (softmax is unchanged when
   every key moves by the same vector); D_i equals dO_i . O_i; with dO = 1 the
-  value gradient of key j is the column sum of P.
+  value gradient of key j is the column sum of P;
+* the sampled functions (dQ of chosen rows, dK and dV of chosen keys, used at
+  sizes the full backward cannot reach) agree with the pinned full backward.
 """
 from __future__ import annotations
 
@@ -100,6 +102,28 @@ def check_bwd_unit_upstream_gives_column_sums(orc):
         _close(g["dv"], np.broadcast_to(p.sum(axis=2)[..., None], g["dv"].shape), TIGHT, "dO = 1: dV = column sums of P")
 
 
+def check_bwd_sampled_outputs_match_full(orc):
+    """The sampled functions (dQ rows; dK, dV of chosen keys) against the full,
+    pinned backward, square and rectangular, causal or not, ragged tiles."""
+    rng = np.random.default_rng(17)
+    for (B, H, Nq, Nk, D, causal) in ((1, 2, 70, 70, 16, True), (2, 1, 33, 90, 8, True), (1, 2, 50, 40, 12, False)):
+        q = make_qkv(B, H, Nq, D, seed=80 + Nq)[0]
+        _, k, v = make_qkv(B, H, Nk, D, seed=81 + Nk)
+        do = make_qkv(B, H, Nq, D, seed=82)[1]
+        scale = 0.4
+        full = orc.attn_bwd(q, k, v, do, causal, scale)
+        bh = rng.integers(0, B * H, 40)
+        ri = rng.integers(0, Nq, 40)
+        dq, delta = orc.attn_bwd_rows(q, k, v, do, causal, scale, bh, ri)
+        _close(dq, full["dq"].reshape(B * H, Nq, D)[bh, ri], TIGHT, "sampled dQ rows")
+        _close(delta, full["delta"].reshape(B * H, Nq)[bh, ri], TIGHT, "sampled D")
+        for h in range(B * H):
+            kj = rng.integers(0, Nk, 25)
+            dk, dv = orc.attn_bwd_keys(q, k, v, do, causal, scale, h, kj)
+            _close(dk, full["dk"].reshape(B * H, Nk, D)[h, kj], TIGHT, "sampled dK")
+            _close(dv, full["dv"].reshape(B * H, Nk, D)[h, kj], TIGHT, "sampled dV")
+
+
 ALL_BWD_CHECKS = [
     check_bwd_finite_differences,
     check_bwd_matches_torch_autograd,
@@ -107,4 +131,5 @@ ALL_BWD_CHECKS = [
     check_bwd_key_gradients_sum_to_zero,
     check_bwd_delta_is_do_dot_o,
     check_bwd_unit_upstream_gives_column_sums,
+    check_bwd_sampled_outputs_match_full,
 ]

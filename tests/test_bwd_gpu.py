@@ -114,3 +114,57 @@ def test_backward_argument_errors():
 def test_backward_padded_head_dims(D, causal):
     got, ref = grads(1, 3, 300, 300, D, causal, seed=1700 + D)
     assert_grads_close(got, ref, f"D={D} causal={causal}")
+
+
+def sample_idx(n_bh, n, n_random, seed):
+    """Random (head, index) pairs plus the first and last 64 indices of the first and last head."""
+    rng = np.random.default_rng(seed)
+    bh = [rng.integers(0, n_bh, n_random)]
+    ix = [rng.integers(0, n, n_random)]
+    for h in (0, n_bh - 1):
+        for i0 in (0, max(0, n - 64)):
+            m = min(64, n)
+            bh.append(np.full(m, h))
+            ix.append(np.arange(i0, i0 + m))
+    return np.concatenate(bh).astype(np.int64), np.concatenate(ix).astype(np.int64)
+
+
+def assert_sample_close(g, r, what):
+    assert np.all(np.isfinite(g)), f"{what}: unwritten or non-finite entries"
+    err = np.abs(g - r)
+    mx = err.max() / max(np.abs(r).max(), 1e-2)
+    mean = err.mean() / max(np.abs(r).mean(), 1e-2)
+    assert mx <= MAX_REL and mean <= MEAN_REL, f"{what}: max/max={mx:.2e} mean/mean={mean:.2e}"
+
+
+@pytest.mark.parametrize("name,key_heads", [("b4h16n4096d128", 2), ("b1h16n16384d128_causal_q4", 1),
+                                            ("b8h16nq512nk8192d128_causal", 2)])
+def test_backward_full_size_sampled(name, key_heads):
+    """The bench's backward workloads at full size, in its launch configuration: dQ and D of sampled
+    query rows, dK and dV of sampled keys of the last head (and the first: one head's softmax
+    statistics cost the oracle O(Nq Nk D), so N = 16384 checks one head)."""
+    from tiled_attention_forward_fa2_gb300.inputs import WORKLOADS, normal_bf16_bits
+    w = WORKLOADS[name]
+    q, k, v = w.qkv()
+    do = normal_bf16_bits(q.size, w.seed + 7, 3).reshape(q.shape)  # seeded upstream gradient
+    B, H, Nq, D, Nk = w.B, w.H, w.N, w.D, w.n_keys
+    qd, kd, vd, dod = to_dev(q), to_dev(k), to_dev(v), to_dev(do)
+    o, lse = pkg.fwd(qd, kd, vd, causal=w.causal, scale=w.scale)
+    s = torch.cuda.current_stream()
+    dq, dk, dv = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
+    delta = torch.empty((B, H, Nq), device="cuda")
+    st = pkg.attn_bwd_qk(qd, kd, vd, o, lse, dod, dq, dk, dv, delta, B, H, Nq, Nk, D, w.causal, w.scale, s)
+    assert st == pkg.ATTN_OK and pkg.attn_last_status(s) == pkg.ATTN_OK
+    bh, ri = sample_idx(B * H, Nq, 256, w.seed)
+    dq_ref, delta_ref = oracle.attn_bwd_rows(q, k, v, do, w.causal, w.scale, bh, ri)
+    g = dq.float().cpu().numpy().astype(np.float64).reshape(B * H, Nq, D)
+    assert_sample_close(g[bh, ri], dq_ref, f"{name} dQ rows")
+    assert_sample_close(delta.cpu().numpy().astype(np.float64).reshape(B * H, Nq)[bh, ri], delta_ref, f"{name} D")
+    gk = dk.float().cpu().numpy().astype(np.float64).reshape(B * H, Nk, D)
+    gv = dv.float().cpu().numpy().astype(np.float64).reshape(B * H, Nk, D)
+    rng = np.random.default_rng(w.seed + 1)
+    for h in (B * H - 1, 0)[:key_heads]:
+        kj = np.concatenate([rng.integers(0, Nk, 96), np.arange(64), np.arange(Nk - 64, Nk)]).astype(np.int64)
+        dk_ref, dv_ref = oracle.attn_bwd_keys(q, k, v, do, w.causal, w.scale, h, kj)
+        assert_sample_close(gk[h, kj], dk_ref, f"{name} dK of head {h}")
+        assert_sample_close(gv[h, kj], dv_ref, f"{name} dV of head {h}")
