@@ -322,3 +322,21 @@ def test_wide_head_dims_large_logits_and_many_tiles():
         o_ref, lse_ref = oracle.attn_rows(q, k, v, causal, 1.0 / 16, bh, ri)
         assert_close(o.reshape(4, 2048, 256)[bh, ri], lse.reshape(4, 2048)[bh, ri], o_ref, lse_ref,
                      f"D=256 N=2048 q_std=4 causal={causal}")
+
+
+def test_key_cache_workload_sampled():
+    """b8h16nq512nk8192d128_causal at full size (attn_fwd_qk, the bench's launch): sampled rows vs the oracle."""
+    w = WORKLOADS["b8h16nq512nk8192d128_causal"]
+    q, k, v = w.qkv()
+    qd, kd, vd = to_dev(q), to_dev(k), to_dev(v)
+    o = torch.full_like(qd, float("nan"))
+    lse = torch.full((w.B, w.H, w.N), float("nan"), dtype=torch.float32, device="cuda")
+    s = torch.cuda.current_stream()
+    st = pkg.attn_fwd_qk(qd, kd, vd, o, lse, w.B, w.H, w.N, w.n_keys, w.D, w.causal, w.scale, s)
+    assert st == pkg.ATTN_OK and pkg.attn_last_status(s) == pkg.ATTN_OK
+    of, lf = o_to_f64(o), lse.cpu().numpy().astype(np.float64)
+    assert np.all(np.isfinite(of)) and np.all(np.isfinite(lf)), "unwritten or non-finite output"
+    bh, ri = sampled_rows(w.B * w.H, w.N, 1024, w.seed)
+    o_ref, lse_ref = oracle.attn_rows(q, k, v, w.causal, w.scale, bh, ri)
+    assert_close(of.reshape(w.B * w.H, w.N, w.D)[bh, ri], lf.reshape(w.B * w.H, w.N)[bh, ri], o_ref, lse_ref,
+                 "b8h16nq512nk8192d128_causal")
