@@ -32,11 +32,12 @@
 //                  thread per row (= TMEM lane).  Masks, running max in base 2,
 //                  p = 2^(s*scale*log2e - m) with packed fp32x2 math, P -> TMEM,
 //                  running sum.  The reference max m only moves when a row's max
-//                  grows by more than 2^8; rescale factors go to TMEM for the
-//                  correction warps; 1/l goes to shared memory; LSE to global.
-//   warpgroup 2  : (warps 8..11) correction: O_i *= alpha in TMEM between PV
-//                  steps (skipped when no row of the warp moved its max);
-//                  epilogue O_i / l -> bf16 -> swizzled staging tile -> TMA store.
+//                  grows by more than 2^8; then the same warp rescales its rows
+//                  of O_i in TMEM before handing P over (the last P V on O_i has
+//                  finished by then), so no other role takes part in a key step.
+//                  1/l goes to shared memory; LSE to global.
+//   warpgroup 2  : (warps 8..11) epilogue: O_i / l -> bf16 -> swizzled staging
+//                  tile -> TMA store.
 // Every barrier wait is bounded: on expiry the kernel records a timeout in a
 // device status word, the other roles see a shared abort flag, in-flight TMA
 // copies and MMAs are drained, TMEM is freed and the CTA returns.
@@ -52,16 +53,17 @@ namespace attn {
 constexpr int BM = 128;                     // query rows per tile (= TMEM lanes)
 constexpr int BN = 128;                     // keys per tile
 constexpr int kThreads = 512;               // 4 warpgroups
-constexpr int kCorrWarp0 = 8;               // warps 8..11: correction / epilogue
+constexpr int kCorrWarp0 = 8;               // warps 8..11: epilogue
 constexpr int kLoadWarp = 12;
 constexpr int kMmaWarp = 13;                // warps 14, 15 idle (complete the warpgroup)
 constexpr uint32_t kSubTile = 128u * 128u;  // 128 rows x 64 bf16 (one 128-B swizzle span)
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleLog2 = 8.0f;        // move the reference max only when it grows by > 2^8
 constexpr int kStatusTimeout = 4;           // value of ATTN_ERR_TIMEOUT
-// Register split (setmaxnreg): 2 x 128 softmax threads at 168, 128 correction
+// Register split (setmaxnreg): 2 x 128 softmax threads at 168, 128 epilogue
 // threads at 96, 128 load/MMA/idle threads at 80 = 65536 = 512 threads x 128
-// (each the smallest count at which its role compiles without spills).
+// (measured best; 176 / 80 / 80 is as fast on long rows and slower on the
+// bench shape).
 constexpr uint32_t kRegSoftmax = 168, kRegCorr = 96, kRegOther = 80;
 static_assert(2 * 128 * kRegSoftmax + 128 * kRegCorr + 128 * kRegOther == kThreads * 128, "register split");
 
@@ -109,24 +111,18 @@ struct Cfg {
   static constexpr int B_QE = 2 * NQB;           // [2 NQB] last S MMA on the buffer finished (MMA commit)
   static constexpr int B_FULL = 4 * NQB, B_EMPTY = 4 * NQB + NSLOT;
   static constexpr int B_SF = 4 * NQB + 2 * NSLOT;  // [2] scores of tile i ready (MMA commit)
-  static constexpr int B_PF = B_SF + 2;          // [2] P of tile i in TMEM (128 softmax threads)
-  static constexpr int B_AR = B_PF + 2;          // [2] per-step rescale factor in TMEM (128 softmax threads)
-  static constexpr int B_OR = B_AR + 2;          // [2] O of tile i rescaled (128 correction threads)
-  static constexpr int B_OF = B_OR + 2;          // [2] O_i += P_i V_j finished (MMA commit)
-  // [2] final 1/l in shared memory (128 softmax threads).  Kept apart from
-  // B_AR: the final hand-off follows the last step's factor without waiting
-  // for the correction warps, so on one barrier it could run two phases ahead.
-  static constexpr int B_FIN = B_OF + 2;
-  static constexpr int B_OE = B_FIN + 2;         // [2] epilogue has read O_i and 1/l (128 correction threads)
+  static constexpr int B_PF = B_SF + 2;          // [2] P of tile i in TMEM, O_i rescaled (128 softmax threads)
+  static constexpr int B_OF = B_PF + 2;          // [2] O_i += P_i V_j finished (MMA commit)
+  static constexpr int B_FIN = B_OF + 2;         // [2] final 1/l in shared memory (128 softmax threads)
+  static constexpr int B_OE = B_FIN + 2;         // [2] epilogue has read O_i and 1/l (128 epilogue threads)
   static constexpr int B_DONE = B_OE + 2;
   static constexpr int NBAR = B_DONE + 1;
   static_assert(NBAR * 8 <= 512, "barrier area");
   // TMEM columns
   static constexpr uint32_t COL_S = 0;     // S_i at COL_S + 128 i (P_i over its first 64 columns)
   static constexpr uint32_t COL_O = 256;   // O_i at COL_O + D i
-  static constexpr uint32_t COL_ALPHA = 64;  // inside S_i, above P_i
   __host__ __device__ static constexpr bool count128(int b) {  // barriers completed by 128 thread arrivals
-    return (b >= B_PF && b < B_OR + 2) || (b >= B_FIN && b < B_OE + 2);
+    return (b >= B_PF && b < B_PF + 2) || (b >= B_FIN && b < B_OE + 2);
   }
 };
 
@@ -268,8 +264,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_sm103(const __grid_const
 
   // Phase bookkeeping.  Every role walks the same units; per query tile i it
   // counts the units that used tile i (phases of B_Q, B_QE, B_FIN, B_OE) and
-  // their key steps (B_SF, B_PF, B_OF).  Each unit has one rescale step fewer
-  // than key steps (j >= 1: B_AR, B_OR), so those number steps - units.
+  // their key steps (B_SF, B_PF, B_OF).
   if (warp >= kLoadWarp) {
     sm103::regs_decrease<kRegOther>();
     if (warp == kLoadWarp) {
@@ -339,8 +334,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_sm103(const __grid_const
       auto wait_full = [&](int c) { return warp_wait(bar(C::B_FULL + c % NSLOT), uint32_t(c / NSLOT) & 1u, ab); };
       auto release = [&](int c) { sm103::mma_commit_warp(bar(C::B_EMPTY + c % NSLOT)); };
       // nu0/nu1: units tile 0/1 had (B_Q / B_QE buffer and phase, B_OE); ph bits
-      // 2/3 = parity of their key steps (B_PF), 4/5 = parity of their rescale
-      // steps (B_OR).
+      // 2/3 = parity of their key steps (B_PF).
       uint32_t cb = 0;  // ring index of the current unit's K_0
       uint32_t ph = 0;
       int nu0 = 0, nu1 = 0;
@@ -367,9 +361,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_sm103(const __grid_const
         };
         auto issue_pv = [&](int i, int j) -> bool {
           if (!warp_wait(bar(C::B_PF + i), ((ph >> (2 + i)) ^ uint32_t(j)) & 1u, ab)) return false;
-          if (j > 0) {
-            if (!warp_wait(bar(C::B_OR + i), ((ph >> (4 + i)) ^ uint32_t(j - 1)) & 1u, ab)) return false;
-          } else if ((i == 0 ? nu0 : nu1) > 0) {
+          if (j == 0 && (i == 0 ? nu0 : nu1) > 0) {
             // The first P V of a unit overwrites O_i: the previous unit's epilogue must have read it.
             if (!warp_wait(bar(C::B_OE + i), uint32_t((i == 0 ? nu0 : nu1) - 1) & 1u, ab)) return false;
           }
@@ -410,11 +402,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_sm103(const __grid_const
           if (next) release(int(cb) + 2 * j + 2);
         }
         cb += 2u * uint32_t(nk);
-        // Tile i: units +1, steps + nk_i, rescale steps + nk_i - 1.
-        ph ^= (uint32_t(nk0 & 1) << 2) | (uint32_t((nk0 - 1) & 1) << 4);
+        // Tile i: units +1, steps + nk_i.
+        ph ^= uint32_t(nk0 & 1) << 2;
         ++nu0;
         if (nk1 > 0) {
-          ph ^= (uint32_t(nk1 & 1) << 3) | (uint32_t((nk1 - 1) & 1) << 5);
+          ph ^= uint32_t(nk1 & 1) << 3;
           ++nu1;
         }
       }
@@ -486,11 +478,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_sm103(const __grid_const
             alpha = sm103::ex2_approx(m_ref - cand);
             m_ref = cand;
           }
-          // Hand alpha to the correction warps now, so O is rescaled while the exps run.
-          sm103::tmem_st1(tS + C::COL_ALPHA, __float_as_uint(alpha));
-          sm103::tmem_st_wait();
-          sm103::tc_fence_before();
-          sm103::mbar_arrive(bar(C::B_AR + i));
         }
         const uint64_t negm = sm103::f2_pack(-m_ref, -m_ref);
         uint64_t acc0 = 0, acc1 = 0;  // packed fp32 partial sums (+0.0f, +0.0f)
@@ -517,6 +504,20 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_sm103(const __grid_const
         sm103::f2_unpack(acc1, a2, a3);
         const float rowsum = (a0 + a1) + (a2 + a3);
         l_run = j == 0 ? rowsum : fmaf(alpha, l_run, rowsum);
+        // O_i *= alpha when a row of the warp moved its reference max (rare after
+        // the first steps).  The P V that last wrote O_i was issued before this
+        // step's S MMAs, so it has finished; the next one waits for B_PF below.
+        if (__any_sync(0xffffffffu, alpha != 1.f)) {
+          const uint32_t tO = tmem + lane_off + C::COL_O + uint32_t(i) * D;
+#pragma unroll 1
+          for (int q = 0; q < D / 32; ++q) {
+            uint32_t v[32];
+            sm103::tmem_ld32(tO + q * 32, v);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
+            sm103::tmem_st32(tO + q * 32, v);
+          }
+        }
         sm103::tmem_st_wait();
         sm103::tc_fence_before();
         sm103::mbar_arrive(bar(C::B_PF + i));
@@ -534,42 +535,15 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_sm103(const __grid_const
       ph = ((ph ^ uint32_t(nki)) & 1u) | ((ph ^ 2u) & 2u) | 4u;
     }
   } else {
-    // ------------------------------------------------- correction, epilogue
+    // -------------------------------------------------------------- epilogue
     sm103::regs_decrease<kRegCorr>();
     const int r = threadIdx.x & 127;
     const uint32_t lane_off = uint32_t((warp & 3) * 32) << 16;
-    int nu0 = 0, nu1 = 0, ns0 = 0, ns1 = 0;  // as in the MMA warp
+    int nu0 = 0, nu1 = 0, ns0 = 0, ns1 = 0;  // units and key steps of tile 0 / 1 so far (B_FIN, B_OE; B_OF)
     bool ok = true;
     for (int k = 0; k < kRounds && more(k); ++k) {
       const Unit u = unit_of<CAUSAL>(p, work(k));
-      const int nk = u.nk();
-      for (int j = 1; ok && j < nk; ++j) {
-#pragma unroll 1
-        for (int i = 0; i < 2; ++i) {
-          if (j >= (i == 0 ? u.nk0 : u.nk1)) continue;
-          const uint32_t tS = tmem + lane_off + C::COL_S + uint32_t(i) * BN;
-          const uint32_t tO = tmem + lane_off + C::COL_O + uint32_t(i) * D;
-          if (!(ok = warp_wait(bar(C::B_AR + i), uint32_t((i == 0 ? ns0 - nu0 : ns1 - nu1) + j - 1) & 1u, ab))) break;
-          sm103::tc_fence_after();
-          const float alpha = __uint_as_float(sm103::tmem_ld1(tS + C::COL_ALPHA));
-          if (!(ok = warp_wait(bar(C::B_OF + i), uint32_t((i == 0 ? ns0 : ns1) + j - 1) & 1u, ab))) break;
-          sm103::tc_fence_after();
-          if (__any_sync(0xffffffffu, alpha != 1.f)) {
-#pragma unroll
-            for (int q = 0; q < D / 32; ++q) {
-              uint32_t v[32];
-              sm103::tmem_ld32(tO + q * 32, v);
-#pragma unroll
-              for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
-              sm103::tmem_st32(tO + q * 32, v);
-            }
-            sm103::tmem_st_wait();
-          }
-          sm103::tc_fence_before();
-          sm103::mbar_arrive(bar(C::B_OR + i));
-        }
-      }
-      // Epilogue.  The four warps agree (reduction barrier) before touching the
+      // The four warps agree (reduction barrier) before touching the
       // shared staging tile, so a warp that gave up on a wait cannot leave the
       // others stuck at the named barrier below.  Tile 0 is in every unit, so the
       // warps meet at least once per unit.
