@@ -154,14 +154,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dq_sm103(const __grid
       return warp_wait(bar(C::B_FULL + slot(j, kv)), uint32_t(j / (kv == 0 ? NK : NV)) & 1u, ab);
     };
     auto release = [&](int j, int kv) { sm103::mma_commit_warp(bar(C::B_EMPTY + slot(j, kv))); };
-    auto issue_s_dp = [&](int j) {  // S = Q K_j^T (buffer j & 1), dP = dO V_j^T
-      const uint64_t dk = dkv_k + slot_off(j, 0), dv = dkv_k + slot_off(j, 1);
+    auto issue_s = [&](int j) {  // S = Q K_j^T into buffer j & 1
+      const uint64_t dk = dkv_k + slot_off(j, 0);
       const uint32_t dS = tmem + C::COL_S + uint32_t(j & 1) * BN;
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint64_t off = uint64_t((uint32_t(kk >> 2) * kSubTile + uint32_t(kk & 3) * 32u) >> 4);
         sm103::mma_ss_warp(dS, dq_k + off, dk + off, kIdescS, kk > 0 ? 1u : 0u);
       }
+    };
+    auto issue_dp = [&](int j) {  // dP = dO V_j^T; S_j and dP_j ready together
+      const uint64_t dv = dkv_k + slot_off(j, 1);
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint64_t off = uint64_t((uint32_t(kk >> 2) * kSubTile + uint32_t(kk & 3) * 32u) >> 4);
@@ -173,16 +176,22 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dq_sm103(const __grid
     bool ok = warp_wait(bar(C::B_Q), 0u, ab) && wait_full(0, 0) && wait_full(0, 1);
     if (ok) {
       sm103::tc_fence_after();
-      issue_s_dp(0);
+      issue_s(0);
+      issue_dp(0);
     }
     for (int j = 0; ok && j < nk; ++j) {
       if (j + 1 < nk) {
-        // S_{j+1} goes to the other buffer (its dS_{j-1} was read by the dQ MMA
-        // issued before); dP_{j+1} once dP_j has left TMEM.
-        if (!(ok = wait_full(j + 1, 0) && wait_full(j + 1, 1))) break;
+        // S_{j+1} goes to the other buffer as soon as K_{j+1} is in (its dS_{j-1}
+        // was read by the dQ MMA issued before, and the elementwise warps had
+        // finished with it), so it runs while they work on step j; dP_{j+1} once
+        // dP_j has left TMEM.
+        if (!(ok = wait_full(j + 1, 0))) break;
+        sm103::tc_fence_after();
+        issue_s(j + 1);
+        if (!(ok = wait_full(j + 1, 1))) break;
         if (!(ok = warp_wait(bar(C::B_DPR), uint32_t(j) & 1u, ab))) break;
         sm103::tc_fence_after();
-        issue_s_dp(j + 1);
+        issue_dp(j + 1);
       }
       if (!(ok = warp_wait(bar(C::B_DSF + (j & 1)), uint32_t(j >> 1) & 1u, ab))) break;
       sm103::tc_fence_after();
