@@ -1,20 +1,24 @@
-"""CPU oracle for the attention forward -- TEST INFRASTRUCTURE ONLY.
+"""CPU oracles for the attention forward and the Based linear-attention forward
+-- TEST INFRASTRUCTURE ONLY.
 
 Only the tests, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
 ``bench.py`` may import this package.  The product path (the CUDA library and
 its Python binding) never imports, links or calls it, and it shares no code
-with that path: its arithmetic lives in ``attn_oracle.c`` (plain C, fp64),
-which is built with gcc into ``oracle/lib/liboracle_attn.so``.
+with that path: its arithmetic lives in ``attn_oracle.c``, ``attn_oracle_bwd.c``
+and ``based_oracle.c`` (plain C, fp64), built with gcc into
+``oracle/lib/liboracle_attn.so``.
 
 Every function takes Q as ``uint16`` bf16 bit patterns shaped [B, H, Nq, D] and
 K, V shaped [B, H, Nk, D] (Nk = Nq for self-attention; the layout of the C
 ABI) and returns float64 results.  Causal masking is aligned at the
 bottom-right corner: key j is visible to query i iff j <= i + Nk - Nq.
 
-Pins for every function here live in ``tests/oracle_pins.py`` (closed forms,
-invariants, an independent tiled online-softmax restatement, a library
-routine and a 50-digit brute force).  The one part left unpinned is the GPU's
-own fp32/bf16 rounding, which nothing fixes beyond the stated tolerance.
+Pins for every function here live in ``tests/oracle_pins.py``,
+``tests/oracle_bwd_pins.py`` and ``tests/oracle_based_pins.py`` (closed forms,
+invariants, independent restatements -- the tiled online softmax, the linear
+attention recurrence over an explicit Taylor feature map -- a library routine
+and exact or 50-digit brute force).  The one part left unpinned is the GPU's
+own fp32/bf16 rounding, which nothing fixes beyond the stated tolerances.
 """
 from __future__ import annotations
 
@@ -28,6 +32,8 @@ import numpy as np
 _HERE = os.path.dirname(os.path.abspath(__file__))
 SOURCE = os.path.join(_HERE, "attn_oracle.c")
 SOURCE_BWD = os.path.join(_HERE, "attn_oracle_bwd.c")
+SOURCE_BASED = os.path.join(_HERE, "based_oracle.c")
+SOURCES = [SOURCE, SOURCE_BWD, SOURCE_BASED]
 _LIBDIR = os.path.join(_HERE, "lib")
 _LIB = os.path.join(_LIBDIR, "liboracle_attn.so")
 _lock = threading.Lock()
@@ -50,10 +56,9 @@ def compile_source(src, out: str) -> str:
 
 def build(force: bool = False) -> str:
     """Build ``oracle/lib/liboracle_attn.so`` if it is missing or stale; returns its path."""
-    if not force and os.path.exists(_LIB) and all(os.path.getmtime(_LIB) >= os.path.getmtime(f)
-                                                  for f in (SOURCE, SOURCE_BWD)):
+    if not force and os.path.exists(_LIB) and all(os.path.getmtime(_LIB) >= os.path.getmtime(f) for f in SOURCES):
         return _LIB
-    return compile_source([SOURCE, SOURCE_BWD], _LIB)
+    return compile_source(SOURCES, _LIB)
 
 
 def _bits(a: np.ndarray) -> np.ndarray:
@@ -92,8 +97,50 @@ class Oracle:
                                                  P, P, I]
             lib.oracle_attn_bwd_rows.restype = I
             lib.oracle_attn_bwd_keys.restype = I
+        self.has_based = hasattr(lib, "oracle_based_fwd")
+        if self.has_based:
+            lib.oracle_based_fwd.argtypes = [P, P, P, P, P, I64, I64, I64, I64, ctypes.c_double, I]
+            lib.oracle_based_rows.argtypes = [P, P, P, I64, I64, I64, I64, ctypes.c_double, P, P, I64, P, P, I]
+            lib.oracle_based_fwd.restype = I
+            lib.oracle_based_rows.restype = I
         self._lib = lib
         self.path = libpath
+
+    @staticmethod
+    def _based_shapes(q, k, v):
+        if not (q.shape == k.shape and q.shape[:3] == v.shape[:3]):
+            raise ValueError("q, k [B,H,N,F] and v [B,H,N,D] expected")
+        B, H, N, F = q.shape
+        return B, H, N, F, v.shape[3]
+
+    def based_fwd(self, q, k, v, scale: float, nthreads: int = 0):
+        """Based linear attention (causal, second-order Taylor kernel) by its plain
+        definition: (Y [B,H,N,D] float64, Z [B,H,N] float64)."""
+        q, k, v = _bits(q), _bits(k), _bits(v)
+        B, H, N, F, D = self._based_shapes(q, k, v)
+        y = np.empty((B, H, N, D), dtype=np.float64)
+        z = np.empty((B, H, N), dtype=np.float64)
+        rc = self._lib.oracle_based_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(y), _ptr(z), B * H, N, F, D, float(scale),
+                                        int(nthreads))
+        if rc != 0:
+            raise RuntimeError("oracle_based_fwd failed")
+        return y, z
+
+    def based_rows(self, q, k, v, scale: float, bh_idx, row_idx, nthreads: int = 0):
+        """Y and Z for the rows (bh_idx[r], row_idx[r]) only: shapes [R, D] and [R]."""
+        q, k, v = _bits(q), _bits(k), _bits(v)
+        B, H, N, F, D = self._based_shapes(q, k, v)
+        bh = np.ascontiguousarray(bh_idx, dtype=np.int64)
+        ri = np.ascontiguousarray(row_idx, dtype=np.int64)
+        if bh.shape != ri.shape or bh.ndim != 1:
+            raise ValueError("bh_idx and row_idx must be 1-D and of one length")
+        y = np.empty((bh.shape[0], D), dtype=np.float64)
+        z = np.empty((bh.shape[0],), dtype=np.float64)
+        rc = self._lib.oracle_based_rows(_ptr(q), _ptr(k), _ptr(v), B * H, N, F, D, float(scale), _ptr(bh), _ptr(ri),
+                                         bh.shape[0], _ptr(y), _ptr(z), int(nthreads))
+        if rc != 0:
+            raise RuntimeError("oracle_based_rows failed (bad index?)")
+        return y, z
 
     def threads(self, nthreads: int = 0) -> int:
         """OpenMP threads a call with ``nthreads`` uses (0 means all available)."""
@@ -254,3 +301,11 @@ def attn_rows(q, k, v, causal: bool, scale: float, bh_idx, row_idx, nthreads: in
 
 def attn_probs(q, k, v, causal: bool, scale: float):
     return default().attn_probs(q, k, v, causal, scale)
+
+
+def based_fwd(q, k, v, scale: float, nthreads: int = 0):
+    return default().based_fwd(q, k, v, scale, nthreads)
+
+
+def based_rows(q, k, v, scale: float, bh_idx, row_idx, nthreads: int = 0):
+    return default().based_rows(q, k, v, scale, bh_idx, row_idx, nthreads)
