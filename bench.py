@@ -174,38 +174,80 @@ def to_dev(bits, device):
     return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(device)
 
 
-def cpu_oracle_rate(w, budget_s: float, rows_cap: int | None = None, seed: int = 0):
-    """Time the CPU oracle on sampled rows of workload ``w`` for about ``budget_s`` seconds.
+def oracle_parity(w, o, lse, q, k, v):
+    """Run the CPU oracle on the whole workload: (cpu_baseline, parity) objects.
 
-    Returns (TFLOP/s, seconds, rows, threads).  Row (b, h, i) costs 4*n_i*D FLOPs
-    (n_i visible keys), the same convention as the GPU metric.
-    """
+    ``o``, ``lse`` are the device results of the timed workload (float64 copies).
+    Parity compares every element: max and mean |dO| (with where the max is)
+    and the LSE relative error |dLSE| / max(1e-2, |LSE|) (floored where a
+    relative error is ill-posed), against the stated bounds."""
     import oracle
 
-    q, k, v = w.qkv()
-    rng = np.random.default_rng(seed)
-
-    def sample(n):
-        bh = rng.integers(0, w.B * w.H, n).astype(np.int64)
-        ri = rng.integers(0, w.N, n).astype(np.int64)
-        return bh, ri
-
-    def flops(ri):
-        vis = np.minimum(ri + 1 + w.n_keys - w.N, w.n_keys) if w.causal else np.full(ri.shape, w.n_keys)
-        return float(4.0 * w.D * vis.sum())
-
-    bh, ri = sample(64)
     t0 = time.perf_counter()
-    oracle.attn_rows(q, k, v, w.causal, w.scale, bh, ri)
-    dt = max(time.perf_counter() - t0, 1e-6)
-    n = max(16, int(64 * budget_s / dt))
-    if rows_cap:
-        n = min(n, rows_cap)
-    bh, ri = sample(n)
-    t0 = time.perf_counter()
-    oracle.attn_rows(q, k, v, w.causal, w.scale, bh, ri)
-    dt = time.perf_counter() - t0
-    return flops(ri) / dt / 1e12, dt, n, oracle.threads()
+    o_ref, lse_ref = oracle.attn_fwd(q, k, v, w.causal, w.scale)
+    secs = time.perf_counter() - t0
+    cpu = {"value": w.flops / secs / 1e12, "unit": "TFLOP/s", "cores": oracle.threads(), "kind": "oracle",
+           "sample": f"the whole workload {w.name} (every query row, all visible keys), {secs:.1f} s wall"}
+    do = np.abs(o - o_ref)
+    at = np.unravel_index(int(np.argmax(do)), do.shape)
+    dl = np.abs(lse - lse_ref)
+    parity = {"against": "CPU oracle (fp64 two-pass softmax attention), every element",
+              "max_abs_dO": float(do.max()), "mean_abs_dO": float(do.mean()),
+              "max_at_bhnd": [int(x) for x in at], "O_ref_at_max": float(o_ref[at]),
+              "lse_err": float((dl / np.maximum(1e-2, np.abs(lse_ref))).max()), "lse_abs_max": float(dl.max()),
+              "bounds": {"max_abs_dO": 2e-2, "mean_abs_dO": 2e-3, "lse_err": 1e-3}}
+    parity["pass"] = bool(parity["max_abs_dO"] <= 2e-2 and parity["mean_abs_dO"] <= 2e-3 and parity["lse_err"] <= 1e-3)
+    return cpu, parity
+
+
+def time_backward(pkg, w, qd, kd, vd, o, lse, stream, dev, flush, scratch, steps, pg, world):
+    """Device-timed backward (attn_bwd_qk: dQ, dK, dV; 2.5x the forward FLOPs) on the
+    forward's own O and LSE with a seeded upstream gradient; same timing rules."""
+    import torch
+
+    from tiled_attention_forward_fa2_gb300.inputs import normal_bf16_bits
+
+    dod = to_dev(normal_bf16_bits(w.B * w.H * w.N * w.D, w.seed, 3).reshape(w.B, w.H, w.N, w.D), dev)
+    dq, dk, dv = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
+    delta = torch.empty_like(lse)
+
+    def step():
+        st = pkg.attn_bwd_qk(qd, kd, vd, o, lse, dod, dq, dk, dv, delta, w.B, w.H, w.N, w.n_keys, w.D, w.causal,
+                             w.scale, stream)
+        if st != pkg.ATTN_OK:
+            raise RuntimeError(pkg.attn_status_string(st))
+
+    for _ in range(3):
+        step()
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize(dev)
+    if flush:
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+        for i in range(steps):
+            scratch.fill_(float(i))
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        torch.cuda.synchronize(dev)
+        ms = sum(a.elapsed_time(b) for a, b in zip(starts, ends)) / steps
+    else:
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        ms = e0.elapsed_time(e1) / steps
+    st = pkg.attn_last_status(stream)
+    if st != pkg.ATTN_OK:
+        raise RuntimeError(pkg.attn_status_string(st))
+    ms = max_over_ranks(ms, pg, dev)
+    flops = pkg.attn_bwd_qk_flops(w.B, w.H, w.N, w.n_keys, w.D, w.causal)
+    return {"metric": "attention bwd TFLOP/s (dQ, dK, dV; 2.5x the forward FLOPs)", "value": job_tflops(flops, world, ms),
+            "unit": "TFLOP/s", "ms_per_step": ms, "steps": steps, "gpu_launches": 2 * steps,
+            "kernels": "attn_bwd_dq_sm103 + attn_bwd_dkdv_sm103"}
 
 
 def run_reference(args, w):
@@ -238,7 +280,7 @@ def run_reference(args, w):
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": workload_config(w),
+        "data": "synthetic", "config": workload_config(w, args.gpus),
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": oracle.threads(), "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -246,9 +288,19 @@ def run_reference(args, w):
     print(json.dumps(line), flush=True)
 
 
-def workload_config(w, extra=None):
+def needs_flush(w) -> bool:
+    """Working set (Q, K, V read, O written) below 2x L2: rewrite a 2x-L2 buffer between steps."""
+    return 2 * w.B * w.H * w.D * (2 * w.N + 2 * w.n_keys) < 2 * L2_BYTES
+
+
+def workload_config(w, world=1, extra=None):
+    """The line's ``config``: the same dict for both arms (ours and --impl reference)."""
+    in_bytes = 2 * w.B * w.H * w.D * (w.N + 2 * w.n_keys)
     cfg = {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "Nk": w.n_keys, "D": w.D, "causal": w.causal, "seed": w.seed,
-           "q_std": w.q_std, "scale": w.scale, "layout": "[B,H,N,D] bf16, D innermost"}
+           "q_std": w.q_std, "scale": w.scale, "layout": "[B,H,N,D] bf16, D innermost",
+           "l2": ("working set < 2x L2: 2x-L2 buffer rewritten between steps, each launch timed alone"
+                  if needs_flush(w) else f"inputs {in_bytes / 2**20:.0f} MiB > 129 MiB L2, no flush"),
+           "parallelism": f"independent replicas x{world}" if world > 1 else "single GPU"}
     if extra:
         cfg.update(extra)
     return cfg
@@ -277,7 +329,7 @@ def run_ours(args, w):
     lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
     in_bytes = q.nbytes + k.nbytes + v.nbytes
-    flush = in_bytes + o.numel() * 2 < 2 * L2_BYTES
+    flush = needs_flush(w)
     scratch = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev) if flush else None
 
     if args.backward:
@@ -356,7 +408,7 @@ def run_ours(args, w):
             line = {"metric": "attention bwd TFLOP/s (bf16, 1\u00d7GB300; 2.5x forward FLOPs)", "value": value,
                     "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
                     "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-                    "dtype": "bf16", "data": "synthetic", "config": workload_config(w, {"pass": "backward"}),
+                    "dtype": "bf16", "data": "synthetic", "config": workload_config(w, world, {"pass": "backward"}),
                     "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                                  "frac": achieved / peak, "traffic": None,
                                  "peak_source": f"bf16_tflops (burst) of {peak_src}",
@@ -398,12 +450,23 @@ def run_ours(args, w):
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
     e2e_ms = max_over_ranks(e2e_ms, pg, dev)
 
+    backward = None
+    if not args.no_backward and w.D <= 128:
+        backward = time_backward(pkg, w, qd, kd, vd, o, lse, stream, dev, flush, scratch, max(3, min(args.steps, 100)),
+                                 pg, world)
+    o_host = o.float().cpu().numpy().astype(np.float64) if rank == 0 else None
+    lse_host = lse.cpu().numpy().astype(np.float64) if rank == 0 else None
+
     if rank != 0:
         if pg:
             pg.destroy_process_group()
         return
 
     peaks, peak_src = measured_peaks()
+    if backward is not None:
+        bpeak = float(peaks["bf16_tflops"])
+        backward.update({"peak": bpeak, "frac": backward["value"] / bpeak,
+                         "peak_source": f"bf16_tflops (burst) of {peak_src}"})
     peak = float(peaks["bf16_tflops"])
     achieved = flops / (ms_per_step * 1e-3) / 1e12
     traffic = ncu_traffic(w.name)
@@ -425,11 +488,11 @@ def run_ours(args, w):
     persist = w.D <= 64 or ((w.n_keys + 127) // 128 <= 32 and w.D <= 128)
     dk = 64 if w.D <= 64 else (128 if w.D <= 128 else 256)
     roofline["kernel"] = f"attn_fwd_sm103<{dk},{str(w.causal).lower()},{'persistent' if persist else 'one unit per CTA'}>"
-    cpu = None
+    cpu, parity = None, None
     if not args.no_cpu_baseline:
-        tf, secs, rows, cores = cpu_oracle_rate(w, args.cpu_seconds)
-        cpu = {"value": tf, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-               "sample": f"{rows} random query rows (all visible keys each) of {w.name}, {secs:.1f} s wall"}
+        # The oracle on the whole workload: its wall time is the CPU baseline and
+        # its output the parity check of the timed run's own output (every row).
+        cpu, parity = oracle_parity(w, o_host, lse_host, q, k, v)
     line = {
         "metric": METRIC,
         "value": value,
@@ -444,10 +507,7 @@ def run_ours(args, w):
         "dtype": "bf16",
         "data": "synthetic",
         "pct_of_peak": 100.0 * achieved / peak,
-        "config": workload_config(w, {
-            "l2": ("working set < 2x L2: 2x-L2 buffer rewritten between steps, each launch timed alone"
-                   if flush else f"inputs {in_bytes / 2**20:.0f} MiB > 129 MiB L2, no flush"),
-            "parallelism": f"independent replicas x{world}" if world > 1 else "single GPU"}),
+        "config": workload_config(w, world),
         "roofline": roofline,
         "cpu_baseline": cpu,
         "e2e": {"value": job_tflops(flops, world, e2e_ms), "unit": "TFLOP/s",
@@ -456,6 +516,8 @@ def run_ours(args, w):
         "gpu_launches": args.steps,
         "clocks": sampler.summary() if sampler else None,
         "kernel_source": kernel_source_hash(),
+        "parity": parity,
+        "backward": backward,
     }
     print(json.dumps(line), flush=True)
     if pg:
@@ -469,8 +531,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)
-    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU-oracle baseline budget")
-    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true",
+                    help="skip the CPU oracle (no cpu_baseline and no parity object)")
+    ap.add_argument("--no-backward", action="store_true", help="leave the backward object out of the line")
     ap.add_argument("--backward", action="store_true",
                     help="time the backward (dQ, dK, dV; 2.5x the forward FLOPs) instead of the forward; device timing only")
     args = ap.parse_args()

@@ -158,12 +158,41 @@ attn_status_t attn_bwd_qk(const void* q, const void* k, const void* v, const voi
                           int causal, float scale, void* stream);
 
 /*
- * attn_last_status -- synchronise `stream`, then report and clear the device
- * status word of the current device: ATTN_OK, or ATTN_ERR_TIMEOUT if a kernel
- * gave up on a pipeline wait since the last call; ATTN_ERR_CUDA if the
- * synchronisation itself failed.
+ * attn_last_status -- report and clear the status word of the current device:
+ * ATTN_OK, or ATTN_ERR_TIMEOUT if some kernel of this library gave up on a
+ * pipeline wait since the word was last cleared; ATTN_ERR_CUDA if the status
+ * read or the synchronisation failed.
+ *
+ * The read is enqueued on `stream` (behind the work already there) as one
+ * atomic read-and-clear on the device, and the call then synchronises
+ * `stream`.  The word is device-wide, not per stream: a timeout of a kernel on
+ * any stream is reported once, to the first call that reads the word after the
+ * kernel recorded it, and is never lost when several streams or threads call
+ * this at the same time.
  */
 attn_status_t attn_last_status(void* stream);
+
+/*
+ * attn_set_tuning -- process-wide overrides of the launcher's own choices, for
+ * tuning and testing.  0 in an argument restores the automatic choice.
+ *
+ * unit              : query tiles (of 128 rows) per work unit: 1, or 2 (two
+ *                     tiles of one head sharing every K/V tile).  Head dims
+ *                     above 128 always run one tile per unit.
+ * grid              : 1 = one CTA per unit; 2 = persistent (one CTA per SM,
+ *                     each walking many units).  Head dims above 128 always
+ *                     run one CTA per unit.
+ * pipe_chunks       : 1..32, chunks of heads in attn_fwd_from_host.
+ * wait_limit_cycles : bound of every pipeline wait in SM cycles (default 2^32,
+ *                     about 2 s); a lower bound turns a stalled pipeline into
+ *                     ATTN_ERR_TIMEOUT sooner.
+ *
+ * An out-of-range value returns ATTN_ERR_INVALID_ARG and changes nothing.
+ * Calls that start after this returns use the new values; any thread may call it.
+ * The results of attn_fwd do not depend on these choices beyond fp32 rounding
+ * order (each setting is tested against the same oracle).
+ */
+attn_status_t attn_set_tuning(int unit, int grid, int pipe_chunks, int64_t wait_limit_cycles);
 
 /* attn_status_string -- static, human-readable name of a status code. */
 const char* attn_status_string(attn_status_t status);

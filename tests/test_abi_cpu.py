@@ -55,6 +55,39 @@ def test_bad_sizes_and_scale(lib):
     assert call(B=2**20, H=2**20) == pkg.ATTN_ERR_INVALID_ARG
 
 
+def test_unit_count_stays_in_int32(lib):
+    """B*H*query tiles near 2^31 would overflow the persistent grid's int32 unit
+    index (up to two grid sizes past the last unit): rejected up front.  The
+    buffers are placed 2^40 bytes apart so only the size check can object."""
+    T = 1 << 40
+    big = dict(q=A16, k=A16 + T, v=A16 + 2 * T, o=A16 + 3 * T, lse=A16 + 4 * T)
+    assert call(B=1, H=2**31 - 1, N=1, D=8, **big) == pkg.ATTN_ERR_INVALID_ARG
+    assert call(B=1, H=2**31 - 4096, N=1, D=8, **big) == pkg.ATTN_ERR_INVALID_ARG
+    assert call(B=2**15, H=2**15 - 1, N=129, D=8, **big) == pkg.ATTN_ERR_INVALID_ARG  # 2 tiles each
+
+
+def test_tuning_overrides_validate(lib):
+    assert pkg.attn_set_tuning(3, 0, 0, 0) == pkg.ATTN_ERR_INVALID_ARG
+    assert pkg.attn_set_tuning(0, 3, 0, 0) == pkg.ATTN_ERR_INVALID_ARG
+    assert pkg.attn_set_tuning(0, 0, 33, 0) == pkg.ATTN_ERR_INVALID_ARG
+    assert pkg.attn_set_tuning(0, 0, 0, -1) == pkg.ATTN_ERR_INVALID_ARG
+    assert pkg.attn_set_tuning(2, 1, 4, 1000) == pkg.ATTN_OK
+    assert pkg.attn_set_tuning() == pkg.ATTN_OK
+
+
+def test_test_hook_only_in_the_test_build(lib):
+    """The production library cannot drop its K/V loads; only the test build
+    (compiled with -DATTN_TEST_HOOKS) exports the hook that does."""
+    from tiled_attention_forward_fa2_gb300 import _binding
+    assert not hasattr(lib, "attn_test_withhold_kv")
+    tl = _binding.load(cuda_build.LIB_TEST)
+    assert hasattr(tl, "attn_test_withhold_kv")
+    for n in declared_functions():
+        assert hasattr(tl, n)
+    src = open(os.path.join(ROOT, "tiled_attention_forward_fa2_gb300", "csrc", "attn_fwd.cu")).read()
+    assert "getenv" not in src
+
+
 def test_unsupported_head_dims(lib):
     for d in (4, 12, 100, 260, 264, 512):
         assert call(D=d) == pkg.ATTN_ERR_UNSUPPORTED

@@ -23,6 +23,7 @@ from ._binding import (  # noqa: F401
     attn_fwd_qk,
     attn_fwd_qk_flops,
     attn_last_status,
+    attn_set_tuning,
     attn_status_string,
     library,
 )

@@ -21,36 +21,40 @@ _lock = threading.Lock()
 _lib = None
 
 
+def load(path: str) -> ctypes.CDLL:
+    """Load a build of the library at ``path`` and declare its C signatures."""
+    if not os.path.exists(path):
+        raise RuntimeError(f"CUDA library not built: {path} is missing (run __graft_entry__.build())")
+    lib = ctypes.CDLL(path)
+    P, I64, I = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+    sigs = {
+        "attn_fwd": ([P, P, P, P, P, I64, I64, I64, I64, I, ctypes.c_float, P], I),
+        "attn_last_status": ([P], I),
+        "attn_status_string": ([I], ctypes.c_char_p),
+        "attn_set_tuning": ([I, I, I, I64], I),
+        "attn_fwd_flops": ([I64, I64, I64, I64, I], ctypes.c_double),
+        "attn_fwd_qk": ([P, P, P, P, P, I64, I64, I64, I64, I64, I, ctypes.c_float, P], I),
+        "attn_fwd_qk_flops": ([I64, I64, I64, I64, I64, I], ctypes.c_double),
+        "attn_bwd": ([P] * 10 + [I64, I64, I64, I64, I, ctypes.c_float, P], I),
+        "attn_bwd_qk": ([P] * 10 + [I64, I64, I64, I64, I64, I, ctypes.c_float, P], I),
+        "attn_bwd_qk_flops": ([I64, I64, I64, I64, I64, I], ctypes.c_double),
+        "attn_fwd_from_host": ([P] * 10 + [I64, I64, I64, I64, I64, I, ctypes.c_float, P], I),
+        "attn_test_withhold_kv": ([I], I),  # test build only
+    }
+    for name, (args, res) in sigs.items():
+        if hasattr(lib, name):
+            fn = getattr(lib, name)
+            fn.argtypes = args
+            fn.restype = res
+    return lib
+
+
 def library() -> ctypes.CDLL:
-    """The loaded CUDA library (built by ``build()``); raises if it is missing."""
+    """The loaded production CUDA library (built by ``build()``); raises if it is missing."""
     global _lib
     with _lock:
         if _lib is None:
-            if not os.path.exists(LIB):
-                raise RuntimeError(f"CUDA library not built: {LIB} is missing (run __graft_entry__.build())")
-            lib = ctypes.CDLL(LIB)
-            P, I64 = ctypes.c_void_p, ctypes.c_int64
-            lib.attn_fwd.argtypes = [P, P, P, P, P, I64, I64, I64, I64, ctypes.c_int, ctypes.c_float, P]
-            lib.attn_fwd.restype = ctypes.c_int
-            lib.attn_last_status.argtypes = [P]
-            lib.attn_last_status.restype = ctypes.c_int
-            lib.attn_status_string.argtypes = [ctypes.c_int]
-            lib.attn_status_string.restype = ctypes.c_char_p
-            lib.attn_fwd_flops.argtypes = [I64, I64, I64, I64, ctypes.c_int]
-            lib.attn_fwd_flops.restype = ctypes.c_double
-            lib.attn_fwd_qk.argtypes = [P, P, P, P, P, I64, I64, I64, I64, I64, ctypes.c_int, ctypes.c_float, P]
-            lib.attn_fwd_qk.restype = ctypes.c_int
-            lib.attn_fwd_qk_flops.argtypes = [I64, I64, I64, I64, I64, ctypes.c_int]
-            lib.attn_fwd_qk_flops.restype = ctypes.c_double
-            lib.attn_bwd.argtypes = [P] * 10 + [I64, I64, I64, I64, ctypes.c_int, ctypes.c_float, P]
-            lib.attn_bwd.restype = ctypes.c_int
-            lib.attn_bwd_qk.argtypes = [P] * 10 + [I64, I64, I64, I64, I64, ctypes.c_int, ctypes.c_float, P]
-            lib.attn_bwd_qk.restype = ctypes.c_int
-            lib.attn_bwd_qk_flops.argtypes = [I64, I64, I64, I64, I64, ctypes.c_int]
-            lib.attn_bwd_qk_flops.restype = ctypes.c_double
-            lib.attn_fwd_from_host.argtypes = [P] * 10 + [I64, I64, I64, I64, I64, ctypes.c_int, ctypes.c_float, P]
-            lib.attn_fwd_from_host.restype = ctypes.c_int
-            _lib = lib
+            _lib = load(LIB)
     return _lib
 
 
@@ -77,6 +81,11 @@ def attn_last_status(stream) -> int:
 
 def attn_status_string(status: int) -> str:
     return library().attn_status_string(int(status)).decode()
+
+
+def attn_set_tuning(unit: int = 0, grid: int = 0, pipe_chunks: int = 0, wait_limit_cycles: int = 0) -> int:
+    """Call ``attn_set_tuning`` (process-wide overrides; all zero = automatic)."""
+    return library().attn_set_tuning(int(unit), int(grid), int(pipe_chunks), int(wait_limit_cycles))
 
 
 def attn_fwd_flops(B: int, H: int, N: int, D: int, causal: bool) -> float:

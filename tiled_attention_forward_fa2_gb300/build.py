@@ -17,6 +17,10 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIBDIR = os.path.join(PKG, "lib")
 LIB = os.path.join(LIBDIR, "libattn_fwd_gb300.so")
+# The same sources with -DATTN_TEST_HOOKS: adds attn_test_withhold_kv, which
+# makes the forward drop its K/V loads (to drive the timeout path).  Only the
+# failure-detection tests load it; the production library cannot do this.
+LIB_TEST = os.path.join(LIBDIR, "libattn_fwd_gb300_testhooks.so")
 SOURCES = [os.path.join(CSRC, "attn_fwd.cu")]  # includes the backward (one module, one status word)
 DEPS = SOURCES + [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith(".cuh")] + \
     [os.path.join(INCLUDE, f) for f in os.listdir(INCLUDE) if f.endswith(".h")]
@@ -30,27 +34,39 @@ def nvcc() -> str:
     return exe
 
 
-def stale() -> bool:
-    if not os.path.exists(LIB):
+def stale(lib: str) -> bool:
+    if not os.path.exists(lib):
         return True
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return any(os.path.getmtime(d) > t for d in DEPS)
 
 
+def _command(out: str, defines) -> list:
+    return [nvcc(), *ARCH, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-shared", "-I" + INCLUDE,
+            *defines, "-Xptxas", "-v", "-o", out, *SOURCES]
+
+
 def build(force: bool = False, verbose: bool = False) -> str:
-    """Compile the library if it is missing or older than its sources; returns its path."""
-    if not force and not stale():
-        return LIB
+    """Compile the production library and its test-hook variant (in parallel) if
+    missing or older than their sources; returns the production library's path."""
     os.makedirs(LIBDIR, exist_ok=True)
-    tmp = LIB + f".tmp{os.getpid()}"
-    cmd = [nvcc(), *ARCH, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-shared",
-           "-I" + INCLUDE, "-Xptxas", "-v", "-o", tmp, *SOURCES]
-    res = subprocess.run(cmd, capture_output=True, text=True)
-    if res.returncode != 0:
-        raise RuntimeError("nvcc failed:\n" + res.stdout + res.stderr)
-    if verbose:
-        print(res.stderr)
-    os.replace(tmp, LIB)
+    jobs = []
+    for lib, defines in ((LIB, []), (LIB_TEST, ["-DATTN_TEST_HOOKS"])):
+        if force or stale(lib):
+            tmp = lib + f".tmp{os.getpid()}"
+            proc = subprocess.Popen(_command(tmp, defines), stdout=subprocess.PIPE, stderr=subprocess.PIPE, text=True)
+            jobs.append((lib, tmp, proc))
+    errors = []
+    for lib, tmp, proc in jobs:
+        out, err = proc.communicate()
+        if proc.returncode != 0:
+            errors.append(f"nvcc failed for {os.path.basename(lib)}:\n{out}{err}")
+            continue
+        if verbose and lib == LIB:
+            print(err)
+        os.replace(tmp, lib)
+    if errors:
+        raise RuntimeError("\n".join(errors))
     return LIB
 
 

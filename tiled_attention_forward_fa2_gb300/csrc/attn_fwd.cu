@@ -7,11 +7,13 @@
 #include <atomic>
 #include <cmath>
 #include <cstdint>
-#include <cstdlib>
 #include <mutex>
 
 #include "attn.h"
 #include "attn_fwd_kernel.cuh"
+#ifdef ATTN_TEST_HOOKS
+#include "attn_test_hooks.h"
+#endif
 
 namespace {
 
@@ -105,12 +107,21 @@ bool ranges_overlap(const void* a, uint64_t na, const void* b, uint64_t nb) {
 // 128 (N = 16384) loses 6 %.
 constexpr int64_t kPersistMaxKeyTiles = 32;
 
+// Process-wide overrides set by attn_set_tuning (0 = the launcher's own choice).
+// Read once per call with relaxed loads: a call sees either the old or the new value.
+std::atomic<int> g_tune_unit{0};          // 1 or 2 query tiles per unit
+std::atomic<int> g_tune_grid{0};          // 1 one CTA per unit, 2 persistent
+std::atomic<int> g_tune_chunks{0};        // chunks of heads in attn_fwd_from_host
+constexpr int kPipeChunksMax = 32;        // chunks at most (events held per device)
+std::atomic<long long> g_tune_wait{0};    // bound of every pipeline wait (SM cycles)
+std::atomic<unsigned> g_status_slot{0};   // next result slot of attn_last_status
+#ifdef ATTN_TEST_HOOKS
+std::atomic<int> g_test_withhold_kv{0};   // test build only: issue no K/V loads
+#endif
+
 long long timeout_cycles() {
   // About two seconds at the GB300 clock; no legitimate wait comes near it.
-  // ATTN_WAIT_LIMIT_CYCLES (read at every call) lowers it, e.g. to test the
-  // timeout path.
-  const char* e = std::getenv("ATTN_WAIT_LIMIT_CYCLES");
-  const long long x = e ? std::atoll(e) : 0;
+  const long long x = g_tune_wait.load(std::memory_order_relaxed);
   return x > 0 ? x : (1LL << 32);
 }
 
@@ -145,7 +156,9 @@ attn_status_t launch_fwd(const void* q, const void* k, const void* v, void* o, f
   const int64_t BH = B * H;
   const int64_t n_qtiles = (Nq + attn::BM - 1) / attn::BM;
   const int64_t n_ktiles = (Nk + attn::BN - 1) / attn::BN;
-  if (BH > kI32 / n_qtiles) return ATTN_ERR_INVALID_ARG;  // grid size
+  // Units of work (at most one per query tile) and the persistent grid's unit
+  // index, which runs up to two grid sizes past the last unit, stay in int32.
+  if (BH > (kI32 - 4096) / n_qtiles) return ATTN_ERR_INVALID_ARG;
   const int64_t Nmax = Nq > Nk ? Nq : Nk;
   if (BH > (int64_t(1) << 62) / (Nmax * D * 2)) return ATTN_ERR_INVALID_ARG;  // byte sizes
   const uint64_t q_bytes = uint64_t(BH) * uint64_t(Nq) * uint64_t(D) * 2u;
@@ -176,15 +189,12 @@ attn_status_t launch_fwd(const void* q, const void* k, const void* v, void* o, f
   // SM cycles, against about 2500 for one tile alone (no partner to overlap
   // with).  Pick the tiling whose waves of CTAs finish first:
   //   waves(T=2) * 3100 <= waves(T=1) * 2500, i.e. about 5 * waves2 <= 4 * waves1.
-  // ATTN_TILES_PER_CTA=1|2 overrides the choice (testing and tuning).
+  // attn_set_tuning overrides the choice (testing and tuning).
   const int64_t sms = g_dev_sms[dev] > 0 ? g_dev_sms[dev] : 1;
   const int64_t waves2 = ((n_qtiles + 1) / 2 * BH + sms - 1) / sms;
   const int64_t waves1 = (n_qtiles * BH + sms - 1) / sms;
   int T = 5 * waves2 <= 4 * waves1 ? 2 : 1;
-  if (const char* e = std::getenv("ATTN_TILES_PER_CTA")) {
-    if (e[0] == '1' && e[1] == 0) T = 1;
-    if (e[0] == '2' && e[1] == 0) T = 2;
-  }
+  if (const int u = g_tune_unit.load(std::memory_order_relaxed)) T = u;
   if (D > 128) T = 1;  // the D = 256 kernel holds one query tile (TMEM)
   prm.lse = lse;
   prm.Nq = int(Nq);
@@ -197,11 +207,11 @@ attn_status_t launch_fwd(const void* q, const void* k, const void* v, void* o, f
   prm.n_units = int((n_qtiles + T - 1) / T);
   prm.scale_log2 = scale * 1.4426950408889634f;
   prm.timeout_cycles = timeout_cycles();
-  // Test hook for the timeout path: ATTN_TEST_WITHHOLD_KV=1 makes the kernel
-  // issue no K/V loads, so its pipeline waits run out and it reports
-  // ATTN_ERR_TIMEOUT (use with a lowered ATTN_WAIT_LIMIT_CYCLES).
-  const char* wh = std::getenv("ATTN_TEST_WITHHOLD_KV");
-  prm.withhold_kv = (wh && wh[0] == '1') ? 1 : 0;
+#ifdef ATTN_TEST_HOOKS
+  // Test build only: the kernel issues no K/V loads, so its pipeline waits run
+  // out and it reports ATTN_ERR_TIMEOUT (used with a lowered wait bound).
+  prm.withhold_kv = g_test_withhold_kv.load(std::memory_order_relaxed);
+#endif
 
   prm.n_work = int(int64_t(prm.n_units) * BH);
   // Causal order: longest first over all heads when the units' key ranges
@@ -220,14 +230,11 @@ attn_status_t launch_fwd(const void* q, const void* k, const void* v, void* o, f
   // unit) overlaps each unit's Q load and epilogue with the previous unit's
   // work.  Long ones: one CTA per unit, whose key loop runs faster (see the
   // kernel) and whose launch cost is small beside the unit.
-  // ATTN_PERSISTENT=0|1 forces the choice (testing and tuning).
+  // attn_set_tuning forces the choice (testing and tuning).
   // At D <= 64 a key step costs about half as much, so the persistent grid wins
   // at every length measured (N = 4096: +6 %, 16384: +2.5 %).
   bool persist = D <= 64 || n_ktiles <= kPersistMaxKeyTiles;
-  if (const char* e = std::getenv("ATTN_PERSISTENT")) {
-    if (e[0] == '0' && e[1] == 0) persist = false;
-    if (e[0] == '1' && e[1] == 0) persist = true;
-  }
+  if (const int g = g_tune_grid.load(std::memory_order_relaxed)) persist = g == 2;
   if (D > 128) persist = false;  // the D = 256 kernel stages O in its Q buffer
   const int64_t ctas = persist && prm.n_work > sms ? sms : prm.n_work;
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -259,15 +266,39 @@ attn_status_t attn_fwd_qk(const void* q, const void* k, const void* v, void* o, 
 }
 
 attn_status_t attn_last_status(void* stream) {
-  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return ATTN_ERR_CUDA;
+  // The status word is taken and cleared in one atomic exchange on the device,
+  // behind the work already on `stream`, so a timeout recorded concurrently by
+  // a kernel on another stream is never lost.  Each call uses its own result
+  // slot (round robin), so concurrent callers do not overwrite each other.
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int slot = int(g_status_slot.fetch_add(1, std::memory_order_relaxed) % unsigned(attn::kStatusSlots));
+  attn::status_take<<<1, 1, 0, st>>>(slot);
+  if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
   int word = 0;
-  if (cudaMemcpyFromSymbol(&word, attn::g_attn_status, sizeof(int)) != cudaSuccess) return ATTN_ERR_CUDA;
-  if (word != 0) {
-    const int zero = 0;
-    if (cudaMemcpyToSymbol(attn::g_attn_status, &zero, sizeof(int)) != cudaSuccess) return ATTN_ERR_CUDA;
-  }
+  if (cudaMemcpyFromSymbolAsync(&word, attn::g_status_taken, sizeof(int), size_t(slot) * sizeof(int),
+                                cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return ATTN_ERR_CUDA;
   return word == 0 ? ATTN_OK : ATTN_ERR_TIMEOUT;
 }
+
+attn_status_t attn_set_tuning(int unit, int grid, int pipe_chunks, int64_t wait_limit_cycles) {
+  if (unit < 0 || unit > 2 || grid < 0 || grid > 2 || pipe_chunks < 0 || pipe_chunks > kPipeChunksMax ||
+      wait_limit_cycles < 0)
+    return ATTN_ERR_INVALID_ARG;
+  g_tune_unit.store(unit, std::memory_order_relaxed);
+  g_tune_grid.store(grid, std::memory_order_relaxed);
+  g_tune_chunks.store(pipe_chunks, std::memory_order_relaxed);
+  g_tune_wait.store(wait_limit_cycles, std::memory_order_relaxed);
+  return ATTN_OK;
+}
+
+#ifdef ATTN_TEST_HOOKS
+attn_status_t attn_test_withhold_kv(int on) {
+  g_test_withhold_kv.store(on ? 1 : 0, std::memory_order_relaxed);
+  return ATTN_OK;
+}
+#endif
 
 const char* attn_status_string(attn_status_t status) {
   switch (status) {

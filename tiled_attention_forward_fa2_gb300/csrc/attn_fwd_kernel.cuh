@@ -81,7 +81,9 @@ struct FwdParams {
   int lpt;                     // causal: nonzero -> heaviest units first over all heads, else a head's units adjacent
   float scale_log2;            // scale * log2(e)
   long long timeout_cycles;
-  int withhold_kv;             // test hook: nonzero -> no K/V loads are issued, so the pipeline waits run out
+#ifdef ATTN_TEST_HOOKS
+  int withhold_kv;             // test build only: nonzero -> no K/V loads are issued, so the pipeline waits run out
+#endif
 };
 
 template <int D>
@@ -161,7 +163,13 @@ __device__ __forceinline__ Unit unit_of(const FwdParams& p, int w) {
   return u;
 }
 
-__device__ int g_attn_status;  // 0 or kStatusTimeout; read and cleared by the host
+__device__ int g_attn_status;  // 0 or kStatusTimeout; taken and cleared by status_take
+
+// attn_last_status's read of the status word: one atomic exchange (read and
+// clear), its result left in a slot of its own for the host to copy.
+constexpr int kStatusSlots = 64;
+__device__ int g_status_taken[kStatusSlots];
+__global__ void status_take(int slot) { g_status_taken[slot] = atomicExch(&g_attn_status, 0); }
 
 struct Abort {
   volatile uint32_t* flag;
@@ -300,7 +308,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_sm103(const __grid_const
             ++nq1;
           }
           const int nk = u.nk();
-          for (int j = 0; ok && !p.withhold_kv && j < nk; ++j) {
+#ifdef ATTN_TEST_HOOKS
+          const bool withhold = p.withhold_kv != 0;
+#else
+          constexpr bool withhold = false;
+#endif
+          for (int j = 0; ok && !withhold && j < nk; ++j) {
             for (int kv = 0; kv < 2; ++kv, ++c) {
               const int s = c % NSLOT;
               if (c >= NSLOT && !(ok = wait_bounded(bar(C::B_EMPTY + s), uint32_t(c / NSLOT - 1) & 1u, ab))) break;

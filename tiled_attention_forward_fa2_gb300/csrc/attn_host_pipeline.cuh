@@ -11,19 +11,16 @@
 
 namespace {
 
-constexpr int kPipeChunksMax = 32;  // events held per device
-
 // Chunks of heads per call.  A chunk's kernel lasts at least as long as its
 // longest unit (all key tiles of two query tiles: ~1.55 us per key tile at
 // D = 128, ~0.8 at D <= 64, measured on GB300), so more chunks only help while
 // each chunk's upload (~200 GB/s over the host link, measured both for the copy
 // engines and for SM loads) still takes longer than that; at most 8 (measured:
 // the bench shape, 32-key-tile units, is best at 8; causal N = 16384, 128-tile
-// units, at 4 -- 816 against 620 TFLOP/s end to end at 8).  ATTN_PIPE_CHUNKS=
-// 1..32 (read at every call) overrides the choice (tuning).
+// units, at 4 -- 816 against 620 TFLOP/s end to end at 8).  attn_set_tuning
+// overrides the choice (tuning).
 int pipe_chunks(uint64_t in_bytes, int64_t n_ktiles, int64_t D) {
-  const char* e = std::getenv("ATTN_PIPE_CHUNKS");
-  const int x = e ? std::atoi(e) : 0;
+  const int x = g_tune_chunks.load(std::memory_order_relaxed);
   if (x >= 1 && x <= kPipeChunksMax) return x;
   const double unit_us = double(n_ktiles) * (D <= 64 ? 0.8 : 1.55);
   const double upload_us = double(in_bytes) / 200e3;  // 200 GB/s = 200e3 bytes per us

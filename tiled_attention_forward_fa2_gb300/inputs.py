@@ -128,3 +128,47 @@ WORKLOADS = {
         Workload("b8h16nq512nk8192d128_causal", 8, 16, 512, 128, True, 1006, Nk=8192),
     ]
 }
+
+
+@dataclass(frozen=True)
+class BasedWorkload:
+    """One Based linear-attention problem: q, k [B, H, N, F], v [B, H, N, D], causal.
+
+    F is the feature dimension of q and k (16 in Based) and D the value head
+    dimension; scale = 1/sqrt(F).  Streams as for attention (Q = 0, K = 1, V = 2).
+    """
+    name: str
+    B: int
+    H: int
+    N: int
+    F: int
+    D: int
+    seed: int
+    q_std: float = 1.0
+
+    @property
+    def scale(self) -> float:
+        return float(np.float32(1.0 / np.sqrt(self.F)))
+
+    @property
+    def tokens(self) -> int:
+        return self.B * self.H * self.N
+
+    def qkv(self):
+        q = normal_bf16_bits(self.B * self.H * self.N * self.F, self.seed, STREAM_Q, self.q_std)
+        k = normal_bf16_bits(self.B * self.H * self.N * self.F, self.seed, STREAM_K, 1.0)
+        v = normal_bf16_bits(self.B * self.H * self.N * self.D, self.seed, STREAM_V, 1.0)
+        return (q.reshape(self.B, self.H, self.N, self.F), k.reshape(self.B, self.H, self.N, self.F),
+                v.reshape(self.B, self.H, self.N, self.D))
+
+
+# Based problem sizes: feature dimension 16 and value head dimension 64 (the
+# Based layer's shape); a small case with a ragged last chunk, and a long-
+# sequence throughput case (B*H = 256 sequences of 4096 tokens).
+BASED_WORKLOADS = {
+    w.name: w
+    for w in [
+        BasedWorkload("based_b1h2n300f16d64", 1, 2, 300, 16, 64, 2001),
+        BasedWorkload("based_b16h16n4096f16d64", 16, 16, 4096, 16, 64, 2002),
+    ]
+}
