@@ -33,13 +33,15 @@ import numpy as np
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-from tiled_attention_forward_fa2_gb300.inputs import WORKLOADS  # noqa: E402
+from tiled_attention_forward_fa2_gb300.inputs import BASED_WORKLOADS, WORKLOADS  # noqa: E402
 
 METRIC = "attention fwd TFLOP/s (bf16, 1×GB300) and % of dense BF16 tensor peak"
 DEFAULT_WORKLOAD = "b4h16n4096d128"
 L2_BYTES = 129 * 2**20
 FALLBACK_PEAK_TFLOPS = 1900.0
 KERNEL_SOURCES = ["tiled_attention_forward_fa2_gb300/csrc/attn_fwd_kernel.cuh",
+                  "tiled_attention_forward_fa2_gb300/csrc/based_fwd_kernel.cuh",
+                  "tiled_attention_forward_fa2_gb300/csrc/based_fwd_host.cuh",
                   "tiled_attention_forward_fa2_gb300/csrc/attn_bwd_kernel.cuh",
                   "tiled_attention_forward_fa2_gb300/csrc/attn_bwd_host.cuh",
                   "tiled_attention_forward_fa2_gb300/csrc/sm103_ptx.cuh",
@@ -250,12 +252,190 @@ def time_backward(pkg, w, qd, kd, vd, o, lse, stream, dev, flush, scratch, steps
             "kernels": "attn_bwd_dq_sm103 + attn_bwd_dkdv_sm103"}
 
 
+def based_config(w, world=1):
+    """The ``config`` of a Based line (the same dict for both arms)."""
+    return {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "F": w.F, "D": w.D, "causal": True, "seed": w.seed,
+            "q_std": w.q_std, "scale": w.scale, "layout": "q, k [B,H,N,F], v, y [B,H,N,D] bf16; z [B,H,N] fp32",
+            "l2": f"working set {based_bytes(w) / 2**20:.0f} MiB > 2x 129 MiB L2, no flush",
+            "parallelism": f"independent replicas x{world}" if world > 1 else "single GPU"}
+
+
+def based_bytes(w) -> float:
+    """Algorithmic HBM bytes of one Based forward: q, k, v read, y written (bf16), z written (fp32)."""
+    return float(w.B * w.H * w.N * (2 * 2 * w.F + 2 * 2 * w.D + 4))
+
+
+BASED_METRIC = "Based linear attention fwd TFLOP/s (linear-form FLOPs, bf16, 1×GB300) and HBM roofline"
+
+
+def run_reference_based(args, w):
+    import oracle
+
+    q, k, v = w.qkv()
+    rng = np.random.default_rng(1)
+    bh, ri = rng.integers(0, w.B * w.H, 32).astype(np.int64), rng.integers(0, w.N, 32).astype(np.int64)
+    t0 = time.perf_counter()
+    oracle.based_rows(q, k, v, w.scale, bh, ri)
+    per_row = max((time.perf_counter() - t0) / 32, 1e-7)
+    rows = int(max(8, min(8192, 60.0 / (args.steps + args.warmup) / per_row)))
+    bh = rng.integers(0, w.B * w.H, rows).astype(np.int64)
+    ri = rng.integers(0, w.N, rows).astype(np.int64)
+    # The oracle's work is quadratic; the value is reported in the metric's own
+    # units: linear-form FLOPs of the sampled rows (per token, as the GPU line counts).
+    fs = 1 + w.F + w.F * (w.F + 1) // 2
+    step_flops = 4.0 * fs * (w.D + 1) * rows
+    for _ in range(args.warmup):
+        oracle.based_rows(q, k, v, w.scale, bh, ri)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.based_rows(q, k, v, w.scale, bh, ri)
+    dt = time.perf_counter() - t0
+    value = step_flops * args.steps / dt / 1e12
+    line = {"impl": "reference", "metric": BASED_METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": based_config(w, args.gpus),
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": oracle.threads(), "kind": "oracle",
+                             "sample": f"{rows} sampled rows (all earlier tokens each) of {w.name} per step"},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_based(args, w):
+    """One JSON line for a Based workload: device-timed attn_based_fwd, e2e from pinned
+    host buffers, HBM roofline, the oracle on the whole workload (parity, cpu_baseline)."""
+    import torch
+
+    import tiled_attention_forward_fa2_gb300 as pkg
+
+    world, rank, local = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device (the product path has no CPU fallback)")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+    pkg.library()
+    q, k, v = w.qkv()
+    qd, kd, vd = to_dev(q, dev), to_dev(k, dev), to_dev(v, dev)
+    y = torch.empty_like(vd)
+    z = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        st = pkg.attn_based_fwd(qd, kd, vd, y, z, w.B, w.H, w.N, w.F, w.D, w.scale, stream)
+        if st != pkg.ATTN_OK:
+            raise RuntimeError(pkg.attn_status_string(st))
+
+    for _ in range(args.warmup):
+        step()
+    st = pkg.attn_last_status(stream)
+    if st != pkg.ATTN_OK:
+        raise RuntimeError(pkg.attn_status_string(st))
+    sampler = ClockSampler(local) if rank == 0 else None
+    if sampler:
+        sampler.wait_first()
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize(dev)
+    if sampler:
+        sampler.mark()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    if sampler:
+        sampler.mark()
+    if pg:
+        pg.barrier()
+    st = pkg.attn_last_status(stream)
+    if st != pkg.ATTN_OK:
+        raise RuntimeError(pkg.attn_status_string(st))
+    ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, pg, dev)
+    if sampler:
+        sampler.stop()
+
+    # End to end: pinned host q, k, v up, the kernel, y and z down, every step.
+    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).pin_memory()  # noqa: E731
+    qh, kh, vh = pin(q), pin(k), pin(v)
+    yh = torch.empty(y.shape, dtype=torch.bfloat16).pin_memory()
+    zh = torch.empty(z.shape, dtype=torch.float32).pin_memory()
+
+    def e2e_step():
+        qd.copy_(qh, non_blocking=True)
+        kd.copy_(kh, non_blocking=True)
+        vd.copy_(vh, non_blocking=True)
+        step()
+        yh.copy_(y, non_blocking=True)
+        zh.copy_(z, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    e2e_steps = max(3, min(args.steps, 20))
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, pg, dev)
+    y_host = y.float().cpu().numpy().astype(np.float64) if rank == 0 else None
+    z_host = z.cpu().numpy().astype(np.float64) if rank == 0 else None
+    if rank != 0:
+        if pg:
+            pg.destroy_process_group()
+        return
+    peaks, peak_src = measured_peaks()
+    flops = pkg.attn_based_fwd_flops(w.B, w.H, w.N, w.F, w.D)
+    alg = based_bytes(w)
+    gbs = alg / (ms * 1e-3) / 1e9
+    cpu, parity = None, None
+    if not args.no_cpu_baseline:
+        import oracle
+        t0 = time.perf_counter()
+        y_ref, z_ref = oracle.based_fwd(q, k, v, w.scale)
+        secs = time.perf_counter() - t0
+        fs = 1 + w.F + w.F * (w.F + 1) // 2
+        cpu = {"value": 4.0 * fs * (w.D + 1) * w.tokens / secs / 1e12, "unit": "TFLOP/s", "cores": oracle.threads(),
+               "kind": "oracle", "sample": f"the whole workload {w.name} (every row), {secs:.1f} s wall"}
+        dy = np.abs(y_host - y_ref)
+        zr = float((np.abs(z_host - z_ref) / z_ref).max())
+        parity = {"against": "CPU oracle (fp64 quadratic definition), every element", "max_abs_dy": float(dy.max()),
+                  "mean_abs_dy": float(dy.mean()), "z_rel_max": zr,
+                  "bounds": {"max_abs_dy": 2e-2, "mean_abs_dy": 1e-3, "z_rel": 2.0 ** -6}}
+        parity["pass"] = bool(dy.max() <= 2e-2 and dy.mean() <= 1e-3 and zr <= 2.0 ** -6)
+    line = {
+        "metric": BASED_METRIC, "value": job_tflops(flops, world, ms), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": based_config(w, world),
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": float(peaks["hbm_gbs"]), "unit": "GB/s",
+                     "frac": gbs / float(peaks["hbm_gbs"]), "traffic": None, "algorithmic_bytes": alg,
+                     "peak_source": f"hbm_gbs of {peak_src}", "kernel": "based_fwd_sm103"},
+        "cpu_baseline": cpu,
+        "e2e": {"value": job_tflops(flops, world, e2e_ms), "unit": "TFLOP/s",
+                "h2d_bytes_per_step": int(q.nbytes + k.nbytes + v.nbytes),
+                "d2h_bytes_per_step": int(y.numel() * 2 + z.numel() * 4), "ms_per_step": e2e_ms, "steps": e2e_steps},
+        "gpu_launches": args.steps, "clocks": sampler.summary() if sampler else None,
+        "kernel_source": kernel_source_hash(), "parity": parity,
+    }
+    print(json.dumps(line), flush=True)
+    if pg:
+        pg.destroy_process_group()
+
+
 def run_reference(args, w):
     world, rank, _ = dist_env()
     if rank != 0:
         return
     import oracle
 
+    if isinstance(w, type(next(iter(BASED_WORKLOADS.values())))):
+        return run_reference_based(args, w)
     q, k, v = w.qkv()
     rng = np.random.default_rng(1)
     # Per step: a fixed sample of rows sized so that warm-up + timed steps take about a minute.
@@ -530,7 +710,7 @@ def main():
     ap.add_argument("--steps", type=int, default=500)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)
+    ap.add_argument("--workload", choices=sorted(WORKLOADS) + sorted(BASED_WORKLOADS), default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true",
                     help="skip the CPU oracle (no cpu_baseline and no parity object)")
     ap.add_argument("--no-backward", action="store_true", help="leave the backward object out of the line")
@@ -539,9 +719,11 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
-    w = WORKLOADS[args.workload]
+    w = WORKLOADS.get(args.workload) or BASED_WORKLOADS[args.workload]
     if args.impl == "reference":
         run_reference(args, w)
+    elif args.workload in BASED_WORKLOADS:
+        run_based(args, w)
     else:
         run_ours(args, w)
 

@@ -176,9 +176,12 @@ attn_status_t attn_last_status(void* stream);
  * attn_set_tuning -- process-wide overrides of the launcher's own choices, for
  * tuning and testing.  0 in an argument restores the automatic choice.
  *
- * unit              : query tiles (of 128 rows) per work unit: 1, or 2 (two
- *                     tiles of one head sharing every K/V tile).  Head dims
- *                     above 128 always run one tile per unit.
+ * unit              : how query tiles form work units: 1 = one tile (of 128
+ *                     rows) per unit; 2 = two tiles of one head sharing every
+ *                     K/V tile; 3 = key split, one tile whose key tiles are
+ *                     shared out between the CTA's two softmax warpgroups and
+ *                     merged at the end (head dims up to 64; above, 3 means 1).
+ *                     Head dims above 128 always run one tile per unit.
  * grid              : 1 = one CTA per unit; 2 = persistent (one CTA per SM,
  *                     each walking many units).  Head dims above 128 always
  *                     run one CTA per unit.
@@ -216,6 +219,43 @@ double attn_fwd_qk_flops(int64_t B, int64_t H, int64_t Nq, int64_t Nk, int64_t D
  * attn_fwd_qk_flops (the kernels recompute S and dP once more).
  */
 double attn_bwd_qk_flops(int64_t B, int64_t H, int64_t Nq, int64_t Nk, int64_t D, int causal);
+
+/*
+ * attn_based_fwd -- enqueue the Based linear-attention forward on `stream`.
+ *
+ * The pages name this kernel ("GPU의 폭발적인 성능 향상", news.hada.io topic
+ * 14783, section "ThunderKittens": a Based linear-attention forward, 215
+ * TFLOP/s on an H100) without a formula; the definition is the published
+ * Based layer (Arora et al., 2024): causal linear attention with the
+ * second-order Taylor kernel of exp.  For every batch b, head h and row i:
+ *   s_ij = scale * sum_f Q[b,h,i,f] K[b,h,j,f]            (j <= i)
+ *   a_ij = 1 + s_ij + s_ij^2 / 2
+ *   Z[b,h,i] = sum_{j<=i} a_ij
+ *   Y[b,h,i,:] = sum_{j<=i} a_ij V[b,h,j,:] / Z[b,h,i]
+ * evaluated chunk by chunk (128 tokens) with a running state of the feature
+ * map phi(k) v^T; accumulation is fp32, the weights, features and state enter
+ * the tensor-core products in bf16, Y is rounded once to bf16, Z is fp32.
+ *
+ * q, k : device, bf16 [B, H, N, F] contiguous (F innermost), 16-byte aligned.
+ * v    : device, bf16 [B, H, N, D] contiguous, 16-byte aligned.
+ * y    : device, bf16 [B, H, N, D], written; z : device, fp32 [B, H, N], written.
+ *        Neither may overlap any input or the other.
+ * F    : feature dimension, 8 or 16 (others ATTN_ERR_UNSUPPORTED; Based uses 16).
+ * D    : value head dimension, a multiple of 8 up to 64 (others ATTN_ERR_UNSUPPORTED).
+ * N    : any length >= 1 (a ragged last chunk is zero padded); B, H or N = 0 is
+ *        an empty problem (ATTN_OK, nothing launched, pointers not examined).
+ * scale: finite and > 0 (usually 1/sqrt(F)).
+ * Ownership, asynchrony and errors as attn_fwd (timeouts through attn_last_status).
+ */
+attn_status_t attn_based_fwd(const void* q, const void* k, const void* v, void* y, float* z, int64_t B,
+                             int64_t H, int64_t N, int64_t F, int64_t D, float scale, void* stream);
+
+/*
+ * attn_based_fwd_flops -- FLOPs of the linear (running-state) form of one
+ * attn_based_fwd call: per token 4 * Fs * (D + 1) (state update and readout),
+ * Fs = 1 + F + F (F + 1) / 2 features of the symmetric Taylor map.
+ */
+double attn_based_fwd_flops(int64_t B, int64_t H, int64_t N, int64_t F, int64_t D);
 
 #ifdef __cplusplus
 }

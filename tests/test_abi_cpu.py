@@ -67,7 +67,9 @@ def test_unit_count_stays_in_int32(lib):
 
 
 def test_tuning_overrides_validate(lib):
-    assert pkg.attn_set_tuning(3, 0, 0, 0) == pkg.ATTN_ERR_INVALID_ARG
+    assert pkg.attn_set_tuning(4, 0, 0, 0) == pkg.ATTN_ERR_INVALID_ARG
+    assert pkg.attn_set_tuning(-1, 0, 0, 0) == pkg.ATTN_ERR_INVALID_ARG
+    assert pkg.attn_set_tuning(3, 0, 0, 0) == pkg.ATTN_OK
     assert pkg.attn_set_tuning(0, 3, 0, 0) == pkg.ATTN_ERR_INVALID_ARG
     assert pkg.attn_set_tuning(0, 0, 33, 0) == pkg.ATTN_ERR_INVALID_ARG
     assert pkg.attn_set_tuning(0, 0, 0, -1) == pkg.ATTN_ERR_INVALID_ARG
@@ -203,3 +205,39 @@ def test_from_host_validation(lib):
     if torch.cuda.is_available():
         pytest.skip("a GPU is present")
     assert call_host() == pkg.ATTN_ERR_CUDA  # valid request, no device: nothing enqueued
+
+
+def call_based(N=256, F=16, D=64, **kw):
+    a = dict(q=A16, k=A16 + 64 * MB, v=A16 + 128 * MB, y=A16 + 192 * MB, z=A16 + 256 * MB, B=1, H=2, scale=0.25)
+    a.update(kw)
+    return pkg.attn_based_fwd(a["q"], a["k"], a["v"], a["y"], a["z"], a["B"], a["H"], N, F, D, a["scale"], None)
+
+
+def test_based_validation(lib):
+    for kw in ("q", "k", "v", "y", "z"):
+        assert call_based(**{kw: None}) == pkg.ATTN_ERR_INVALID_ARG, kw
+    for F in (4, 12, 24, 32):
+        assert call_based(F=F) == pkg.ATTN_ERR_UNSUPPORTED
+    for D in (4, 100, 128):
+        assert call_based(D=D) == pkg.ATTN_ERR_UNSUPPORTED
+    assert call_based(scale=0.0) == pkg.ATTN_ERR_INVALID_ARG
+    assert call_based(scale=float("nan")) == pkg.ATTN_ERR_INVALID_ARG
+    assert call_based(N=-1) == pkg.ATTN_ERR_INVALID_ARG
+    assert call_based(N=0, q=None, k=None, v=None, y=None, z=None) == pkg.ATTN_OK
+    assert call_based(y=A16) == pkg.ATTN_ERR_INVALID_ARG                 # y over q
+    assert call_based(z=A16 + 192 * MB + 64) == pkg.ATTN_ERR_INVALID_ARG  # z inside y
+    assert call_based(q=A16 + 4) == pkg.ATTN_ERR_INVALID_ARG
+    assert call_based(z=A16 + 256 * MB + 2) == pkg.ATTN_ERR_INVALID_ARG
+
+
+def test_based_flops(lib):
+    # 1 + 16 + 136 = 153 features, 65 value columns, state update and readout.
+    assert pkg.attn_based_fwd_flops(2, 3, 100, 16, 64) == 4.0 * 153 * 65 * 600
+
+
+def test_based_no_gpu_means_cuda_error(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert call_based() == pkg.ATTN_ERR_CUDA
+    assert call_based(F=8, D=8) == pkg.ATTN_ERR_CUDA

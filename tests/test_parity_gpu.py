@@ -76,9 +76,11 @@ def test_full_size_every_row(name):
         del o, lse
 
 
-@pytest.fixture(params=[1, 2], ids=["one_tile_per_cta", "two_tiles_per_cta"])
+@pytest.fixture(params=[1, 2, 3], ids=["one_tile_per_cta", "two_tiles_per_cta", "key_split"])
 def tiles_per_cta(request):
-    """Force the launcher's choice of query tiles per CTA (normally picked from the grid size)."""
+    """Force the launcher's choice of work unit (normally picked from the grid size): one or
+    two query tiles, or one tile with its key tiles split over both softmax warpgroups
+    (D <= 64; at larger head dims the request runs as one tile per unit)."""
     tune(unit=request.param)
     yield request.param
     tune(unit=0)

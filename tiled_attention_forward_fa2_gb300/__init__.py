@@ -14,6 +14,8 @@ from ._binding import (  # noqa: F401
     ATTN_ERR_TIMEOUT,
     ATTN_ERR_UNSUPPORTED,
     ATTN_OK,
+    attn_based_fwd,
+    attn_based_fwd_flops,
     attn_bwd,
     attn_bwd_qk,
     attn_bwd_qk_flops,
@@ -126,3 +128,33 @@ def fwd_from_host(q, k, v, causal: bool = False, scale: float | None = None, out
     if st != ATTN_OK:
         raise AttnError(st)
     return out, lse
+
+
+def based_fwd(q, k, v, scale: float | None = None, out=None, z=None, stream=None):
+    """Based linear attention on contiguous bf16 CUDA tensors q, k [B, H, N, F], v [B, H, N, D].
+
+    Returns ``(y, z)``: y bf16 [B, H, N, D], z fp32 [B, H, N] (the normaliser).
+    ``scale`` defaults to 1/sqrt(F).  Runs on ``stream`` (default: torch's
+    current stream) without synchronising.
+    """
+    import torch
+
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if t.dtype != torch.bfloat16 or not t.is_cuda or t.dim() != 4 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous bf16 CUDA tensor")
+    if not (q.shape == k.shape and q.shape[:3] == v.shape[:3]):
+        raise ValueError("q, k must be [B, H, N, F] and v [B, H, N, D]")
+    B, H, N, F = q.shape
+    D = v.shape[3]
+    if scale is None:
+        scale = 1.0 / math.sqrt(F)
+    if out is None:
+        out = torch.empty_like(v)
+    if z is None:
+        z = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    st = attn_based_fwd(q, k, v, out, z, B, H, N, F, D, scale, stream)
+    if st != ATTN_OK:
+        raise AttnError(st)
+    return out, z

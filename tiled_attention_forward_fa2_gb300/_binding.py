@@ -39,6 +39,8 @@ def load(path: str) -> ctypes.CDLL:
         "attn_bwd_qk": ([P] * 10 + [I64, I64, I64, I64, I64, I, ctypes.c_float, P], I),
         "attn_bwd_qk_flops": ([I64, I64, I64, I64, I64, I], ctypes.c_double),
         "attn_fwd_from_host": ([P] * 10 + [I64, I64, I64, I64, I64, I, ctypes.c_float, P], I),
+        "attn_based_fwd": ([P, P, P, P, P, I64, I64, I64, I64, I64, ctypes.c_float, P], I),
+        "attn_based_fwd_flops": ([I64, I64, I64, I64, I64], ctypes.c_double),
         "attn_test_withhold_kv": ([I], I),  # test build only
     }
     for name, (args, res) in sigs.items():
@@ -133,3 +135,13 @@ def attn_fwd_from_host(q_host, k_host, v_host, o_host, lse_host, q, k, v, o, lse
     a = [_addr(x) for x in (q_host, k_host, v_host, o_host, lse_host, q, k, v, o, lse)]
     return library().attn_fwd_from_host(*a, int(B), int(H), int(Nq), int(Nk), int(D), int(bool(causal)),
                                         float(scale), _stream(stream))
+
+
+def attn_based_fwd(q, k, v, y, z, B: int, H: int, N: int, F: int, D: int, scale: float, stream) -> int:
+    """Call ``attn_based_fwd`` (Based linear attention; tensors or raw addresses)."""
+    a = [_addr(x) for x in (q, k, v, y, z)]
+    return library().attn_based_fwd(*a, int(B), int(H), int(N), int(F), int(D), float(scale), _stream(stream))
+
+
+def attn_based_fwd_flops(B: int, H: int, N: int, F: int, D: int) -> float:
+    return library().attn_based_fwd_flops(int(B), int(H), int(N), int(F), int(D))

@@ -61,6 +61,11 @@ cudaError_t opt_in_smem() {
   cudaError_t e = cudaFuncSetAttribute(attn::attn_fwd_sm103<D, CAUSAL, false>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, int(attn::Cfg<D>::SMEM));
   if (e != cudaSuccess) return e;
+  if constexpr (D == 64) {
+    e = cudaFuncSetAttribute(attn::attn_fwd_sm103<64, CAUSAL, true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             int(attn::Cfg<64>::SMEM));
+    if (e != cudaSuccess) return e;
+  }
   if constexpr (attn::Cfg<D>::STAGE_IN_Q) return cudaSuccess;  // one-unit grid only
   else
     return cudaFuncSetAttribute(attn::attn_fwd_sm103<D, CAUSAL, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -109,7 +114,7 @@ constexpr int64_t kPersistMaxKeyTiles = 32;
 
 // Process-wide overrides set by attn_set_tuning (0 = the launcher's own choice).
 // Read once per call with relaxed loads: a call sees either the old or the new value.
-std::atomic<int> g_tune_unit{0};          // 1 or 2 query tiles per unit
+std::atomic<int> g_tune_unit{0};          // 1 or 2 query tiles per unit, 3 key split
 std::atomic<int> g_tune_grid{0};          // 1 one CTA per unit, 2 persistent
 std::atomic<int> g_tune_chunks{0};        // chunks of heads in attn_fwd_from_host
 constexpr int kPipeChunksMax = 32;        // chunks at most (events held per device)
@@ -126,7 +131,14 @@ long long timeout_cycles() {
 }
 
 template <int D, bool CAUSAL>
-cudaError_t launch(const attn::FwdParams& prm, int64_t ctas, bool persist, cudaStream_t stream) {
+cudaError_t launch(const attn::FwdParams& prm, int64_t ctas, bool persist, bool split, cudaStream_t stream) {
+  if constexpr (D == 64) {
+    if (split) {  // the key-split kernel walks its units like the persistent one
+      attn::attn_fwd_sm103<64, CAUSAL, true, true><<<dim3(unsigned(ctas)), dim3(attn::kThreads), attn::Cfg<64>::SMEM,
+                                                     stream>>>(prm);
+      return cudaGetLastError();
+    }
+  }
   if constexpr (!attn::Cfg<D>::STAGE_IN_Q) {
     if (persist) {
       attn::attn_fwd_sm103<D, CAUSAL, true><<<dim3(unsigned(ctas)), dim3(attn::kThreads), attn::Cfg<D>::SMEM,
@@ -194,7 +206,18 @@ attn_status_t launch_fwd(const void* q, const void* k, const void* v, void* o, f
   const int64_t waves2 = ((n_qtiles + 1) / 2 * BH + sms - 1) / sms;
   const int64_t waves1 = (n_qtiles * BH + sms - 1) / sms;
   int T = 5 * waves2 <= 4 * waves1 ? 2 : 1;
-  if (const int u = g_tune_unit.load(std::memory_order_relaxed)) T = u;
+  // Key split (D <= 64): one query tile per unit, its key tiles shared out
+  // between the two softmax warpgroups.  It halves a unit's chain of key steps
+  // at the same tensor-core throughput per CTA as two tiles per unit, so it
+  // wins when the single-tile units fit in one wave of CTAs (then every CTA's
+  // time is one unit's chain; b2h8n1024d64: 128 tiles on 152 SMs).  Beyond a
+  // wave its extra per-unit cost (Q load, merge) loses to two tiles per unit.
+  bool split = D <= 64 && n_ktiles >= 2 && n_qtiles * BH <= sms;
+  if (const int u = g_tune_unit.load(std::memory_order_relaxed)) {
+    T = u == 3 ? 1 : u;
+    split = u == 3 && D <= 64;
+  }
+  if (split) T = 1;
   if (D > 128) T = 1;  // the D = 256 kernel holds one query tile (TMEM)
   prm.lse = lse;
   prm.Nq = int(Nq);
@@ -224,7 +247,14 @@ attn_status_t launch_fwd(const void* q, const void* k, const void* v, void* o, f
     const int64_t light_row = last_row_light < Nq - 1 ? last_row_light : Nq - 1;
     int64_t nk_light = (light_row + (Nk - Nq)) / attn::BN + 1;
     if (nk_light > n_ktiles) nk_light = n_ktiles;
-    prm.lpt = 4 * nk_light < 3 * n_ktiles ? 1 : 0;
+    if (4 * nk_light < 3 * n_ktiles) {
+      // Bands of heads whose K and V together take at most half of L2 (64 MB):
+      // over all 16 heads of causal N = 16384 (8 MB each) the longest-first
+      // order read 552 MB from HBM for 201 MB of K, V and Q.
+      const int64_t kv_head = 4 * Nk * D;
+      const int64_t band = (int64_t(64) << 20) / kv_head;
+      prm.lpt = int(band < 1 ? 1 : (band > BH ? BH : band));
+    }
   }
   // Short key ranges: a persistent grid (one CTA per SM taking every gridDim-th
   // unit) overlaps each unit's Q load and epilogue with the previous unit's
@@ -243,11 +273,11 @@ attn_status_t launch_fwd(const void* q, const void* k, const void* v, void* o, f
   // D, so TMA fills the missing columns with zeros on load (they add nothing to
   // Q K^T, and P V gives zeros there) and leaves them out on store.
   if (D <= 64)
-    err = causal ? launch<64, true>(prm, ctas, persist, st) : launch<64, false>(prm, ctas, persist, st);
+    err = causal ? launch<64, true>(prm, ctas, persist, split, st) : launch<64, false>(prm, ctas, persist, split, st);
   else if (D <= 128)
-    err = causal ? launch<128, true>(prm, ctas, persist, st) : launch<128, false>(prm, ctas, persist, st);
+    err = causal ? launch<128, true>(prm, ctas, persist, false, st) : launch<128, false>(prm, ctas, persist, false, st);
   else
-    err = causal ? launch<256, true>(prm, ctas, persist, st) : launch<256, false>(prm, ctas, persist, st);
+    err = causal ? launch<256, true>(prm, ctas, persist, false, st) : launch<256, false>(prm, ctas, persist, false, st);
   return err == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
@@ -283,7 +313,7 @@ attn_status_t attn_last_status(void* stream) {
 }
 
 attn_status_t attn_set_tuning(int unit, int grid, int pipe_chunks, int64_t wait_limit_cycles) {
-  if (unit < 0 || unit > 2 || grid < 0 || grid > 2 || pipe_chunks < 0 || pipe_chunks > kPipeChunksMax ||
+  if (unit < 0 || unit > 3 || grid < 0 || grid > 2 || pipe_chunks < 0 || pipe_chunks > kPipeChunksMax ||
       wait_limit_cycles < 0)
     return ATTN_ERR_INVALID_ARG;
   g_tune_unit.store(unit, std::memory_order_relaxed);
@@ -330,6 +360,7 @@ double attn_fwd_qk_flops(int64_t B, int64_t H, int64_t Nq, int64_t Nk, int64_t D
 }  // extern "C"
 #include "attn_bwd_host.cuh"
 #include "attn_host_pipeline.cuh"
+#include "based_fwd_host.cuh"
 
 extern "C" double attn_bwd_qk_flops(int64_t B, int64_t H, int64_t Nq, int64_t Nk, int64_t D, int causal) {
   return 2.5 * attn_fwd_qk_flops(B, H, Nq, Nk, D, causal);

@@ -78,7 +78,7 @@ struct FwdParams {
   int tiles_per_cta;           // T = 1 or 2 query tiles per unit
   int n_units;                 // ceil(n_qtiles / T): units per (batch, head)
   int n_work;                  // n_units * B*H: units of the whole problem
-  int lpt;                     // causal: nonzero -> heaviest units first over all heads, else a head's units adjacent
+  int lpt;                     // causal: heads per band, heaviest units first within each band (0: a head's units adjacent)
   float scale_log2;            // scale * log2(e)
   long long timeout_cycles;
 #ifdef ATTN_TEST_HOOKS
@@ -133,20 +133,37 @@ struct Cfg {
 // The unit a CTA works on: query tiles t0 (and t0 + 1), key tiles nk0 (nk1)
 // visited by them; nk1 = 0 when the unit has one tile.  Causal with units of
 // very different lengths (p.lpt): heaviest units first (longest-processing-time
-// order over all heads).  Otherwise the units of one head are adjacent, so CTAs
-// working at the same time share its K and V in L2.
+// order) within bands of heads.  Otherwise the units of one head are adjacent,
+// so CTAs working at the same time share its K and V in L2.
 struct Unit {
   int t0, bh, nk0, nk1;
   __device__ __forceinline__ int nk() const { return max(nk0, nk1); }
 };
 
-template <bool CAUSAL>
+// Key split (SPLITK): a unit is one query tile whose key tiles are shared out
+// between the two softmax warpgroups -- even key tiles to tile slot 0, odd ones
+// to slot 1 -- each keeping its own running max, sum and O; the epilogue merges
+// the two.  The unit's serial chain of key steps is halved, which is what
+// bounds problems with fewer query tiles than SMs.  nk0 / nk1 count the key
+// steps of each slot; slot i's step j is key tile 2 j + i.
+template <bool SPLITK>
+__device__ __forceinline__ int key_tile(int i, int j) {
+  return SPLITK ? 2 * j + i : j;
+}
+
+template <bool CAUSAL, bool SPLITK = false>
 __device__ __forceinline__ Unit unit_of(const FwdParams& p, int w) {
   Unit u;
   int unit;
   if (CAUSAL && p.lpt) {
-    unit = p.n_units - 1 - w / p.bh;
-    u.bh = w % p.bh;
+    // Longest first within bands of p.lpt heads (the last band may be
+    // smaller): the CTAs running at one time then read the K and V of only
+    // about a band of heads, which stays resident in L2.
+    const int span = p.lpt * p.n_units;
+    const int band = w / span, idx = w - band * span;
+    const int g = min(p.lpt, p.bh - band * p.lpt);
+    unit = p.n_units - 1 - idx / g;
+    u.bh = band * p.lpt + idx % g;
   } else {
     unit = w % p.n_units;
     u.bh = w / p.n_units;
@@ -158,9 +175,21 @@ __device__ __forceinline__ Unit unit_of(const FwdParams& p, int w) {
     const int last_row = min(t * BM + BM - 1, p.Nq - 1);
     return min(p.n_ktiles, (last_row + p.kv_off) / BN + 1);
   };
-  u.nk0 = tiles(u.t0);
-  u.nk1 = (p.tiles_per_cta == 2 && u.t0 + 1 < p.n_qtiles) ? tiles(u.t0 + 1) : 0;
+  if constexpr (SPLITK) {
+    const int nk = tiles(u.t0);
+    u.nk0 = (nk + 1) / 2;
+    u.nk1 = nk / 2;
+  } else {
+    u.nk0 = tiles(u.t0);
+    u.nk1 = (p.tiles_per_cta == 2 && u.t0 + 1 < p.n_qtiles) ? tiles(u.t0 + 1) : 0;
+  }
   return u;
+}
+
+// Key tiles a unit streams (each as K then V).
+template <bool SPLITK>
+__device__ __forceinline__ int unit_key_tiles(const Unit& u) {
+  return SPLITK ? u.nk0 + u.nk1 : u.nk();
 }
 
 __device__ int g_attn_status;  // 0 or kStatusTimeout; taken and cleared by status_take
@@ -215,10 +244,11 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const A
   return __all_sync(0xffffffffu, wait_bounded(bar, parity, ab));
 }
 
-template <int D, bool CAUSAL, bool PERSIST>
+template <int D, bool CAUSAL, bool PERSIST, bool SPLITK = false>
 __global__ void __launch_bounds__(kThreads, 1) attn_fwd_sm103(const __grid_constant__ FwdParams p) {
   using C = Cfg<D>;
   static_assert(!(PERSIST && C::STAGE_IN_Q), "O staged in the Q buffer: one unit per CTA");
+  static_assert(!SPLITK || (D == 64 && PERSIST), "key split: D = 64 persistent kernel only");
   constexpr int KB = C::KB;
   constexpr int NSLOT = C::NSLOT;
 
@@ -232,6 +262,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_sm103(const __grid_const
   const uint32_t sQ = base + C::OFF_Q;      // Q buffer qi = i * NQB + b at sQ + qi * TILE
   const uint32_t sStg = base + C::OFF_STG;  // O staging tile
   const uint32_t sKV = base + C::OFF_KV;    // slot s at sKV + s * TILE
+  // Key split: both slots read tile slot 0's Q buffers; slot 1's hold the two
+  // partial (max, sum) rows of every query row, [slot][max | sum][128].
+  float* const ml = reinterpret_cast<float*>(sbase + C::OFF_Q + C::NQB * C::TILE);
   auto bar = [base](int i) { return base + 8u * uint32_t(i); };
 
   const int warp = threadIdx.x >> 5;
@@ -255,6 +288,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_sm103(const __grid_const
   // rest.  Measured on the causal one-unit grid only: +5 % there (causal
   // N = 16384), -0.6 to -0.8 % on full rows, -1.8 % on the persistent grid.
   constexpr bool kSplitP = CAUSAL && !PERSIST;
+  (void)ml;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::NBAR; ++i) sm103::mbar_init(bar(i), C::count128(i) ? uint32_t(BM) : 1u);
@@ -289,7 +323,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_sm103(const __grid_const
         int nq0 = 0, nq1 = 0;  // Q loads issued for tile 0 / 1 (the n-th into buffer n % NQB)
         bool ok = true;
         for (int k = 0; k < kRounds && ok && more(k); ++k) {
-          const Unit u = unit_of<CAUSAL>(p, work(k));
+          const Unit u = unit_of<CAUSAL, SPLITK>(p, work(k));
           // A buffer is free once the last S MMA of the unit that used it before
           // (NQB loads ago) has finished.
           auto load_q = [&](int i, int nq) -> bool {
@@ -303,11 +337,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_sm103(const __grid_const
           };
           if (!(ok = load_q(0, nq0))) break;
           ++nq0;
-          if (u.nk1 > 0) {
+          if (!SPLITK && u.nk1 > 0) {
             if (!(ok = load_q(1, nq1))) break;
             ++nq1;
           }
-          const int nk = u.nk();
+          const int nk = unit_key_tiles<SPLITK>(u);
 #ifdef ATTN_TEST_HOOKS
           const bool withhold = p.withhold_kv != 0;
 #else
@@ -362,14 +396,15 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_sm103(const __grid_const
       for (int k = 0; k < kRounds && ok && more(k); ++k) {
         int nk0, nk1;
         {
-          const Unit u = unit_of<CAUSAL>(p, work(k));
+          const Unit u = unit_of<CAUSAL, SPLITK>(p, work(k));
           nk0 = u.nk0;
           nk1 = u.nk1;
         }
         const int nk = max(nk0, nk1);
         auto issue_s = [&](int i, int j) {
-          const int qi = i * C::NQB + (i == 0 ? nu0 : nu1) % C::NQB;
-          const uint32_t dk = desc_k + slot_off(int(cb) + 2 * j), dq = desc_q + uint32_t(qi) * (C::TILE >> 4);
+          const int qi = SPLITK ? nu0 % C::NQB : i * C::NQB + (i == 0 ? nu0 : nu1) % C::NQB;
+          const uint32_t dk = desc_k + slot_off(int(cb) + 2 * key_tile<SPLITK>(i, j));
+          const uint32_t dq = desc_q + uint32_t(qi) * (C::TILE >> 4);
           const uint32_t dS = tmem + C::COL_S + uint32_t(i) * BN;
 #pragma unroll(kUnrollS)
           for (int kk = 0; kk < D / 16; ++kk) {  // 16 of the head dim per MMA
@@ -377,7 +412,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_sm103(const __grid_const
             sm103::mma_ss_warp_lo(dS, dq + off, dk + off, kIdescS, kk > 0 ? 1u : 0u, hi);
           }
           sm103::mma_commit_warp(bar(C::B_SF + i));
-          if (j == (i == 0 ? nk0 : nk1) - 1) sm103::mma_commit_warp(bar(C::B_QE + qi));  // Q buffer no longer read
+          // Q buffer no longer read: after the unit's last S MMA on it.  With the
+          // key split that is slot 0's last S when the unit has an odd number of
+          // key tiles (nk0 = nk1 + 1), else slot 1's -- exactly one commit per unit.
+          const bool last_s = SPLITK ? (i == 0 ? (j == nk0 - 1 && nk1 < nk0) : (j == nk1 - 1 && nk1 == nk0))
+                                     : j == (i == 0 ? nk0 : nk1) - 1;
+          if (last_s) sm103::mma_commit_warp(bar(C::B_QE + qi));
         };
         auto issue_pv = [&](int i, int j) -> bool {
           if (!warp_wait(bar((kSplitP ? C::B_PH : C::B_PF) + i), ((ph >> (2 + i)) ^ uint32_t(j)) & 1u, ab)) return false;
@@ -386,7 +426,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_sm103(const __grid_const
             if (!warp_wait(bar(C::B_OE + i), uint32_t((i == 0 ? nu0 : nu1) - 1) & 1u, ab)) return false;
           }
           sm103::tc_fence_after();
-          const uint32_t dv = desc_v + slot_off(int(cb) + 2 * j + 1);
+          const uint32_t dv = desc_v + slot_off(int(cb) + 2 * key_tile<SPLITK>(i, j) + 1);
           const uint32_t aP = tmem + C::COL_S + uint32_t(i) * BN;
           const uint32_t dO = tmem + C::COL_O + uint32_t(i) * D;
 #pragma unroll
@@ -405,11 +445,39 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_sm103(const __grid_const
         sm103::tc_fence_after();
         issue_s(0, 0);
         if (nk1 > 0) {
-          if (!(ok = warp_wait(bar(C::B_Q + C::NQB + nu1 % C::NQB), uint32_t(nu1 / C::NQB) & 1u, ab))) break;
+          if constexpr (SPLITK) {
+            if (!(ok = wait_full(int(cb) + 2))) break;  // K of key tile 1
+          } else {
+            if (!(ok = warp_wait(bar(C::B_Q + C::NQB + nu1 % C::NQB), uint32_t(nu1 / C::NQB) & 1u, ab))) break;
+          }
           sm103::tc_fence_after();
           issue_s(1, 0);
         }
         release(int(cb));
+        if (SPLITK && nk1 > 0) release(int(cb) + 2);
+        if constexpr (SPLITK) {
+          // Step j: P V of key tiles 2j (slot 0) and 2j + 1 (slot 1), then S of
+          // key tiles 2j + 2 and 2j + 3 for the next step.
+          for (int j = 0; ok && j < nk; ++j) {
+            const bool has1 = j < nk1, next0 = j + 1 < nk0, next1 = j + 1 < nk1;
+            if (next0 && !(ok = wait_full(int(cb) + 2 * (2 * j + 2)))) break;
+            if (next1 && !(ok = wait_full(int(cb) + 2 * (2 * j + 3)))) break;
+            if (!(ok = wait_full(int(cb) + 2 * (2 * j) + 1))) break;
+            if (has1 && !(ok = wait_full(int(cb) + 2 * (2 * j + 1) + 1))) break;
+            sm103::tc_fence_after();
+            if (!(ok = issue_pv(0, j))) break;
+            if (next0) issue_s(0, j + 1);
+            if (has1) {
+              if (!(ok = issue_pv(1, j))) break;
+              if (next1) issue_s(1, j + 1);
+            }
+            release(int(cb) + 2 * (2 * j) + 1);
+            if (has1) release(int(cb) + 2 * (2 * j + 1) + 1);
+            if (next0) release(int(cb) + 2 * (2 * j + 2));
+            if (next1) release(int(cb) + 2 * (2 * j + 3));
+          }
+          cb += 2u * uint32_t(nk0 + nk1);
+        } else {
         for (int j = 0; ok && j < nk; ++j) {
           const bool next = j + 1 < nk;
           if (next && !(ok = wait_full(int(cb) + 2 * j + 2))) break;
@@ -427,6 +495,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_sm103(const __grid_const
           if (next) release(int(cb) + 2 * j + 2);
         }
         cb += 2u * uint32_t(nk);
+        }
         // Tile i: units +1, steps + nk_i.
         ph ^= uint32_t(nk0 & 1) << 2;
         ++nu0;
@@ -457,9 +526,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_sm103(const __grid_const
     for (int k = 0; k < kRounds && ok && more(k); ++k) {
       int nki, diag;  // key steps; causal: last visible key of this row (row + Nk - Nq)
       {
-        const Unit u = unit_of<CAUSAL>(p, work(k));
+        const Unit u = unit_of<CAUSAL, SPLITK>(p, work(k));
         nki = i == 0 ? u.nk0 : u.nk1;
-        diag = (u.t0 + i) * BM + r + p.kv_off;
+        diag = (u.t0 + (SPLITK ? 0 : i)) * BM + r + p.kv_off;
       }
       if (nki == 0) continue;
       float m_ref = 0.f;  // reference max (base 2) the exponents are taken against
@@ -475,8 +544,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_sm103(const __grid_const
           for (int c = 0; c < BN; ++c) s[c] = __uint_as_float(uu[c]);
         }
         // Masks: keys past N, and keys after the query row when causal.
-        int lim = min(BN - 1, p.Nk - 1 - j * BN);
-        if (CAUSAL) lim = min(lim, diag - j * BN);
+        const int kt = key_tile<SPLITK>(i, j);
+        int lim = min(BN - 1, p.Nk - 1 - kt * BN);
+        if (CAUSAL) lim = min(lim, diag - kt * BN);
         if (lim < BN - 1) {
 #pragma unroll
           for (int c = 0; c < BN; ++c) s[c] = c > lim ? -INFINITY : s[c];
@@ -569,6 +639,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_sm103(const __grid_const
       if (!ok) break;
       // 1/l for the epilogue, once it has read the previous unit's value; LSE from here.
       if ((ph & 4u) && !(ok = warp_wait(bar(C::B_OE + i), ((ph >> 1) & 1u) ^ 1u, ab))) break;
+      if constexpr (SPLITK) {
+        // The partial max and sum; the epilogue merges the two slots and writes LSE.
+        ml[(2 * i) * BM + r] = m_ref;
+        ml[(2 * i + 1) * BM + r] = l_run;
+        sm103::mbar_arrive(bar(C::B_FIN + i));
+        ph = ((ph ^ uint32_t(nki)) & 1u) | ((ph ^ 2u) & 2u) | 4u;
+        continue;
+      }
       invl[i * BM + r] = 1.f / l_run;
       sm103::mbar_arrive(bar(C::B_FIN + i));
       {
@@ -586,7 +664,67 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_sm103(const __grid_const
     int nu0 = 0, nu1 = 0, ns0 = 0, ns1 = 0;  // units and key steps of tile 0 / 1 so far (B_FIN, B_OE; B_OF)
     bool ok = true;
     for (int k = 0; k < kRounds && more(k); ++k) {
-      const Unit u = unit_of<CAUSAL>(p, work(k));
+      const Unit u = unit_of<CAUSAL, SPLITK>(p, work(k));
+      if constexpr (SPLITK) {
+        // One query tile per unit: merge the two slots' partial results.
+        //   m = max(m0, m1), c_i = 2^(m_i - m) / (2^(m0 - m) l0 + 2^(m1 - m) l1),
+        //   O = c0 O0 + c1 O1, LSE = ln 2 (m + log2 l).
+        const bool two = u.nk1 > 0;
+        if (ok) ok = warp_wait(bar(C::B_FIN), uint32_t(nu0) & 1u, ab);
+        if (ok) ok = warp_wait(bar(C::B_OF), uint32_t(ns0 + u.nk0 - 1) & 1u, ab);
+        if (ok && two) ok = warp_wait(bar(C::B_FIN + 1), uint32_t(nu1) & 1u, ab);
+        if (ok && two) ok = warp_wait(bar(C::B_OF + 1), uint32_t(ns1 + u.nk1 - 1) & 1u, ab);
+        if (r == 0) sm103::bulk_wait_read0();
+        ok = sm103::named_bar_and(1, 128, ok);
+        if (!ok) break;
+        sm103::tc_fence_after();
+        const float m0 = ml[r], l0 = ml[BM + r];
+        const float m1 = two ? ml[2 * BM + r] : -INFINITY, l1 = two ? ml[3 * BM + r] : 0.f;
+        const float m = fmaxf(m0, m1);
+        const float a0 = sm103::ex2_approx(m0 - m), a1 = two ? sm103::ex2_approx(m1 - m) : 0.f;
+        const float l = a0 * l0 + a1 * l1;
+        const float inv = 1.f / l;
+        const float c0 = a0 * inv, c1 = a1 * inv;
+        const uint32_t tO0 = tmem + lane_off + C::COL_O, tO1 = tO0 + uint32_t(D);
+#pragma unroll
+        for (int q = 0; q < D / 16; ++q) {  // 16 columns = two 16-byte chunks of the staging row
+          uint32_t v0[16], v1[16];
+          sm103::tmem_ld16(tO0 + q * 16, v0);
+          if (two) sm103::tmem_ld16(tO1 + q * 16, v1);
+          if (q == D / 16 - 1) {
+            sm103::tc_fence_before();
+            sm103::mbar_arrive(bar(C::B_OE));
+            if (two) sm103::mbar_arrive(bar(C::B_OE + 1));
+          }
+          uint32_t pk[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            float lo = __uint_as_float(v0[2 * e]) * c0, hi = __uint_as_float(v0[2 * e + 1]) * c0;
+            if (two) {
+              lo = fmaf(__uint_as_float(v1[2 * e]), c1, lo);
+              hi = fmaf(__uint_as_float(v1[2 * e + 1]), c1, hi);
+            }
+            pk[e] = sm103::pack_bf16x2(lo, hi);
+          }
+          const uint32_t rowbase = sStg + uint32_t(r) * 128u;
+          sm103::st_shared_v4(rowbase + ((uint32_t(2 * q) ^ uint32_t(r & 7)) << 4), pk[0], pk[1], pk[2], pk[3]);
+          sm103::st_shared_v4(rowbase + ((uint32_t(2 * q + 1) ^ uint32_t(r & 7)) << 4), pk[4], pk[5], pk[6], pk[7]);
+        }
+        sm103::fence_proxy_async_smem();
+        sm103::named_bar_sync(1, 128);
+        if (r == 0) {
+          sm103::tma_store_3d(&p.to, sStg, 0, u.t0 * BM, u.bh);
+          sm103::bulk_commit();
+        }
+        const int row = u.t0 * BM + r;
+        if (row < p.Nq) p.lse[size_t(u.bh) * size_t(p.Nq) + size_t(row)] = (m + log2f(l)) * 0.6931471805599453f;
+        ++nu0;
+        ns0 += u.nk0;
+        if (two) {
+          ++nu1;
+          ns1 += u.nk1;
+        }
+      } else {
       // The four warps agree (reduction barrier) before touching the
       // shared staging tile, so a warp that gave up on a wait cannot leave the
       // others stuck at the named barrier below.  Tile 0 is in every unit, so the
@@ -639,6 +777,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_sm103(const __grid_const
       if (u.nk1 > 0) {
         ++nu1;
         ns1 += u.nk1;
+      }
       }
     }
     if (r == 0) sm103::bulk_wait_read0();  // the stores have read shared memory

@@ -211,6 +211,11 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_byt
 // leading offset, the high word (stride 1024 B, version, 128-B swizzle) is the
 // same for every tile this library describes.
 constexpr uint32_t kSdescHi = (1024u >> 4) | (1u << 14) | (2u << 29);
+// High word for the unswizzled K-major layout: core matrices of 8 rows x 16
+// bytes (rows 16 bytes apart), `sbo_bytes` between 8-row groups along M / N;
+// the low word (sdesc_sw128_lo) then carries the start and, as its leading
+// offset, the distance between core matrices along K.
+__host__ __device__ constexpr uint32_t sdesc_noswz_hi(uint32_t sbo_bytes) { return (sbo_bytes >> 4) | (1u << 14); }
 __device__ __forceinline__ uint32_t sdesc_sw128_lo(uint32_t saddr, uint32_t lbo_bytes) {
   return ((saddr & 0x3FFFFu) >> 4) | (((lbo_bytes >> 4) & 0x3FFFu) << 16);
 }
@@ -342,6 +347,25 @@ __device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
 __device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
   uint64_t d;
   asm("add.f32x2 %0, %1, %2;\n" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;\n" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+// Packed bf16 pair product, rounded once to nearest even (the product of two
+// bf16 values is exact before that rounding).
+__device__ __forceinline__ uint32_t bf2_mul(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.bf16x2 %0, %1, %2;\n" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+// Byte permute of the pair {b:a} (selector nibbles 0-3 pick bytes of a, 4-7 of b).
+template <uint32_t SEL>
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;\n" : "=r"(d) : "r"(a), "r"(b), "n"(SEL));
   return d;
 }
 __device__ __forceinline__ float max3(float a, float b, float c) {
