@@ -93,6 +93,28 @@ attn_status_t attn_fwd_qk(const void* q, const void* k, const void* v, void* o, 
                           float scale, void* stream);
 
 /*
+ * attn_fwd_ld -- attn_fwd_qk for tensors whose rows are padded: every row of q,
+ * k, v and o starts `ld` elements after the previous one, i.e. [B, H, N, ld]
+ * buffers of which the first D columns are the data.  This takes any head
+ * dimension 1 <= D <= 256, including those that are not multiples of 8, which
+ * contiguous rows cannot carry (the tensor copies need 16-byte row strides).
+ * The FlashAttention-2 Triton forward shown on the pages takes per-tensor
+ * strides for the same purpose (null-ptr.tistory.com "development", the
+ * `_fwd_kernel` post: stride_qm, stride_kn, ...).
+ *
+ * The kernels use the first D8 = roundup8(D) columns of every row (the tensor
+ * copies move whole 16-byte groups): columns D..D8-1 of q, k, v must hold
+ * zeros (they add nothing then) and the same columns of o receive zeros;
+ * columns D8..ld-1 are never read or written.  ld must be a multiple of 8 and
+ * at least D8 (else ATTN_ERR_INVALID_ARG).  lse stays [B, H, Nq] contiguous.
+ * Sizes, pointer rules, masks and errors otherwise as attn_fwd_qk, with byte
+ * extents B*H*N*ld*2.
+ */
+attn_status_t attn_fwd_ld(const void* q, const void* k, const void* v, void* o, float* lse,
+                          int64_t B, int64_t H, int64_t Nq, int64_t Nk, int64_t D, int64_t ld,
+                          int causal, float scale, void* stream);
+
+/*
  * attn_fwd_from_host -- attn_fwd_qk for inputs and outputs in host memory.
  *
  * q_host, k_host, v_host : host (or device) pointers, the layouts of attn_fwd_qk's
@@ -156,6 +178,19 @@ attn_status_t attn_bwd_qk(const void* q, const void* k, const void* v, const voi
                           const float* lse, const void* dout, void* dq, void* dk, void* dv,
                           float* delta, int64_t B, int64_t H, int64_t Nq, int64_t Nk, int64_t D,
                           int causal, float scale, void* stream);
+
+/*
+ * attn_bwd_ld -- attn_bwd_qk for row-padded tensors: q, k, v, o, dout, dq, dk,
+ * dv all with rows `ld` elements apart, any head dimension 1 <= D <= 128; lse
+ * and delta contiguous [B, H, Nq].  As for attn_fwd_ld, the first roundup8(D)
+ * columns are used: columns D.. of that group must be zero in the inputs (as
+ * attn_fwd_ld leaves them in o) and receive zeros in dq, dk, dv; columns
+ * beyond it are never read or written.  Errors as attn_fwd_ld.
+ */
+attn_status_t attn_bwd_ld(const void* q, const void* k, const void* v, const void* o,
+                          const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                          float* delta, int64_t B, int64_t H, int64_t Nq, int64_t Nk, int64_t D,
+                          int64_t ld, int causal, float scale, void* stream);
 
 /*
  * attn_last_status -- report and clear the status word of the current device:

@@ -241,3 +241,34 @@ def test_based_no_gpu_means_cuda_error(lib):
         pytest.skip("a GPU is present")
     assert call_based() == pkg.ATTN_ERR_CUDA
     assert call_based(F=8, D=8) == pkg.ATTN_ERR_CUDA
+
+
+def call_ld(D=100, ld=104, **kw):
+    a = dict(q=A16, k=A16 + 64 * MB, v=A16 + 128 * MB, o=A16 + 192 * MB, lse=A16 + 256 * MB, B=1, H=2, Nq=256, Nk=256)
+    a.update(kw)
+    return pkg.attn_fwd_ld(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"], a["Nq"], a["Nk"], D, ld, 0, 0.125,
+                           None)
+
+
+def test_padded_rows_validation(lib):
+    """attn_fwd_ld / attn_bwd_ld: any head dim with rows padded to a multiple of 8 elements."""
+    import torch
+    gpu = torch.cuda.is_available()
+    for D, ld in ((4, 8), (12, 16), (100, 104), (100, 200), (255, 256), (1, 8), (96, 96)):
+        if not gpu:
+            assert call_ld(D=D, ld=ld) == pkg.ATTN_ERR_CUDA, (D, ld)  # past validation, no device
+    # ld must be a multiple of 8 and hold roundup8(D) columns
+    for D, ld in ((100, 100), (100, 96), (12, 12), (8, 4), (64, 0), (64, -8), (97, 100), (97, 96)):
+        assert call_ld(D=D, ld=ld) == pkg.ATTN_ERR_INVALID_ARG, (D, ld)
+    assert call_ld(D=260, ld=264) == pkg.ATTN_ERR_UNSUPPORTED
+    # o inside k when k is measured with its padded rows (2*256*104*2 bytes)
+    assert call_ld(o=A16 + 64 * MB + 2 * 256 * 100 * 2) == pkg.ATTN_ERR_INVALID_ARG
+    b = dict(q=A16, k=A16 + 64 * MB, v=A16 + 128 * MB, o=A16 + 192 * MB, lse=A16 + 256 * MB, do=A16 + 320 * MB,
+             dq=A16 + 384 * MB, dk=A16 + 448 * MB, dv=A16 + 512 * MB, dl=A16 + 576 * MB)
+    bwd = lambda D, ld: pkg.attn_bwd_ld(b["q"], b["k"], b["v"], b["o"], b["lse"], b["do"], b["dq"], b["dk"],  # noqa: E731
+                                        b["dv"], b["dl"], 1, 2, 256, 256, D, ld, 0, 0.125, None)
+    assert bwd(100, 100) == pkg.ATTN_ERR_INVALID_ARG
+    assert bwd(136, 136) == pkg.ATTN_ERR_UNSUPPORTED
+    if not gpu:
+        assert bwd(100, 104) == pkg.ATTN_ERR_CUDA
+        assert bwd(4, 8) == pkg.ATTN_ERR_CUDA

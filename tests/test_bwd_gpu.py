@@ -168,3 +168,42 @@ def test_backward_full_size_sampled(name, key_heads):
         dk_ref, dv_ref = oracle.attn_bwd_keys(q, k, v, do, w.causal, w.scale, h, kj)
         assert_sample_close(gk[h, kj], dk_ref, f"{name} dK of head {h}")
         assert_sample_close(gv[h, kj], dv_ref, f"{name} dV of head {h}")
+
+
+@pytest.mark.parametrize("D,ld", [(4, 8), (12, 24), (100, 104), (73, 80)])
+@pytest.mark.parametrize("causal", [False, True])
+def test_backward_padded_rows_any_head_dim(D, ld, causal):
+    """attn_bwd_ld: rows ld elements apart, head dims that are not multiples of 8; zeros up to
+    roundup8(D) and NaN beyond in the inputs (never read), a sentinel beyond roundup8(D) in the
+    gradient outputs (never written)."""
+    B, H, N = 1, 2, 300
+    q, k, v = make_qkv(B, H, N, D, seed=1800 + D)
+    do = make_qkv(B, H, N, D, seed=1801 + D)[0]
+    scale = 1.0 / math.sqrt(D)
+    d8 = (D + 7) // 8 * 8
+
+    def pad(bits, fill):
+        buf = np.full((B, H, N, ld), fill, dtype=np.uint16)
+        buf[..., :d8] = 0
+        buf[..., :D] = bits
+        return to_dev(buf)
+
+    nan, sentinel = 0x7FC0, 0x4049
+    qd, kd, vd, dod = pad(q, nan), pad(k, nan), pad(v, nan), pad(do, nan)
+    o = pad(np.zeros_like(q), nan)
+    lse = torch.empty((B, H, N), device="cuda")
+    s = torch.cuda.current_stream()
+    assert pkg.attn_fwd_ld(qd, kd, vd, o, lse, B, H, N, N, D, ld, causal, scale, s) == pkg.ATTN_OK
+    dq, dk, dv = (pad(np.zeros_like(q), sentinel) for _ in range(3))
+    delta = torch.full((B, H, N), float("nan"), device="cuda")
+    st = pkg.attn_bwd_ld(qd, kd, vd, o, lse, dod, dq, dk, dv, delta, B, H, N, N, D, ld, causal, scale, s)
+    assert st == pkg.ATTN_OK, pkg.attn_status_string(st)
+    assert pkg.attn_last_status(s) == pkg.ATTN_OK
+    got = {}
+    for n, t in (("dq", dq), ("dk", dk), ("dv", dv)):
+        bits = t.view(torch.int16).cpu().numpy().view(np.uint16)
+        assert np.all(bits[..., d8:] == sentinel), f"columns past roundup8(D) of {n} were written"
+        assert np.all(bits[..., D:d8] == 0), f"columns D..roundup8(D)-1 of {n} are not zero"
+        got[n] = t[..., :D].float().cpu().numpy().astype(np.float64)
+    got["delta"] = delta.cpu().numpy().astype(np.float64)
+    assert_grads_close(got, oracle.attn_bwd(q, k, v, do, causal, scale), f"D={D} ld={ld} causal={causal}")

@@ -329,3 +329,41 @@ def test_wide_head_dims_large_logits_and_many_tiles():
         full_check(q, k, v, causal, 1.0 / 16, f"D=256 N=2048 q_std=4 causal={causal}")
 
 
+
+
+def padded(bits, ld, fill):
+    """A [B, H, N, ld] device buffer: ``bits`` in the first D columns, zeros up to roundup8(D)
+    (the group of 16 bytes the kernels use), ``fill`` bits beyond."""
+    B, H, N, D = bits.shape
+    buf = np.full((B, H, N, ld), fill, dtype=np.uint16)
+    buf[..., :(D + 7) // 8 * 8] = 0
+    buf[..., :D] = bits
+    return to_dev(buf)
+
+
+@pytest.mark.parametrize("D,ld", [(4, 8), (12, 24), (100, 104), (100, 112), (200, 208), (1, 16)])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("Nq,Nk", [(300, 300), (100, 450)])
+def test_padded_rows_any_head_dim(D, ld, causal, Nq, Nk):
+    """attn_fwd_ld: rows ld elements apart, head dims that are not multiples of 8.  Beyond
+    roundup8(D) the inputs hold NaN (never read) and o a sentinel (never written); the columns
+    D..roundup8(D)-1 of o come back zero."""
+    q = make_qkv(2, 3, Nq, D, seed=1700 + D + Nq)[0]
+    _, k, v = make_qkv(2, 3, Nk, D, seed=1701 + D + Nk)
+    nan, sentinel = 0x7FC0, 0x4049  # bf16 NaN, 3.140625
+    qd, kd, vd = padded(q, ld, nan), padded(k, ld, nan), padded(v, ld, nan)
+    od = padded(np.zeros((2, 3, Nq, D), np.uint16), ld, sentinel)
+    od[..., :D] = float("nan")
+    lse = torch.full((2, 3, Nq), float("nan"), dtype=torch.float32, device="cuda")
+    s = torch.cuda.current_stream()
+    scale = 1.0 / math.sqrt(D)
+    st = pkg.attn_fwd_ld(qd, kd, vd, od, lse, 2, 3, Nq, Nk, D, ld, causal, scale, s)
+    assert st == pkg.ATTN_OK, pkg.attn_status_string(st)
+    assert pkg.attn_last_status(s) == pkg.ATTN_OK
+    d8 = (D + 7) // 8 * 8
+    ob = od.view(torch.int16).cpu().numpy().view(np.uint16)
+    assert np.all(ob[..., d8:] == sentinel), "columns past roundup8(D) of o were written"
+    assert np.all(ob[..., D:d8] == 0), "columns D..roundup8(D)-1 of o are not zero"
+    o = od[..., :D].float().cpu().numpy().astype(np.float64)
+    o_ref, lse_ref = oracle.attn_fwd(q, k, v, causal, scale)
+    assert_close(o, lse.cpu().numpy().astype(np.float64), o_ref, lse_ref, f"D={D} ld={ld} causal={causal} Nq={Nq} Nk={Nk}")

@@ -17,11 +17,13 @@ from ._binding import (  # noqa: F401
     attn_based_fwd,
     attn_based_fwd_flops,
     attn_bwd,
+    attn_bwd_ld,
     attn_bwd_qk,
     attn_bwd_qk_flops,
     attn_fwd,
     attn_fwd_flops,
     attn_fwd_from_host,
+    attn_fwd_ld,
     attn_fwd_qk,
     attn_fwd_qk_flops,
     attn_last_status,

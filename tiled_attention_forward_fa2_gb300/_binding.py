@@ -39,6 +39,8 @@ def load(path: str) -> ctypes.CDLL:
         "attn_bwd_qk": ([P] * 10 + [I64, I64, I64, I64, I64, I, ctypes.c_float, P], I),
         "attn_bwd_qk_flops": ([I64, I64, I64, I64, I64, I], ctypes.c_double),
         "attn_fwd_from_host": ([P] * 10 + [I64, I64, I64, I64, I64, I, ctypes.c_float, P], I),
+        "attn_fwd_ld": ([P, P, P, P, P, I64, I64, I64, I64, I64, I64, I, ctypes.c_float, P], I),
+        "attn_bwd_ld": ([P] * 10 + [I64, I64, I64, I64, I64, I64, I, ctypes.c_float, P], I),
         "attn_based_fwd": ([P, P, P, P, P, I64, I64, I64, I64, I64, ctypes.c_float, P], I),
         "attn_based_fwd_flops": ([I64, I64, I64, I64, I64], ctypes.c_double),
         "attn_test_withhold_kv": ([I], I),  # test build only
@@ -145,3 +147,19 @@ def attn_based_fwd(q, k, v, y, z, B: int, H: int, N: int, F: int, D: int, scale:
 
 def attn_based_fwd_flops(B: int, H: int, N: int, F: int, D: int) -> float:
     return library().attn_based_fwd_flops(int(B), int(H), int(N), int(F), int(D))
+
+
+def attn_fwd_ld(q, k, v, o, lse, B: int, H: int, Nq: int, Nk: int, D: int, ld: int, causal: bool, scale: float,
+                stream) -> int:
+    """Call ``attn_fwd_ld`` (rows ``ld`` elements apart; any head dim up to 256)."""
+    a = [_addr(x) for x in (q, k, v, o, lse)]
+    return library().attn_fwd_ld(*a, int(B), int(H), int(Nq), int(Nk), int(D), int(ld), int(bool(causal)),
+                                 float(scale), _stream(stream))
+
+
+def attn_bwd_ld(q, k, v, o, lse, dout, dq, dk, dv, delta, B: int, H: int, Nq: int, Nk: int, D: int, ld: int,
+                causal: bool, scale: float, stream) -> int:
+    """Call ``attn_bwd_ld`` (rows ``ld`` elements apart; any head dim up to 128)."""
+    a = [_addr(x) for x in (q, k, v, o, lse, dout, dq, dk, dv, delta)]
+    return library().attn_bwd_ld(*a, int(B), int(H), int(Nq), int(Nk), int(D), int(ld), int(bool(causal)),
+                                 float(scale), _stream(stream))

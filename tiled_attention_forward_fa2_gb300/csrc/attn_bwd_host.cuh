@@ -39,12 +39,21 @@ cudaError_t launch_bwd_kernels(const attn::BwdParams& prm, cudaStream_t st) {
   return cudaGetLastError();
 }
 
+// ld: row stride in elements of every [.., N, D] tensor (0 = contiguous, ld = D).
 attn_status_t launch_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
                          const void* dout, void* dq, void* dk, void* dv, float* delta, int64_t B, int64_t H,
-                         int64_t Nq, int64_t Nk, int64_t D, int causal, float scale, void* stream) {
+                         int64_t Nq, int64_t Nk, int64_t D, int causal, float scale, void* stream, int64_t ld = 0) {
   if (B < 0 || H < 0 || Nq < 0 || Nk < 0 || D <= 0) return ATTN_ERR_INVALID_ARG;
   if (!(scale > 0.f) || !std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
-  if (D > 128 || D % 8 != 0) return ATTN_ERR_UNSUPPORTED;
+  if (D > 128) return ATTN_ERR_UNSUPPORTED;
+  if (ld == 0) {
+    if (D % 8 != 0) return ATTN_ERR_UNSUPPORTED;  // contiguous rows must be 16-byte multiples (TMA)
+    ld = D;
+  } else {
+    // Padded rows: the kernels use the first roundup8(D) columns (see launch_fwd).
+    D = (D + 7) & ~int64_t(7);
+    if (ld < D || ld % 8 != 0 || ld > (int64_t(1) << 20)) return ATTN_ERR_INVALID_ARG;
+  }
   if (B == 0 || H == 0 || (Nq == 0 && Nk == 0)) return ATTN_OK;  // nothing is read or written
   // Nq = 0 leaves dK = dV = 0 and Nk = 0 leaves rows without keys: neither is
   // produced by these kernels.
@@ -56,8 +65,8 @@ attn_status_t launch_bwd(const void* q, const void* k, const void* v, const void
   const int64_t n_qtiles = (Nq + attn::BM - 1) / attn::BM, n_ktiles = (Nk + attn::BN - 1) / attn::BN;
   if (BH > kI32 / (n_qtiles > n_ktiles ? n_qtiles : n_ktiles)) return ATTN_ERR_INVALID_ARG;
   const int64_t Nmax = Nq > Nk ? Nq : Nk;
-  if (BH > (int64_t(1) << 62) / (Nmax * D * 2)) return ATTN_ERR_INVALID_ARG;
-  const uint64_t qb = uint64_t(BH) * uint64_t(Nq) * uint64_t(D) * 2u, kb = uint64_t(BH) * uint64_t(Nk) * uint64_t(D) * 2u;
+  if (BH > (int64_t(1) << 62) / (Nmax * ld * 2)) return ATTN_ERR_INVALID_ARG;
+  const uint64_t qb = uint64_t(BH) * uint64_t(Nq) * uint64_t(ld) * 2u, kb = uint64_t(BH) * uint64_t(Nk) * uint64_t(ld) * 2u;
   const uint64_t vb4 = uint64_t(BH) * uint64_t(Nq) * 4u;
   const auto mis16 = [](const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) != 0; };
   const auto mis4 = [](const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 3u) != 0; };
@@ -82,10 +91,10 @@ attn_status_t launch_bwd(const void* q, const void* k, const void* v, const void
   const EncodeTiledFn enc = encode_fn();
   if (!enc) return ATTN_ERR_CUDA;
   attn::BwdParams prm{};
-  if (!encode_qkv_map(enc, &prm.tq, q, D, Nq, BH) || !encode_qkv_map(enc, &prm.tdo, dout, D, Nq, BH) ||
-      !encode_qkv_map(enc, &prm.tk, k, D, Nk, BH) || !encode_qkv_map(enc, &prm.tv, v, D, Nk, BH) ||
-      !encode_qkv_map(enc, &prm.tdq, dq, D, Nq, BH) || !encode_qkv_map(enc, &prm.tdk, dk, D, Nk, BH) ||
-      !encode_qkv_map(enc, &prm.tdv, dv, D, Nk, BH))
+  if (!encode_qkv_map(enc, &prm.tq, q, D, Nq, BH, ld) || !encode_qkv_map(enc, &prm.tdo, dout, D, Nq, BH, ld) ||
+      !encode_qkv_map(enc, &prm.tk, k, D, Nk, BH, ld) || !encode_qkv_map(enc, &prm.tv, v, D, Nk, BH, ld) ||
+      !encode_qkv_map(enc, &prm.tdq, dq, D, Nq, BH, ld) || !encode_qkv_map(enc, &prm.tdk, dk, D, Nk, BH, ld) ||
+      !encode_qkv_map(enc, &prm.tdv, dv, D, Nk, BH, ld))
     return ATTN_ERR_CUDA;
   prm.o = static_cast<const __nv_bfloat16*>(o);
   prm.dout = static_cast<const __nv_bfloat16*>(dout);
@@ -98,6 +107,7 @@ attn_status_t launch_bwd(const void* q, const void* k, const void* v, const void
   prm.n_qtiles = int(n_qtiles);
   prm.n_ktiles = int(n_ktiles);
   prm.d = int(D);
+  prm.ld = int(ld);
   prm.scale = scale;
   prm.scale_log2 = scale * 1.4426950408889634f;
   prm.timeout_cycles = timeout_cycles();
@@ -124,6 +134,13 @@ attn_status_t attn_bwd_qk(const void* q, const void* k, const void* v, const voi
                           const void* dout, void* dq, void* dk, void* dv, float* delta, int64_t B, int64_t H,
                           int64_t Nq, int64_t Nk, int64_t D, int causal, float scale, void* stream) {
   return launch_bwd(q, k, v, o, lse, dout, dq, dk, dv, delta, B, H, Nq, Nk, D, causal, scale, stream);
+}
+
+attn_status_t attn_bwd_ld(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                          const void* dout, void* dq, void* dk, void* dv, float* delta, int64_t B, int64_t H,
+                          int64_t Nq, int64_t Nk, int64_t D, int64_t ld, int causal, float scale, void* stream) {
+  if (ld <= 0) return ATTN_ERR_INVALID_ARG;
+  return launch_bwd(q, k, v, o, lse, dout, dq, dk, dv, delta, B, H, Nq, Nk, D, causal, scale, stream, ld);
 }
 
 }  // extern "C"

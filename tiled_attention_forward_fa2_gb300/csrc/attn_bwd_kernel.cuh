@@ -41,6 +41,7 @@ struct BwdParams {
   float* delta;                 // [B*H, Nq] D_i: written by the dQ kernel, read by the dK/dV kernel
   int Nq, Nk, kv_off, bh, n_qtiles, n_ktiles;
   int d;                        // true head dim (<= the kernel's D; the rest is zero padding)
+  int ld;                       // row stride (elements) of every [.., N, D] tensor: a multiple of 8, >= d
   float scale;                  // softmax scale
   float scale_log2;             // scale * log2(e)
   long long timeout_cycles;
@@ -216,8 +217,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dq_sm103(const __grid
     // D_i = dO_i . O_i and the row's LSE in base 2 (rows past Nq: P = 0).
     float dlt = 0.f, lse2 = INFINITY;
     if (row < p.Nq) {
-      const uint4* po = reinterpret_cast<const uint4*>(p.o + (size_t(bh) * p.Nq + row) * size_t(p.d));
-      const uint4* pd = reinterpret_cast<const uint4*>(p.dout + (size_t(bh) * p.Nq + row) * size_t(p.d));
+      // Rows are p.ld elements apart (a multiple of 8, >= d); a partial last
+      // group of 8 is read in full (it lies within the row's padding) and
+      // masked to the first d elements.
+      const uint4* po = reinterpret_cast<const uint4*>(p.o + (size_t(bh) * p.Nq + row) * size_t(p.ld));
+      const uint4* pd = reinterpret_cast<const uint4*>(p.dout + (size_t(bh) * p.Nq + row) * size_t(p.ld));
       float a0 = 0.f, a1 = 0.f;
 #pragma unroll 4
       for (int x = 0; x < p.d / 8; ++x) {
@@ -227,6 +231,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dq_sm103(const __grid
         for (int e = 0; e < 4; ++e) {
           a0 = fmaf(sm103::bf16lo_to_f32(wo[e]), sm103::bf16lo_to_f32(wd[e]), a0);
           a1 = fmaf(sm103::bf16hi_to_f32(wo[e]), sm103::bf16hi_to_f32(wd[e]), a1);
+        }
+      }
+      if (p.d & 7) {
+        const int x = p.d / 8, rem = p.d & 7;
+        const uint4 uo = po[x], ud = pd[x];
+        const uint32_t wo[4] = {uo.x, uo.y, uo.z, uo.w}, wd[4] = {ud.x, ud.y, ud.z, ud.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          if (2 * e < rem) a0 = fmaf(sm103::bf16lo_to_f32(wo[e]), sm103::bf16lo_to_f32(wd[e]), a0);
+          if (2 * e + 1 < rem) a1 = fmaf(sm103::bf16hi_to_f32(wo[e]), sm103::bf16hi_to_f32(wd[e]), a1);
         }
       }
       dlt = a0 + a1;

@@ -37,11 +37,14 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// [B*H, N, D] bf16 viewed as a 3-D tensor {D, N, B*H}; boxes of 64 x 128 x 1
-// (64 bf16 = one 128-byte swizzle span); rows past N read as zero.
-bool encode_qkv_map(EncodeTiledFn enc, CUtensorMap* map, const void* ptr, int64_t D, int64_t N, int64_t BH) {
+// [B*H, N, D] bf16 with rows ld elements apart (ld = D when contiguous) viewed
+// as a 3-D tensor {D, N, B*H}; boxes of 64 x 128 x 1 (64 bf16 = one 128-byte
+// swizzle span); columns past D and rows past N read as zero and are never written.
+bool encode_qkv_map(EncodeTiledFn enc, CUtensorMap* map, const void* ptr, int64_t D, int64_t N, int64_t BH,
+                    int64_t ld = 0) {
+  if (ld == 0) ld = D;
   const cuuint64_t dims[3] = {cuuint64_t(D), cuuint64_t(N), cuuint64_t(BH)};
-  const cuuint64_t strides[2] = {cuuint64_t(D) * 2u, cuuint64_t(N) * cuuint64_t(D) * 2u};
+  const cuuint64_t strides[2] = {cuuint64_t(ld) * 2u, cuuint64_t(N) * cuuint64_t(ld) * 2u};
   const cuuint32_t box[3] = {64u, 128u, 1u};
   const cuuint32_t estride[3] = {1u, 1u, 1u};
   return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estride,
@@ -152,12 +155,22 @@ cudaError_t launch(const attn::FwdParams& prm, int64_t ctas, bool persist, bool 
 
 // Shared launcher of attn_fwd and attn_fwd_qk: Q, O [B*H, Nq, D]; K, V [B*H, Nk, D].
 // With check_only it validates the arguments and the device and returns.
+// ld: row stride in elements of q, k, v, o (0 = contiguous, ld = D).
 attn_status_t launch_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int64_t B, int64_t H,
                          int64_t Nq, int64_t Nk, int64_t D, int causal, float scale, void* stream,
-                         bool check_only = false) {
+                         bool check_only = false, int64_t ld = 0) {
   if (B < 0 || H < 0 || Nq < 0 || Nk < 0 || D <= 0) return ATTN_ERR_INVALID_ARG;
   if (!(scale > 0.f) || !std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
-  if (D > 256 || D % 8 != 0) return ATTN_ERR_UNSUPPORTED;
+  if (D > 256) return ATTN_ERR_UNSUPPORTED;
+  if (ld == 0) {
+    if (D % 8 != 0) return ATTN_ERR_UNSUPPORTED;  // contiguous rows must be 16-byte multiples (TMA)
+    ld = D;
+  } else {
+    // Padded rows: the kernels use the first roundup8(D) columns (the tensor
+    // copies move whole 16-byte groups); columns D.. of that group are zeros.
+    D = (D + 7) & ~int64_t(7);
+    if (ld < D || ld % 8 != 0 || ld > (int64_t(1) << 20)) return ATTN_ERR_INVALID_ARG;
+  }
   if (B == 0 || H == 0 || Nq == 0) return ATTN_OK;  // nothing is read or written
   // Query rows that see no key at all (Nk = 0, or causal with Nq > Nk) are not
   // produced by the kernel.
@@ -172,9 +185,9 @@ attn_status_t launch_fwd(const void* q, const void* k, const void* v, void* o, f
   // index, which runs up to two grid sizes past the last unit, stay in int32.
   if (BH > (kI32 - 4096) / n_qtiles) return ATTN_ERR_INVALID_ARG;
   const int64_t Nmax = Nq > Nk ? Nq : Nk;
-  if (BH > (int64_t(1) << 62) / (Nmax * D * 2)) return ATTN_ERR_INVALID_ARG;  // byte sizes
-  const uint64_t q_bytes = uint64_t(BH) * uint64_t(Nq) * uint64_t(D) * 2u;
-  const uint64_t kv_bytes = uint64_t(BH) * uint64_t(Nk) * uint64_t(D) * 2u;
+  if (BH > (int64_t(1) << 62) / (Nmax * ld * 2)) return ATTN_ERR_INVALID_ARG;  // byte sizes
+  const uint64_t q_bytes = uint64_t(BH) * uint64_t(Nq) * uint64_t(ld) * 2u;
+  const uint64_t kv_bytes = uint64_t(BH) * uint64_t(Nk) * uint64_t(ld) * 2u;
   const uint64_t lse_bytes = uint64_t(BH) * uint64_t(Nq) * 4u;
   const auto mis16 = [](const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) != 0; };
   if (mis16(q) || mis16(k) || mis16(v) || mis16(o) || (reinterpret_cast<uintptr_t>(lse) & 3u) != 0)
@@ -193,8 +206,8 @@ attn_status_t launch_fwd(const void* q, const void* k, const void* v, void* o, f
   if (!enc) return ATTN_ERR_CUDA;
 
   attn::FwdParams prm{};
-  if (!encode_qkv_map(enc, &prm.tq, q, D, Nq, BH) || !encode_qkv_map(enc, &prm.tk, k, D, Nk, BH) ||
-      !encode_qkv_map(enc, &prm.tv, v, D, Nk, BH) || !encode_qkv_map(enc, &prm.to, o, D, Nq, BH))
+  if (!encode_qkv_map(enc, &prm.tq, q, D, Nq, BH, ld) || !encode_qkv_map(enc, &prm.tk, k, D, Nk, BH, ld) ||
+      !encode_qkv_map(enc, &prm.tv, v, D, Nk, BH, ld) || !encode_qkv_map(enc, &prm.to, o, D, Nq, BH, ld))
     return ATTN_ERR_CUDA;
   // Two query tiles per CTA share every K/V tile and let two softmax warpgroups
   // take turns on the tensor core: one key step of both tiles costs about 3100
@@ -293,6 +306,12 @@ attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, flo
 attn_status_t attn_fwd_qk(const void* q, const void* k, const void* v, void* o, float* lse, int64_t B, int64_t H,
                           int64_t Nq, int64_t Nk, int64_t D, int causal, float scale, void* stream) {
   return launch_fwd(q, k, v, o, lse, B, H, Nq, Nk, D, causal, scale, stream);
+}
+
+attn_status_t attn_fwd_ld(const void* q, const void* k, const void* v, void* o, float* lse, int64_t B, int64_t H,
+                          int64_t Nq, int64_t Nk, int64_t D, int64_t ld, int causal, float scale, void* stream) {
+  if (ld <= 0) return ATTN_ERR_INVALID_ARG;
+  return launch_fwd(q, k, v, o, lse, B, H, Nq, Nk, D, causal, scale, stream, false, ld);
 }
 
 attn_status_t attn_last_status(void* stream) {

@@ -28,7 +28,7 @@
 // One CTA per (batch, head) sequence walks its chunks of 128 tokens.  Per
 // chunk c, on the tensor core (tcgen05, fp32 accumulators in TMEM), in issue order:
 //   S      = Q_c K_c^T                 (the raw tiles; the A warps apply the scale)
-//   Sig   += phi_K(K_c)^T V'_c         (M = features in two groups of 128, N = 80, K = 128 tokens)
+//   Sig^T += V'_c^T phi_K(K_c)         (M = 80 value columns (of 128), N = 160 features, K = 128 tokens)
 //   A'     = causal(1 + s + s^2/2) -> bf16, in TMEM over S  (A warps)
 //   Y'_b   = A' V'_c                   (intra-chunk part, b = c mod 2; A' read from TMEM)
 //   Y'_b  += phi_Q(Q_c) bf16(Sig before chunk c)            (all earlier chunks)
@@ -41,11 +41,14 @@
 //                128-byte-swizzled shared tiles; epilogue of the previous chunk
 //                (y -> bf16 -> TMA store, z -> global).
 //   warps 4-7  : A warps: the Taylor weights of the intra-chunk block, causal mask.
-//   warps 8-11 : state warps, one thread per feature (TMEM lane): Sig (fp32,
-//                TMEM) -> bf16 B operand in shared memory for the next readout.
+//   warps 8-11 : state warps, one thread per value column (TMEM lane): its row
+//                of Sig^T (fp32, TMEM) -> bf16 row of the readout's K-major B
+//                operand in shared memory (16-byte stores).
 //   warp 12    : TMA producer (q, k as two 8-feature boxes each, in the
 //                unswizzled K-major layout the S product reads; v 128-byte swizzled).
-//   warp 13    : allocates TMEM and issues every MMA (one elected lane).
+//   warp 15    : allocates TMEM and issues every MMA (one elected lane); the
+//                next chunk's S is issued right after this chunk's A' V', so the
+//                A warps work while the readout and the state update run.
 // Every barrier wait is bounded (the forward's status word and abort flag).
 #pragma once
 #include "attn_fwd_kernel.cuh"
@@ -56,7 +59,7 @@ constexpr int C = 128;          // tokens per chunk (= TMEM lanes)
 constexpr int NF = 160;         // phi features held (153 used)
 constexpr int NV = 80;          // columns of v', Y' and Sig: 64 values, the z column, padding
 constexpr int kThreads = 512;
-constexpr int kLoadWarp = 12, kMmaWarp = 13;
+constexpr int kLoadWarp = 12, kMmaWarp = 15;  // the MMA warp on the sub-partition with the idle state warp
 constexpr uint32_t kTile = 128u * 128u;    // 16 KB: 128 rows of 128 bytes
 constexpr int NQK = 4;                     // q/k stages
 constexpr int NVS = 2;                     // v stages
@@ -67,7 +70,7 @@ constexpr uint32_t kHalf = 128u * 16u;
 constexpr uint32_t kQK = 4u * kHalf;          // q and k tiles of one chunk
 constexpr uint32_t kSbfBlock = 80u * 128u;    // one 64-feature block of the bf16 state: 80 rows x 128 B
 constexpr uint32_t kTmemCols = 512;
-// Register split (setmaxnreg; warps 14 and 15 idle): 4 x 128 threads, sum = 512 x 128.
+// Register split (setmaxnreg; warps 13 and 14 idle): 4 x 128 threads, sum = 512 x 128.
 constexpr uint32_t kRegFeature = 152, kRegA = 104, kRegState = 192, kRegOther = 64;
 static_assert(kRegFeature + kRegA + kRegState + kRegOther == 4 * 128, "register split");
 
@@ -94,7 +97,7 @@ constexpr int B_QKF = 0;              // [NQK] q, k landed (TMA bytes)
 constexpr int B_QKE = B_QKF + NQK;    // [NQK] q, k rows read (128 feature threads) and S done (commit)
 constexpr int B_VF = B_QKE + NQK;     // [NVS] v landed
 constexpr int B_VE = B_VF + NVS;      // [NVS] last MMA on v done (commit)
-constexpr int B_PHIK = B_VE + NVS;    // phi_K of the chunk written (128)
+constexpr int B_PHIK = B_VE + NVS;    // phi_K of the chunk written (128 feature threads)
 constexpr int B_PHIQ = B_PHIK + 1;    // phi_Q written (128)
 constexpr int B_S = B_PHIQ + 1;       // S in TMEM (commit)
 constexpr int B_A = B_S + 1;          // A' in TMEM (128)
@@ -116,7 +119,7 @@ __host__ __device__ constexpr uint32_t bar_count(int b) {
 // TMEM columns
 constexpr uint32_t COL_S = 0;     // S (fp32, 128), then A' (bf16 pairs, 64)
 constexpr uint32_t COL_Y = 128;   // Y' buffer b at COL_Y + 96 b (80 each)
-constexpr uint32_t COL_SIG = 320; // Sig group g at COL_SIG + 96 g (80 each): features 128 g + lane
+constexpr uint32_t COL_SIG = 320; // Sig^T (160): lane = value column, column = feature
 
 struct BasedParams {
   CUtensorMap tq, tk;  // {F, N, B*H}, box {8, 128, 1}, no swizzle, zero fill
@@ -326,43 +329,43 @@ __global__ void __launch_bounds__(kThreads, 1) based_fwd_sm103(const __grid_cons
     } else if (warp == kMmaWarp) {
       // --------------------------------------------------------- MMA issue
       constexpr uint32_t kIdescS = sm103::idesc_bf16_f32(128, 128, 0, 0);    // q, k K-major (unswizzled)
-      constexpr uint32_t kIdescSig = sm103::idesc_bf16_f32(128, NV, 1, 1);   // phi_K^T (MN-major), v' MN-major
+      constexpr uint32_t kIdescSig = sm103::idesc_bf16_f32(128, 160, 1, 1);  // v'^T (MN-major), phi_K MN-major
       constexpr uint32_t kIdescYt = sm103::idesc_bf16_f32(128, NV, 0, 1);    // A' from TMEM, v' MN-major
       constexpr uint32_t kIdescYs = sm103::idesc_bf16_f32(128, NV, 0, 0);    // phi_Q K-major, state K-major
       const uint32_t hi = sm103::kSdescHi;
       constexpr uint32_t kHiRaw = sm103::sdesc_noswz_hi(128);  // 8-row groups 128 bytes apart
       const uint32_t dPQ = sm103::sdesc_sw128_lo(sPQ, 16);
+      const uint32_t dPK = sm103::sdesc_sw128_lo(sPK, kTile);  // phi_K as an MN-major operand: 64-feature blocks
       const uint32_t dSbf = sm103::sdesc_sw128_lo(sSbf, 16);
       bool ok = true;
+      // S = Q K^T of chunk c from the raw tiles (the two 8-feature halves kHalf apart along K).
+      auto issue_s = [&](int c) -> bool {
+        const int s = c % NQK;
+        if (!attn::warp_wait(bar(B_QKF + s), uint32_t(c / NQK) & 1u, ab)) return false;
+        sm103::tc_fence_after();
+        const uint32_t qk = sQK + uint32_t(s) * kQK;
+        sm103::mma_ss_warp_lo(tmem + COL_S, sm103::sdesc_sw128_lo(qk, kHalf), sm103::sdesc_sw128_lo(qk + 2u * kHalf, kHalf),
+                              kIdescS, 0u, kHiRaw);
+        sm103::mma_commit_warp(bar(B_S));
+        sm103::mma_commit_warp(bar(B_QKE + s));
+        return true;
+      };
+      if (n > 0) ok = issue_s(0);
       for (int c = 0; c < n && ok; ++c) {
-        const int s = c % NQK, sv = c % NVS, yb = c & 1;
+        const int sv = c % NVS, yb = c & 1;
         const uint32_t vslot = sV + uint32_t(sv) * kTile;
         // v' = [v | ones]: the second 64-column block sits at the ones block.
         const uint32_t dV = sm103::sdesc_sw128_lo(vslot, sOnes - vslot);
         const uint32_t tY = tmem + COL_Y + uint32_t(yb) * 96u;
-        // S = Q K^T from the raw tiles (the two 8-feature halves kHalf apart along K)
-        if (!(ok = attn::warp_wait(bar(B_QKF + s), uint32_t(c / NQK) & 1u, ab))) break;
-        sm103::tc_fence_after();
-        {
-          const uint32_t qk = sQK + uint32_t(s) * kQK;
-          sm103::mma_ss_warp_lo(tmem + COL_S, sm103::sdesc_sw128_lo(qk, kHalf),
-                                sm103::sdesc_sw128_lo(qk + 2u * kHalf, kHalf), kIdescS, 0u, kHiRaw);
-        }
-        sm103::mma_commit_warp(bar(B_S));
-        sm103::mma_commit_warp(bar(B_QKE + s));
-        // Sig += phi_K^T v'  (features 0..127, then 128..255)
+        // Sig^T += v'^T phi_K
         if (!(ok = attn::warp_wait(bar(B_PHIK), uint32_t(c) & 1u, ab))) break;
         if (!(ok = attn::warp_wait(bar(B_VF + sv), uint32_t(c / NVS) & 1u, ab))) break;
         if (c > 0 && !(ok = attn::warp_wait(bar(B_SIGF), uint32_t(c - 1) & 1u, ab))) break;
         sm103::tc_fence_after();
 #pragma unroll
-        for (int g = 0; g < 2; ++g) {
-          const uint32_t dA = sm103::sdesc_sw128_lo(sPK + uint32_t(g) * 2u * kTile, kTile);
-#pragma unroll
-          for (int kk = 0; kk < C / 16; ++kk)  // 16 tokens per MMA: 2048 bytes of rows
-            sm103::mma_ss_warp_lo(tmem + COL_SIG + uint32_t(g) * 96u, dA + uint32_t(kk) * 128u,
-                                  dV + uint32_t(kk) * 128u, kIdescSig, (c > 0 || kk > 0) ? 1u : 0u, hi);
-        }
+        for (int kk = 0; kk < C / 16; ++kk)  // 16 tokens per MMA: 2048 bytes of rows
+          sm103::mma_ss_warp_lo(tmem + COL_SIG, dV + uint32_t(kk) * 128u, dPK + uint32_t(kk) * 128u, kIdescSig,
+                                (c > 0 || kk > 0) ? 1u : 0u, hi);
         sm103::mma_commit_warp(bar(B_SIG));
         // Y'_b = A' v'  (buffer b last read by the epilogue of chunk c - 2)
         if (!(ok = attn::warp_wait(bar(B_A), uint32_t(c) & 1u, ab))) break;
@@ -373,6 +376,8 @@ __global__ void __launch_bounds__(kThreads, 1) based_fwd_sm103(const __grid_cons
           sm103::mma_ts_warp_lo(tY, tmem + COL_S + uint32_t(kk) * 8u, dV + uint32_t(kk) * 128u, kIdescYt,
                                 kk > 0 ? 1u : 0u, hi);
         sm103::mma_commit_warp(bar(B_VE + sv));
+        // The next chunk's S (over A' of this chunk, which the product above has read).
+        if (c + 1 < n && !(ok = issue_s(c + 1))) break;
         // Y'_b += phi_Q bf16(Sig of the earlier chunks)
         if (c > 0) {
           if (!(ok = attn::warp_wait(bar(B_PHIQ), uint32_t(c) & 1u, ab))) break;
@@ -477,7 +482,7 @@ __global__ void __launch_bounds__(kThreads, 1) based_fwd_sm103(const __grid_cons
         if (row < p.N) p.z[size_t(bh) * size_t(p.N) + size_t(row)] = zr;
       }
       // The next chunk's rows, and phi_K(c + 1) once the state update of chunk c
-      // (after S of chunk c) has read phi_K(c).
+      // has read phi_K(c).
       if (c + 1 < n && ok) {
         ok = load_rows(c + 1);
         if (ok) ok = attn::warp_wait(bar(B_SIG), uint32_t(c) & 1u, ab);
@@ -501,31 +506,29 @@ __global__ void __launch_bounds__(kThreads, 1) based_fwd_sm103(const __grid_cons
       // Quarter q reads S columns 32q..32q+31 and writes A' columns 16q..16q+15
       // (bf16 pairs), which hold S values already read.  The causal mask is
       // warp-uniform off the diagonal quarter: q < g all visible, q > g none.
+      // One quarter body (kept rolled: four roles share each SM sub-partition's
+      // instruction cache).
+#pragma unroll 1
+      for (int q = 0; q <= g; ++q) {
+        uint32_t sv[32], pk[16];
+        sm103::tmem_ld32(tS + uint32_t(q) * 32u, sv);
+        const int lim = r - q * 32;  // columns 32q + j with j <= lim are visible
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        uint32_t pk[16];
-        if (q > g) {
-#pragma unroll
-          for (int e = 0; e < 16; ++e) pk[e] = 0u;
-        } else {
-          uint32_t sv[32];
-          sm103::tmem_ld32(tS + uint32_t(q) * 32u, sv);
-#pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            // a = 1 + s (1 + s / 2), s = scale * S, two at a time
-            const uint64_t s2 = sm103::f2_mul(sm103::f2_pack(__uint_as_float(sv[2 * e]), __uint_as_float(sv[2 * e + 1])), sc2);
-            const uint64_t a2 = sm103::f2_fma(s2, sm103::f2_fma(s2, half2, one2), one2);
-            float a0, a1;
-            sm103::f2_unpack(a2, a0, a1);
-            if (q == g) {
-              const int j0 = q * 32 + 2 * e;
-              a0 = j0 <= r ? a0 : 0.f;
-              a1 = j0 + 1 <= r ? a1 : 0.f;
-            }
-            pk[e] = sm103::pack_bf16x2(a0, a1);
-          }
+        for (int e = 0; e < 16; ++e) {
+          // a = 1 + s (1 + s / 2), s = scale * S, two at a time
+          const uint64_t s2 = sm103::f2_mul(sm103::f2_pack(__uint_as_float(sv[2 * e]), __uint_as_float(sv[2 * e + 1])), sc2);
+          float a0, a1;
+          sm103::f2_unpack(sm103::f2_fma(s2, sm103::f2_fma(s2, half2, one2), one2), a0, a1);
+          pk[e] = sm103::pack_bf16x2(2 * e <= lim ? a0 : 0.f, 2 * e + 1 <= lim ? a1 : 0.f);
         }
         sm103::tmem_st16(tS + uint32_t(q) * 16u, pk);
+      }
+      {
+        uint32_t zero[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) zero[e] = 0u;
+#pragma unroll 1
+        for (int q = g + 1; q < 4; ++q) sm103::tmem_st16(tS + uint32_t(q) * 16u, zero);
       }
       sm103::tmem_st_wait();
       sm103::tc_fence_before();
@@ -534,50 +537,37 @@ __global__ void __launch_bounds__(kThreads, 1) based_fwd_sm103(const __grid_cons
   } else {
     // --------------------------------------------------------- state warps
     sm103::regs_increase<kRegState>();
-    const int f0 = (warp & 3) * 32 + lane;  // feature of this lane in group 0; group 1: 128 + lane (warp 8)
-    const uint32_t lane_off = uint32_t((warp & 3) * 32) << 16;
-    const bool g1 = (warp & 3) == 0;
-    // Lane pairs (features f, f + 1 with f even) trade halves: the even lane
-    // stores row 2e of both features, the odd lane row 2e + 1 (4-byte stores
-    // of two adjacent features of one K-major row).
-    auto store_feature = [&](int f, const uint32_t (&pk)[40]) {
-      const uint32_t fe = uint32_t(f & ~1);
-      const uint32_t blk = sSbf + (fe >> 6) * kSbfBlock;
-      const uint32_t chunk = (fe & 63u) >> 3, within = (fe & 7u) * 2u;
-      const uint32_t odd = uint32_t(lane & 1);
-#pragma unroll
-      for (int e = 0; e < 40; ++e) {
-        const uint32_t other = __shfl_xor_sync(0xffffffffu, pk[e], 1);
-        const uint32_t word = odd ? sm103::prmt<0x7632>(other, pk[e]) : sm103::prmt<0x5410>(pk[e], other);
-        const uint32_t nn = uint32_t(2 * e) + odd;
-        st_shared_u32(blk + nn * 128u + ((chunk ^ (nn & 7u)) << 4) + within, word);
-      }
-    };
-    auto load_group = [&](uint32_t col, uint32_t (&pk)[40]) {
-      uint32_t a[32], b[32], d[16];
-      sm103::tmem_ld32(tmem + lane_off + col, a);
-      sm103::tmem_ld32(tmem + lane_off + col + 32u, b);
-      sm103::tmem_ld16(tmem + lane_off + col + 64u, d);
-#pragma unroll
-      for (int e = 0; e < 16; ++e) {
-        pk[e] = sm103::pack_bf16x2(__uint_as_float(a[2 * e]), __uint_as_float(a[2 * e + 1]));
-        pk[16 + e] = sm103::pack_bf16x2(__uint_as_float(b[2 * e]), __uint_as_float(b[2 * e + 1]));
-      }
-#pragma unroll
-      for (int e = 0; e < 8; ++e) pk[32 + e] = sm103::pack_bf16x2(__uint_as_float(d[2 * e]), __uint_as_float(d[2 * e + 1]));
-    };
+    // Thread = value column d (TMEM lane) of Sig^T; columns 0..79 are the
+    // readout's B rows (64 values, the z column, zero padding).
+    const int d = (warp & 3) * 32 + lane;
+    const uint32_t tSig = tmem + (uint32_t((warp & 3) * 32) << 16) + COL_SIG;
+    const bool active = (warp & 3) < 3;  // lanes 96..127 hold no value column
     for (int c = 0; c < n; ++c) {
       if (!attn::warp_wait(bar(B_SIG), uint32_t(c) & 1u, ab)) break;
       sm103::tc_fence_after();
-      uint32_t p0[40], p1[40];
-      load_group(COL_SIG, p0);
-      if (g1) load_group(COL_SIG + 96u, p1);
+      uint32_t pk[80];  // features (2i, 2i+1) of row d, bf16
+      if (active) {
+#pragma unroll
+        for (int g = 0; g < 5; ++g) {
+          uint32_t a[32];
+          sm103::tmem_ld32(tSig + uint32_t(g) * 32u, a);
+#pragma unroll
+          for (int e = 0; e < 16; ++e) pk[16 * g + e] = sm103::pack_bf16x2(__uint_as_float(a[2 * e]), __uint_as_float(a[2 * e + 1]));
+        }
+      }
       sm103::tc_fence_before();
       sm103::mbar_arrive(bar(B_SIGF));
       // The readout of chunk c (B_Y) has read the bf16 state of chunk c - 1.
       if (!attn::warp_wait(bar(B_Y), uint32_t(c) & 1u, ab)) break;
-      store_feature(f0, p0);
-      if (g1) store_feature(128 + lane, p1);
+      if (active && d < NV) {
+        // Row d of the K-major B operand: 16-byte chunk q (features 8q..8q+7) at
+        // chunk (q mod 8) of 64-feature block q / 8, swizzled by the row.
+#pragma unroll
+        for (int q = 0; q < NF / 8; ++q)
+          sm103::st_shared_v4(sSbf + uint32_t(q / 8) * kSbfBlock + uint32_t(d) * 128u +
+                                  ((uint32_t(q % 8) ^ uint32_t(d & 7)) << 4),
+                              pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+      }
       sm103::fence_proxy_async_smem();
       sm103::mbar_arrive(bar(B_SBF));
     }
