@@ -504,6 +504,17 @@ def run_ours(args, w):
     pkg.library()
 
     q, k, v = w.qkv()
+    w_job = w
+    if args.shard_heads and world > 1:
+        # Strong scaling: each rank computes its contiguous block of the B*H
+        # slices (independent problems, no collective on the data path).
+        import dataclasses
+
+        from tiled_attention_forward_fa2_gb300.sharding import head_range
+        a, b = head_range(w.B * w.H, rank, world)
+        cut = lambda t: np.ascontiguousarray(t.reshape(w.B * w.H, *t.shape[2:])[a:b][None])  # noqa: E731
+        q, k, v = cut(q), cut(k), cut(v)
+        w = dataclasses.replace(w, B=1, H=b - a)
     qd, kd, vd = to_dev(q, dev), to_dev(k, dev), to_dev(v, dev)
     o = torch.empty_like(qd)
     lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
@@ -578,7 +589,11 @@ def run_ours(args, w):
     flops = (pkg.attn_bwd_qk_flops if args.backward else pkg.attn_fwd_qk_flops)(w.B, w.H, w.N, w.n_keys, w.D,
                                                                                 w.causal)
     ms_per_step = elapsed_ms / args.steps
-    value = job_tflops(flops, world, ms_per_step)
+    if w_job is w:
+        value = job_tflops(flops, world, ms_per_step)
+    else:  # the ranks share one problem: its FLOPs over the slowest rank's time
+        value = (pkg.attn_bwd_qk_flops if args.backward else pkg.attn_fwd_qk_flops)(
+            w_job.B, w_job.H, w_job.N, w_job.n_keys, w_job.D, w_job.causal) / (ms_per_step * 1e-3) / 1e12
 
     if args.backward:
         if rank == 0:
@@ -682,15 +697,17 @@ def run_ours(args, w):
         "warmup": args.warmup,
         "ms_per_step": ms_per_step,
         "higher_is_better": True,
-        "scaling": "weak",
+        "scaling": "weak" if w_job is w else "strong",
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic",
         "pct_of_peak": 100.0 * achieved / peak,
-        "config": workload_config(w, world),
+        "config": workload_config(w_job, world, None if w_job is w else {
+            "parallelism": f"B*H slices split over {world} ranks (contiguous blocks, no collective)"}),
         "roofline": roofline,
         "cpu_baseline": cpu,
-        "e2e": {"value": job_tflops(flops, world, e2e_ms), "unit": "TFLOP/s",
+        "e2e": {"value": job_tflops(flops, world, e2e_ms) if w_job is w else value * ms_per_step / e2e_ms,
+                "unit": "TFLOP/s",
                 "h2d_bytes_per_step": int(in_bytes), "d2h_bytes_per_step": int(o.numel() * 2 + lse.numel() * 4),
                 "ms_per_step": e2e_ms, "steps": e2e_steps},
         "gpu_launches": args.steps,
@@ -714,6 +731,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true",
                     help="skip the CPU oracle (no cpu_baseline and no parity object)")
     ap.add_argument("--no-backward", action="store_true", help="leave the backward object out of the line")
+    ap.add_argument("--shard-heads", action="store_true",
+                    help="under torchrun: split the workload's B*H slices over the ranks (strong scaling) instead of "
+                         "running one replica per rank (weak scaling, the default)")
     ap.add_argument("--backward", action="store_true",
                     help="time the backward (dQ, dK, dV; 2.5x the forward FLOPs) instead of the forward; device timing only")
     args = ap.parse_args()
