@@ -72,7 +72,8 @@ constexpr uint32_t kSbfBlock = 80u * 128u;    // one 64-feature block of the bf1
 constexpr uint32_t kTmemCols = 512;
 // Register split (setmaxnreg; warps 13 and 14 idle): 4 x 128 threads, sum = 512 x 128.
 constexpr uint32_t kRegFeature = 152, kRegA = 104, kRegState = 192, kRegOther = 64;
-static_assert(kRegFeature + kRegA + kRegState + kRegOther == 4 * 128, "register split");
+constexpr uint32_t kRegLaunch = 65536 / kThreads;  // registers per thread at launch (1 CTA per SM)
+static_assert(kRegFeature + kRegA + kRegState + kRegOther == 4 * kRegLaunch, "register split");
 
 // Shared memory (offsets from a 1024-byte aligned base).  The ones block must
 // follow the three phi_K blocks: it is the fourth 64-feature block the second
@@ -295,7 +296,7 @@ __global__ void __launch_bounds__(kThreads, 1) based_fwd_sm103(const __grid_cons
   const Abort ab{abort_flag, p.timeout_cycles};
 
   if (warp >= kLoadWarp) {
-    sm103::regs_decrease<kRegOther>();
+    sm103::regs_set<kRegOther, kRegLaunch>();
     if (warp == kLoadWarp) {
       // ---------------------------------------------------------- producer
       if (lane == 0) {
@@ -398,7 +399,7 @@ __global__ void __launch_bounds__(kThreads, 1) based_fwd_sm103(const __grid_cons
     }
   } else if (warp < 4) {
     // --------------------------------------------- feature warps + epilogue
-    sm103::regs_increase<kRegFeature>();
+    sm103::regs_set<kRegFeature, kRegLaunch>();
     const int r = int(threadIdx.x) & 127;
     const uint32_t lane_off = uint32_t((warp & 3) * 32) << 16;
     const float sc = p.scale;
@@ -494,7 +495,7 @@ __global__ void __launch_bounds__(kThreads, 1) based_fwd_sm103(const __grid_cons
     if (r == 0) sm103::bulk_wait_read0();
   } else if (warp < 8) {
     // ------------------------------------------------------------- A warps
-    sm103::regs_decrease<kRegA>();
+    sm103::regs_set<kRegA, kRegLaunch>();
     const int r = int(threadIdx.x) & 127;
     const uint32_t tS = tmem + (uint32_t((warp & 3) * 32) << 16) + COL_S;
     const float sc = p.scale;
@@ -536,7 +537,7 @@ __global__ void __launch_bounds__(kThreads, 1) based_fwd_sm103(const __grid_cons
     }
   } else {
     // --------------------------------------------------------- state warps
-    sm103::regs_increase<kRegState>();
+    sm103::regs_set<kRegState, kRegLaunch>();
     // Thread = value column d (TMEM lane) of Sig^T; columns 0..79 are the
     // readout's B rows (64 values, the z column, zero padding).
     const int d = (warp & 3) * 32 + lane;

@@ -340,6 +340,15 @@ template <uint32_t NREG>
 __device__ __forceinline__ void regs_decrease() {
   asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(NREG));
 }
+// Move this warpgroup from the LAUNCH registers per thread it started with to
+// NREG: an increase or a decrease, chosen at compile time (an increase to
+// fewer registers than the warp holds is an invalid request).
+template <uint32_t NREG, uint32_t LAUNCH>
+__device__ __forceinline__ void regs_set() {
+  static_assert(NREG % 8 == 0 && NREG >= 24 && NREG <= 256, "setmaxnreg range");
+  if constexpr (NREG > LAUNCH) regs_increase<NREG>();
+  else if constexpr (NREG < LAUNCH) regs_decrease<NREG>();
+}
 
 // ------------------------------------------------- packed fp32 pairs (sm_100+)
 __device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
