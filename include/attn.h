@@ -147,6 +147,50 @@ attn_status_t attn_fwd_from_host(const void* q_host, const void* k_host, const v
                                  float* lse, int64_t B, int64_t H, int64_t Nq, int64_t Nk,
                                  int64_t D, int causal, float scale, void* stream);
 
+/* Size in bytes of the device array that attn_fwd_from_host_static stages through. */
+#define ATTN_STATIC_STAGING_BYTES (64u << 20)
+
+/*
+ * attn_fwd_from_host_static -- attn_fwd_from_host without caller-owned device
+ * buffers, for callers that hold host data and a stream but cannot allocate
+ * device memory.  The pages have no counterpart: their forward always runs on
+ * tensors that already sit in device memory.
+ *
+ * q_host, k_host, v_host, o_host, lse_host : as attn_fwd_from_host (host, or
+ *           device, pointers in attn_fwd_qk's layouts; the first three read,
+ *           the last two written).  Other arguments as attn_fwd_qk.
+ *
+ * Staging: Q, K, V, O and LSE are placed one after another, each on a 256-byte
+ * boundary, in one device array of ATTN_STATIC_STAGING_BYTES (64 MiB) that is
+ * part of this library's device code.  No device memory is allocated or freed
+ * by the call.  The array exists on every device that has loaded the library's
+ * device code, is shared by every call on that device and keeps the last
+ * call's inputs and results; nothing in it needs to start at zero (each call
+ * writes, before its kernel, every byte that kernel reads).
+ *
+ * Ordering: three host-to-device copies, the kernel and two device-to-host
+ * copies are enqueued on `stream` behind the work already there, and the call
+ * returns; synchronising `stream` waits for all of it.  Calls whose work can
+ * overlap on the device (on different streams, or from several host threads
+ * without ordering) race on the shared array and give undefined results; order
+ * them on one stream.  The first call on a device looks up the array's device
+ * address (and may load the library's device code); make that first call before
+ * any stream capture begins.  Host buffers should be pinned for the copies to
+ * be asynchronous and must stay valid until the work completes.
+ *
+ * Errors: attn_fwd_qk's argument rules (ATTN_ERR_INVALID_ARG for a null host
+ * pointer in a non-empty problem); ATTN_ERR_UNSUPPORTED when the staged bytes
+ * (2 B*H*(2 Nq + 2 Nk) D plus 4 B*H*Nq, with each part rounded up to 256) exceed
+ * ATTN_STATIC_STAGING_BYTES -- use attn_fwd_from_host with buffers of one's own
+ * then; ATTN_ERR_CUDA for a failed copy, launch or address lookup (work enqueued
+ * before the failure stays enqueued); timeouts through attn_last_status.
+ * Results are bit-identical to attn_fwd_qk on the same inputs.
+ */
+attn_status_t attn_fwd_from_host_static(const void* q_host, const void* k_host, const void* v_host,
+                                        void* o_host, float* lse_host, int64_t B, int64_t H,
+                                        int64_t Nq, int64_t Nk, int64_t D, int causal, float scale,
+                                        void* stream);
+
 /*
  * attn_bwd -- enqueue the backward of attn_fwd on `stream`: the gradients of
  * sum(dO * O) with respect to Q, K and V.

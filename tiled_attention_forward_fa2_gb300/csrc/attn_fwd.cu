@@ -379,6 +379,7 @@ double attn_fwd_qk_flops(int64_t B, int64_t H, int64_t Nq, int64_t Nk, int64_t D
 }  // extern "C"
 #include "attn_bwd_host.cuh"
 #include "attn_host_pipeline.cuh"
+#include "attn_host_static.cuh"
 #include "based_fwd_host.cuh"
 
 extern "C" double attn_bwd_qk_flops(int64_t B, int64_t H, int64_t Nq, int64_t Nk, int64_t D, int causal) {
