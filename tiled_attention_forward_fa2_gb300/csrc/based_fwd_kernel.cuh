@@ -71,7 +71,9 @@ constexpr uint32_t kQK = 4u * kHalf;          // q and k tiles of one chunk
 constexpr uint32_t kSbfBlock = 80u * 128u;    // one 64-feature block of the bf16 state: 80 rows x 128 B
 constexpr uint32_t kTmemCols = 512;
 // Register split (setmaxnreg; warps 13 and 14 idle): 4 x 128 threads, sum = 512 x 128.
-constexpr uint32_t kRegFeature = 152, kRegA = 104, kRegState = 192, kRegOther = 64;
+// The load/MMA warpgroup spills at 72 or fewer (ptxas); the state warps need
+// no more than 176.
+constexpr uint32_t kRegFeature = 152, kRegA = 104, kRegState = 176, kRegOther = 80;
 constexpr uint32_t kRegLaunch = 65536 / kThreads;  // registers per thread at launch (1 CTA per SM)
 static_assert(kRegFeature + kRegA + kRegState + kRegOther == 4 * kRegLaunch, "register split");
 
