@@ -39,20 +39,21 @@ METRIC = "attention fwd TFLOP/s (bf16, 1×GB300) and % of dense BF16 tensor peak
 DEFAULT_WORKLOAD = "b4h16n4096d128"
 L2_BYTES = 129 * 2**20
 FALLBACK_PEAK_TFLOPS = 1900.0
-KERNEL_SOURCES = ["tiled_attention_forward_fa2_gb300/csrc/attn_fwd_kernel.cuh",
-                  "tiled_attention_forward_fa2_gb300/csrc/based_fwd_kernel.cuh",
-                  "tiled_attention_forward_fa2_gb300/csrc/based_fwd_host.cuh",
-                  "tiled_attention_forward_fa2_gb300/csrc/attn_bwd_kernel.cuh",
-                  "tiled_attention_forward_fa2_gb300/csrc/attn_bwd_host.cuh",
-                  "tiled_attention_forward_fa2_gb300/csrc/sm103_ptx.cuh",
-                  "tiled_attention_forward_fa2_gb300/csrc/attn_fwd.cu"]
+_CSRC = "tiled_attention_forward_fa2_gb300/csrc/"
+# Sources that decide what each kernel family runs (kernel, launcher, PTX helpers);
+# an ncu summary's traffic figure is used only while these are unchanged.
+KERNEL_SOURCES = {
+    "fwd": [_CSRC + f for f in ("attn_fwd_kernel.cuh", "sm103_ptx.cuh", "attn_fwd.cu")],
+    "based": [_CSRC + f for f in ("based_fwd_kernel.cuh", "based_fwd_host.cuh", "sm103_ptx.cuh")],
+    "bwd": [_CSRC + f for f in ("attn_bwd_kernel.cuh", "attn_bwd_host.cuh", "sm103_ptx.cuh")],
+}
 
 
-def kernel_source_hash() -> str:
-    """Hash of the kernel sources' code: comments and blank lines are left out,
-    so editing a comment does not mark the committed ncu summaries stale."""
+def kernel_source_hash(family: str = "fwd") -> str:
+    """Hash of one kernel family's sources' code: comments and blank lines are
+    left out, so editing a comment does not mark the committed ncu summaries stale."""
     h = hashlib.sha256()
-    for f in KERNEL_SOURCES:
+    for f in KERNEL_SOURCES[family]:
         with open(os.path.join(ROOT, f), encoding="utf-8") as fh:
             text = re.sub(r"/\*.*?\*/", "", fh.read(), flags=re.S)
         lines = [re.sub(r"//.*$", "", ln).rstrip() for ln in text.splitlines()]
@@ -90,15 +91,15 @@ def measured_peaks():
     return {"bf16_tflops": FALLBACK_PEAK_TFLOPS, "hbm_gbs": 6800.0}, "fallback"
 
 
-def ncu_traffic(workload: str):
+def ncu_traffic(workload: str, kernel: str = "attn_fwd_sm103", family: str = "fwd"):
     """DRAM bytes per launch from the committed ncu summary, if taken on this kernel source."""
-    path = os.path.join(ROOT, "profiles", f"attn_fwd_sm103_{workload}.md")
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
     if not os.path.exists(path):
         return None
     text = open(path).read()
     m_src = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]{16})", text)
     m_tr = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
-    if not m_src or not m_tr or m_src.group(1) != kernel_source_hash():
+    if not m_src or not m_tr or m_src.group(1) != kernel_source_hash(family):
         return None
     return float(m_tr.group(1))
 
@@ -414,14 +415,15 @@ def run_based(args, w):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": based_config(w, world),
         "roofline": {"bound": "hbm", "achieved": gbs, "peak": float(peaks["hbm_gbs"]), "unit": "GB/s",
-                     "frac": gbs / float(peaks["hbm_gbs"]), "traffic": None, "algorithmic_bytes": alg,
+                     "frac": gbs / float(peaks["hbm_gbs"]), "traffic": ncu_traffic(w.name, "based_fwd_sm103", "based"),
+                     "algorithmic_bytes": alg,
                      "peak_source": f"hbm_gbs of {peak_src}", "kernel": "based_fwd_sm103"},
         "cpu_baseline": cpu,
         "e2e": {"value": job_tflops(flops, world, e2e_ms), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": int(q.nbytes + k.nbytes + v.nbytes),
                 "d2h_bytes_per_step": int(y.numel() * 2 + z.numel() * 4), "ms_per_step": e2e_ms, "steps": e2e_steps},
         "gpu_launches": args.steps, "clocks": sampler.summary() if sampler else None,
-        "kernel_source": kernel_source_hash(), "parity": parity,
+        "kernel_source": kernel_source_hash("based"), "parity": parity,
     }
     print(json.dumps(line), flush=True)
     if pg:
@@ -609,7 +611,7 @@ def run_ours(args, w):
                                  "peak_source": f"bf16_tflops (burst) of {peak_src}",
                                  "kernel": "attn_bwd_dq_sm103 + attn_bwd_dkdv_sm103"},
                     "gpu_launches": 2 * args.steps, "clocks": sampler.summary() if sampler else None,
-                    "kernel_source": kernel_source_hash()}
+                    "kernel_source": kernel_source_hash("bwd")}
             print(json.dumps(line), flush=True)
         if pg:
             pg.destroy_process_group()

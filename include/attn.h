@@ -202,11 +202,13 @@ attn_status_t attn_fwd_from_host_static(const void* q_host, const void* k_host, 
  * (ds_ij = p_ij (dp_ij - D_i)); returned so that no scratch memory is needed.
  * Outputs must not overlap each other or any input.  Same sizes, alignment
  * (16 bytes for bf16 tensors, 4 for fp32) and scale rules as attn_fwd; head
- * dims a multiple of 8 up to 128 (ATTN_ERR_UNSUPPORTED above).  The pages call the backward an order of magnitude harder than
- * the forward ("GPUの爆発的な性能向上", ja.news.hada.io topic 14783) without a
- * formula; the math is the chain rule written out in oracle/attn_oracle_bwd.c
- * and the kernels' header comment.  Two kernels are enqueued (dQ and D first,
- * then dK and dV); errors as attn_fwd, timeouts through attn_last_status.
+ * dims a multiple of 8 up to 256, like attn_fwd (ATTN_ERR_UNSUPPORTED
+ * otherwise; 136..256 run on the D = 256 kernels, zero-padded).  The pages
+ * call the backward an order of magnitude harder than the forward
+ * ("GPUの爆発的な性能向上", ja.news.hada.io topic 14783) without a formula;
+ * the math is the chain rule written out in oracle/attn_oracle_bwd.c and the
+ * kernels' header comment.  Two kernels are enqueued (dQ and D first, then dK
+ * and dV); errors as attn_fwd, timeouts through attn_last_status.
  */
 attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
                        const void* dout, void* dq, void* dk, void* dv, float* delta, int64_t B,
@@ -225,7 +227,7 @@ attn_status_t attn_bwd_qk(const void* q, const void* k, const void* v, const voi
 
 /*
  * attn_bwd_ld -- attn_bwd_qk for row-padded tensors: q, k, v, o, dout, dq, dk,
- * dv all with rows `ld` elements apart, any head dimension 1 <= D <= 128; lse
+ * dv all with rows `ld` elements apart, any head dimension 1 <= D <= 256; lse
  * and delta contiguous [B, H, Nq].  As for attn_fwd_ld, the first roundup8(D)
  * columns are used: columns D.. of that group must be zero in the inputs (as
  * attn_fwd_ld leaves them in o) and receive zeros in dq, dk, dv; columns

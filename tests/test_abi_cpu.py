@@ -104,9 +104,13 @@ def call_bwd(D=64, **kw):
 
 
 def test_backward_head_dims(lib):
-    """The backward stops at D = 128 (its kernels' TMEM and shared-memory budgets)."""
-    for d in (4, 100, 136, 192, 256):
+    """The backward takes contiguous head dims that are multiples of 8 up to 256, like the forward."""
+    import torch
+    for d in (4, 100, 260, 264, 512):
         assert call_bwd(D=d) == pkg.ATTN_ERR_UNSUPPORTED
+    if not torch.cuda.is_available():
+        for d in (8, 136, 192, 256):
+            assert call_bwd(D=d) == pkg.ATTN_ERR_CUDA  # past validation, no device
     assert call_bwd(D=64, dq=None) == pkg.ATTN_ERR_INVALID_ARG
 
 
@@ -268,7 +272,8 @@ def test_padded_rows_validation(lib):
     bwd = lambda D, ld: pkg.attn_bwd_ld(b["q"], b["k"], b["v"], b["o"], b["lse"], b["do"], b["dq"], b["dk"],  # noqa: E731
                                         b["dv"], b["dl"], 1, 2, 256, 256, D, ld, 0, 0.125, None)
     assert bwd(100, 100) == pkg.ATTN_ERR_INVALID_ARG
-    assert bwd(136, 136) == pkg.ATTN_ERR_UNSUPPORTED
+    assert bwd(260, 264) == pkg.ATTN_ERR_UNSUPPORTED
     if not gpu:
         assert bwd(100, 104) == pkg.ATTN_ERR_CUDA
         assert bwd(4, 8) == pkg.ATTN_ERR_CUDA
+        assert bwd(250, 256) == pkg.ATTN_ERR_CUDA

@@ -116,6 +116,28 @@ def test_backward_padded_head_dims(D, causal):
     assert_grads_close(got, ref, f"D={D} causal={causal}")
 
 
+@pytest.mark.parametrize("D", [136, 192, 256])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("N", [1, 33, 200, 640])
+def test_backward_head_dims_above_128(N, D, causal):
+    """The D = 256 kernels (64-key steps for dQ; dK and dV in two 128-column halves over
+    32-query stages), with D = 136 and 192 zero-padded to 256: several key tiles, ragged tails."""
+    got, ref = grads(2, 2, N, N, D, causal, seed=1900 + N + D)
+    assert_grads_close(got, ref, f"N={N} D={D} causal={causal}")
+
+
+@pytest.mark.parametrize("D", [256, 200])
+@pytest.mark.parametrize("Nq,Nk,causal", [(1, 500, True), (130, 700, True), (700, 300, False)])
+def test_backward_head_dims_above_128_different_lengths(Nq, Nk, causal, D):
+    got, ref = grads(1, 2, Nq, Nk, D, causal, seed=1950 + Nq + Nk)
+    assert_grads_close(got, ref, f"Nq={Nq} Nk={Nk} D={D} causal={causal}")
+
+
+def test_backward_d256_large_logits():
+    got, ref = grads(1, 2, 512, 512, 256, True, seed=1990, q_std=4.0)
+    assert_grads_close(got, ref, "q_std=4 N=512 D=256 causal")
+
+
 def sample_idx(n_bh, n, n_random, seed):
     """Random (head, index) pairs plus the first and last 64 indices of the first and last head."""
     rng = np.random.default_rng(seed)
@@ -170,7 +192,7 @@ def test_backward_full_size_sampled(name, key_heads):
         assert_sample_close(gv[h, kj], dv_ref, f"{name} dV of head {h}")
 
 
-@pytest.mark.parametrize("D,ld", [(4, 8), (12, 24), (100, 104), (73, 80)])
+@pytest.mark.parametrize("D,ld", [(4, 8), (12, 24), (100, 104), (73, 80), (250, 256), (129, 144)])
 @pytest.mark.parametrize("causal", [False, True])
 def test_backward_padded_rows_any_head_dim(D, ld, causal):
     """attn_bwd_ld: rows ld elements apart, head dims that are not multiples of 8; zeros up to

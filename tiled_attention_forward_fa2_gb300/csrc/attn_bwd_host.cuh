@@ -22,20 +22,24 @@ attn_status_t prepare_bwd(int dev) {
   std::lock_guard<std::mutex> lock(g_dev_mutex);
   if (g_bwd_ready[dev].load(std::memory_order_relaxed) == 1) return ATTN_OK;
   if (opt_in_bwd_smem<64, false>() != cudaSuccess || opt_in_bwd_smem<64, true>() != cudaSuccess ||
-      opt_in_bwd_smem<128, false>() != cudaSuccess || opt_in_bwd_smem<128, true>() != cudaSuccess)
+      opt_in_bwd_smem<128, false>() != cudaSuccess || opt_in_bwd_smem<128, true>() != cudaSuccess ||
+      opt_in_bwd_smem<256, false>() != cudaSuccess || opt_in_bwd_smem<256, true>() != cudaSuccess)
     return ATTN_ERR_CUDA;
   g_bwd_ready[dev].store(1, std::memory_order_release);
   return ATTN_OK;
 }
 
+// prm_dq, prm_dkv: the same problem; they differ only in the box heights of
+// the load maps (D = 256: 64-key K/V boxes for dQ, 32-query Q/dO boxes for dK/dV).
 template <int D, bool CAUSAL>
-cudaError_t launch_bwd_kernels(const attn::BwdParams& prm, cudaStream_t st) {
-  attn::attn_bwd_dq_sm103<D, CAUSAL>
-      <<<dim3(unsigned(int64_t(prm.n_qtiles) * prm.bh)), dim3(attn::kBwdThreads), attn::CfgDq<D>::SMEM, st>>>(prm);
+cudaError_t launch_bwd_kernels(const attn::BwdParams& prm_dq, const attn::BwdParams& prm_dkv, cudaStream_t st) {
+  attn::attn_bwd_dq_sm103<D, CAUSAL><<<dim3(unsigned(int64_t(prm_dq.n_qtiles) * prm_dq.bh)), dim3(attn::kBwdThreads),
+                                       attn::CfgDq<D>::SMEM, st>>>(prm_dq);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   attn::attn_bwd_dkdv_sm103<D, CAUSAL>
-      <<<dim3(unsigned(int64_t(prm.n_ktiles) * prm.bh)), dim3(attn::kBwdThreads), attn::CfgDkv<D>::SMEM, st>>>(prm);
+      <<<dim3(unsigned(int64_t(prm_dkv.n_ktiles) * prm_dkv.bh * attn::CfgDkv<D>::NHALF)), dim3(attn::kBwdThreads),
+         attn::CfgDkv<D>::SMEM, st>>>(prm_dkv);
   return cudaGetLastError();
 }
 
@@ -45,7 +49,7 @@ attn_status_t launch_bwd(const void* q, const void* k, const void* v, const void
                          int64_t Nq, int64_t Nk, int64_t D, int causal, float scale, void* stream, int64_t ld = 0) {
   if (B < 0 || H < 0 || Nq < 0 || Nk < 0 || D <= 0) return ATTN_ERR_INVALID_ARG;
   if (!(scale > 0.f) || !std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
-  if (D > 128) return ATTN_ERR_UNSUPPORTED;
+  if (D > 256) return ATTN_ERR_UNSUPPORTED;
   if (ld == 0) {
     if (D % 8 != 0) return ATTN_ERR_UNSUPPORTED;  // contiguous rows must be 16-byte multiples (TMA)
     ld = D;
@@ -63,7 +67,8 @@ attn_status_t launch_bwd(const void* q, const void* k, const void* v, const void
   if (B > kI32 || H > kI32 || B * H > kI32 || Nq > kI32 - 256 || Nk > kI32 - 256) return ATTN_ERR_INVALID_ARG;
   const int64_t BH = B * H;
   const int64_t n_qtiles = (Nq + attn::BM - 1) / attn::BM, n_ktiles = (Nk + attn::BN - 1) / attn::BN;
-  if (BH > kI32 / (n_qtiles > n_ktiles ? n_qtiles : n_ktiles)) return ATTN_ERR_INVALID_ARG;
+  // Grids: n_qtiles * BH dQ CTAs, n_ktiles * BH (two per key tile at D > 128) dK/dV CTAs.
+  if (BH > kI32 / (n_qtiles > 2 * n_ktiles ? n_qtiles : 2 * n_ktiles)) return ATTN_ERR_INVALID_ARG;
   const int64_t Nmax = Nq > Nk ? Nq : Nk;
   if (BH > (int64_t(1) << 62) / (Nmax * ld * 2)) return ATTN_ERR_INVALID_ARG;
   const uint64_t qb = uint64_t(BH) * uint64_t(Nq) * uint64_t(ld) * 2u, kb = uint64_t(BH) * uint64_t(Nk) * uint64_t(ld) * 2u;
@@ -111,12 +116,22 @@ attn_status_t launch_bwd(const void* q, const void* k, const void* v, const void
   prm.scale = scale;
   prm.scale_log2 = scale * 1.4426950408889634f;
   prm.timeout_cycles = timeout_cycles();
+  // D > 128 (the D = 256 kernels): the dQ kernel loads K, V in 64-key boxes,
+  // the dK/dV kernel Q, dO in 32-query boxes.
+  attn::BwdParams prm_dq = prm, prm_dkv = prm;
+  if (D > 128 && (!encode_qkv_map(enc, &prm_dq.tk, k, D, Nk, BH, ld, attn::CfgDq<256>::BNK) ||
+                  !encode_qkv_map(enc, &prm_dq.tv, v, D, Nk, BH, ld, attn::CfgDq<256>::BNK) ||
+                  !encode_qkv_map(enc, &prm_dkv.tq, q, D, Nq, BH, ld, attn::CfgDkv<256>::SQ) ||
+                  !encode_qkv_map(enc, &prm_dkv.tdo, dout, D, Nq, BH, ld, attn::CfgDkv<256>::SQ)))
+    return ATTN_ERR_CUDA;
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t err;
-  if (D <= 64)  // padded to 64 or 128 as in the forward
-    err = causal ? launch_bwd_kernels<64, true>(prm, st) : launch_bwd_kernels<64, false>(prm, st);
+  if (D <= 64)  // padded to 64, 128 or 256 as in the forward
+    err = causal ? launch_bwd_kernels<64, true>(prm_dq, prm_dkv, st) : launch_bwd_kernels<64, false>(prm_dq, prm_dkv, st);
+  else if (D <= 128)
+    err = causal ? launch_bwd_kernels<128, true>(prm_dq, prm_dkv, st) : launch_bwd_kernels<128, false>(prm_dq, prm_dkv, st);
   else
-    err = causal ? launch_bwd_kernels<128, true>(prm, st) : launch_bwd_kernels<128, false>(prm, st);
+    err = causal ? launch_bwd_kernels<256, true>(prm_dq, prm_dkv, st) : launch_bwd_kernels<256, false>(prm_dq, prm_dkv, st);
   return err == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 

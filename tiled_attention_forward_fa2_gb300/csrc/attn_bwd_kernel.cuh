@@ -29,6 +29,17 @@
 
 namespace attn {
 
+// 64 consecutive columns of this thread's lane as two x32 loads and one wait.
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&r)[64]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%64];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, [%65];\n\t"
+      "tcgen05.wait::ld.sync.aligned;\n"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+      : "r"(taddr), "r"(taddr + 32u)
+      : "memory");
+}
+
 constexpr int kBwdThreads = 192;
 constexpr int kBwdLoadWarp = 4, kBwdMmaWarp = 5;
 
@@ -51,15 +62,20 @@ struct BwdParams {
 template <int D>
 struct CfgDq {
   static constexpr int KB = D / 64;
-  static constexpr uint32_t TILE = KB * kSubTile;
+  // Keys per step: 128, or 64 at D = 256, where S, dP and dQ (256 columns)
+  // must share TMEM's 512 columns and the K, V tiles shared memory with Q, dO.
+  static constexpr int BNK = D == 256 ? 64 : 128;
+  static constexpr uint32_t TILE = KB * kSubTile;               // Q, dO: 128 rows
+  static constexpr uint32_t KVSUB = uint32_t(BNK) * 128u;       // one 64-column box of a K or V tile
+  static constexpr uint32_t TILE_KV = KB * KVSUB;
   // Separate rings for K and V, sized to how long each tile is needed: K_j
   // until dQ_j (the end of step j), V_j only until dP_j.  Three K slots and two
   // V slots give every load a whole step of lead (one four-slot ring left the
-  // MMA warp waiting ~1760 cycles a step for K/V).
-  static constexpr int NK = D == 128 ? 3 : 5, NV = D == 128 ? 2 : 3;
+  // MMA warp waiting ~1760 cycles a step for K/V); at D = 256 two and one fit.
+  static constexpr int NK = D == 64 ? 5 : (D == 128 ? 3 : 2), NV = D == 64 ? 3 : (D == 128 ? 2 : 1);
   static constexpr int NSLOT = NK + NV;            // K slots, then V slots
   static constexpr uint32_t OFF_Q = 1024, OFF_DO = OFF_Q + TILE, OFF_KV = OFF_DO + TILE;
-  static constexpr uint32_t SMEM = OFF_KV + NSLOT * TILE + 1024;
+  static constexpr uint32_t SMEM = OFF_KV + NSLOT * TILE_KV + 1024;
   static_assert(SMEM <= 232448, "shared memory");
   // B_SF: S_j and dP_j in TMEM (MMA commit); B_DPR: dP_j in the elementwise
   // warps' registers (128 arrivals); B_DSF[j & 1]: dS_j in TMEM (128 arrivals).
@@ -68,14 +84,15 @@ struct CfgDq {
   // yet seen; dS_{j+2} needs S_{j+2}, which is only issued after that wait.
   static constexpr int B_Q = 0, B_FULL = 1, B_EMPTY = 1 + NSLOT, B_SF = 1 + 2 * NSLOT, B_DSF = B_SF + 1,
                        B_DPR = B_DSF + 2, B_QDONE = B_DPR + 1, B_DONE = B_QDONE + 1, NBAR = B_DONE + 1;
-  // S_j at COL_S + 128 (j & 1), dS_j (bf16) over its first 64 columns.
-  static constexpr uint32_t COL_S = 0, COL_DP = 256, COL_DQ = 384;
+  // S_j at COL_S + BNK (j & 1), dS_j (bf16) over its first BNK / 2 columns.
+  static constexpr uint32_t COL_S = 0, COL_DP = 2 * BNK, COL_DQ = D == 256 ? 256 : 384;
+  static_assert(COL_DP + BNK <= COL_DQ && COL_DQ + D <= kTmemCols, "TMEM columns");
 };
 
 template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dq_sm103(const __grid_constant__ BwdParams p) {
   using C = CfgDq<D>;
-  constexpr int KB = C::KB, NK = C::NK, NV = C::NV;
+  constexpr int KB = C::KB, NK = C::NK, NV = C::NV, BNK = C::BNK;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = sm103::smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -96,7 +113,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dq_sm103(const __grid
     bh = int(blockIdx.x / uint32_t(p.n_qtiles));
   }
   const int m0 = qt * BM;
-  const int nk = CAUSAL ? min(p.n_ktiles, (min(m0 + BM - 1, p.Nq - 1) + p.kv_off) / BN + 1) : p.n_ktiles;
+  const int n_kt = (p.Nk + BNK - 1) / BNK;
+  const int nk = CAUSAL ? min(n_kt, (min(m0 + BM - 1, p.Nq - 1) + p.kv_off) / BNK + 1) : n_kt;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::NBAR; ++i)
@@ -126,10 +144,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dq_sm103(const __grid
       auto load = [&](int j, bool is_k) -> bool {
         const int n = is_k ? NK : NV, s = (is_k ? 0 : NK) + j % n;
         if (j >= n && !wait_bounded(bar(C::B_EMPTY + s), uint32_t(j / n - 1) & 1u, ab)) return false;
-        sm103::mbar_arrive_expect_tx(bar(C::B_FULL + s), C::TILE);
+        sm103::mbar_arrive_expect_tx(bar(C::B_FULL + s), C::TILE_KV);
         for (int kb = 0; kb < KB; ++kb)
-          sm103::tma_load_3d(sKV + s * C::TILE + kb * kSubTile, is_k ? &p.tk : &p.tv, bar(C::B_FULL + s), kb * 64,
-                             j * BN, bh);
+          sm103::tma_load_3d(sKV + s * C::TILE_KV + kb * C::KVSUB, is_k ? &p.tk : &p.tv, bar(C::B_FULL + s), kb * 64,
+                             j * BNK, bh);
         return true;
       };
       for (int j = 0; ok && j < nk; ++j) {
@@ -144,33 +162,31 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dq_sm103(const __grid
     }
     __syncwarp();
   } else if (warp == kBwdMmaWarp) {
-    constexpr uint32_t kIdescS = sm103::idesc_bf16_f32(BM, BN, 0, 0);  // both operands K-major
-    constexpr uint32_t kIdescQ = sm103::idesc_bf16_f32(BM, D, 0, 1);   // dS from TMEM, K MN-major
+    constexpr uint32_t kIdescS = sm103::idesc_bf16_f32(BM, BNK, 0, 0);  // both operands K-major
+    constexpr uint32_t kIdescQ = sm103::idesc_bf16_f32(BM, D, 0, 1);    // dS from TMEM, K MN-major
     const uint64_t dq_k = sm103::sdesc_sw128(sQ, 16, 1024), ddo_k = sm103::sdesc_sw128(sDO, 16, 1024);
-    const uint64_t dkv_k = sm103::sdesc_sw128(sKV, 16, 1024), dkv_mn = sm103::sdesc_sw128(sKV, kSubTile, 1024);
+    const uint64_t dkv_k = sm103::sdesc_sw128(sKV, 16, 1024), dkv_mn = sm103::sdesc_sw128(sKV, C::KVSUB, 1024);
     // Ring slot of K_j (kv = 0) or V_j (kv = 1), its fill phase, and release.
     auto slot = [](int j, int kv) { return kv == 0 ? j % NK : NK + j % NV; };
-    auto slot_off = [&](int j, int kv) { return uint64_t(uint32_t(slot(j, kv)) * (C::TILE >> 4)); };
+    auto slot_off = [&](int j, int kv) { return uint64_t(uint32_t(slot(j, kv)) * (C::TILE_KV >> 4)); };
+    // 16 columns kk of D: in a 128-row tile (Q, dO) and in a K or V tile.
+    auto off_q = [](int kk) { return uint64_t((uint32_t(kk >> 2) * kSubTile + uint32_t(kk & 3) * 32u) >> 4); };
+    auto off_kv = [](int kk) { return uint64_t((uint32_t(kk >> 2) * C::KVSUB + uint32_t(kk & 3) * 32u) >> 4); };
     auto wait_full = [&](int j, int kv) {
       return warp_wait(bar(C::B_FULL + slot(j, kv)), uint32_t(j / (kv == 0 ? NK : NV)) & 1u, ab);
     };
     auto release = [&](int j, int kv) { sm103::mma_commit_warp(bar(C::B_EMPTY + slot(j, kv))); };
     auto issue_s = [&](int j) {  // S = Q K_j^T into buffer j & 1
       const uint64_t dk = dkv_k + slot_off(j, 0);
-      const uint32_t dS = tmem + C::COL_S + uint32_t(j & 1) * BN;
+      const uint32_t dS = tmem + C::COL_S + uint32_t(j & 1) * BNK;
 #pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        const uint64_t off = uint64_t((uint32_t(kk >> 2) * kSubTile + uint32_t(kk & 3) * 32u) >> 4);
-        sm103::mma_ss_warp(dS, dq_k + off, dk + off, kIdescS, kk > 0 ? 1u : 0u);
-      }
+      for (int kk = 0; kk < D / 16; ++kk) sm103::mma_ss_warp(dS, dq_k + off_q(kk), dk + off_kv(kk), kIdescS, kk > 0 ? 1u : 0u);
     };
     auto issue_dp = [&](int j) {  // dP = dO V_j^T; S_j and dP_j ready together
       const uint64_t dv = dkv_k + slot_off(j, 1);
 #pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        const uint64_t off = uint64_t((uint32_t(kk >> 2) * kSubTile + uint32_t(kk & 3) * 32u) >> 4);
-        sm103::mma_ss_warp(tmem + C::COL_DP, ddo_k + off, dv + off, kIdescS, kk > 0 ? 1u : 0u);
-      }
+      for (int kk = 0; kk < D / 16; ++kk)
+        sm103::mma_ss_warp(tmem + C::COL_DP, ddo_k + off_q(kk), dv + off_kv(kk), kIdescS, kk > 0 ? 1u : 0u);
       sm103::mma_commit_warp(bar(C::B_SF));
       release(j, 1);  // V_j is done with
     };
@@ -197,9 +213,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dq_sm103(const __grid
       if (!(ok = warp_wait(bar(C::B_DSF + (j & 1)), uint32_t(j >> 1) & 1u, ab))) break;
       sm103::tc_fence_after();
       const uint64_t dkmn = dkv_mn + slot_off(j, 0);
-      const uint32_t aS = tmem + C::COL_S + uint32_t(j & 1) * BN;
+      const uint32_t aS = tmem + C::COL_S + uint32_t(j & 1) * BNK;
 #pragma unroll
-      for (int kk = 0; kk < BN / 16; ++kk)  // dQ += dS K_j: 16 keys per MMA
+      for (int kk = 0; kk < BNK / 16; ++kk)  // dQ += dS K_j: 16 keys per MMA
         sm103::mma_ts_warp(tmem + C::COL_DQ, aS + kk * 8, dkmn + uint64_t(kk * (2048 >> 4)), kIdescQ,
                            (j > 0 || kk > 0) ? 1u : 0u);
       release(j, 0);  // K_j is done with
@@ -252,21 +268,24 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dq_sm103(const __grid
     for (int j = 0; j < nk; ++j) {
       if (!(ok = warp_wait(bar(C::B_SF), uint32_t(j) & 1u, ab))) break;
       sm103::tc_fence_after();
-      int lim = min(BN - 1, p.Nk - 1 - j * BN);
-      if (CAUSAL) lim = min(lim, row + p.kv_off - j * BN);
+      int lim = min(BNK - 1, p.Nk - 1 - j * BNK);
+      if (CAUSAL) lim = min(lim, row + p.kv_off - j * BNK);
       // dP_j - D into registers, then its TMEM columns go back to the MMA warp.
-      float dpd[BN];
+      float dpd[BNK];
       {
-        uint32_t ud[BN];
-        sm103::tmem_ld128(tmem + lane_off + C::COL_DP, ud);
+        uint32_t ud[BNK];
+        if constexpr (BNK == 128)
+          sm103::tmem_ld128(tmem + lane_off + C::COL_DP, ud);
+        else
+          tmem_ld64(tmem + lane_off + C::COL_DP, ud);
 #pragma unroll
-        for (int c = 0; c < BN; ++c) dpd[c] = __uint_as_float(ud[c]) - dlt;
+        for (int c = 0; c < BNK; ++c) dpd[c] = __uint_as_float(ud[c]) - dlt;
       }
       sm103::tc_fence_before();
       sm103::mbar_arrive(bar(C::B_DPR));
-      const uint32_t tS = tmem + lane_off + C::COL_S + uint32_t(j & 1) * BN;
+      const uint32_t tS = tmem + lane_off + C::COL_S + uint32_t(j & 1) * BNK;
 #pragma unroll
-      for (int q = 0; q < BN / 32; ++q) {
+      for (int q = 0; q < BNK / 32; ++q) {
         uint32_t us[32];
         sm103::tmem_ld32(tS + q * 32, us);
         uint32_t pk[16];
@@ -280,7 +299,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dq_sm103(const __grid
           const float p1 = c + 1 > lim ? 0.f : sm103::ex2_approx(t1);
           pk[e] = sm103::pack_bf16x2(p0 * dpd[c], p1 * dpd[c + 1]);
         }
-        sm103::tmem_st16(tS + q * 16, pk);  // dS over the first 64 columns of S_j
+        sm103::tmem_st16(tS + q * 16, pk);  // dS over the first BNK / 2 columns of S_j
       }
       sm103::tmem_st_wait();
       sm103::tc_fence_before();
@@ -327,27 +346,38 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dq_sm103(const __grid
 template <int D>
 struct CfgDkv {
   static constexpr int KB = D / 64;
-  static constexpr uint32_t TILE = KB * kSubTile;
+  // At D = 256 dK and dV (256 fp32 columns each) do not fit in TMEM together:
+  // each key tile is shared by two CTAs, each accumulating one 128-column half
+  // of dK and dV (both compute the whole S^T and dP^T); and with whole K and V
+  // tiles of 64 KB in shared memory, a stage holds 32 queries.
+  static constexpr int DACC = D == 256 ? 128 : D;          // dK, dV columns per CTA
+  static constexpr int NHALF = D / DACC;                   // CTAs per key tile
+  static constexpr int SQ = D == 256 ? 32 : 128;           // queries per stage
+  static constexpr int HQ = D == 256 ? 32 : 64;            // queries per sub-step
+  static constexpr int NSUB = SQ / HQ;                     // sub-steps per stage
+  static constexpr uint32_t TILE = KB * kSubTile;          // K, V: 128 rows
+  static constexpr uint32_t QSUB = uint32_t(SQ) * 128u;    // one 64-column box of a stage's Q or dO
+  static constexpr uint32_t STILE = KB * QSUB;
   static constexpr int NSTAGE = 2;                         // (Q_i, dO_i, LSE, D) stages
-  static constexpr uint32_t OFF_VEC = 1024;                // [NSTAGE][2][128] fp32: LSE*log2e, D
+  static constexpr uint32_t OFF_VEC = 1024;                // [NSTAGE][2][SQ] fp32: LSE*log2e, D
   static constexpr uint32_t OFF_K = 4096, OFF_V = OFF_K + TILE, OFF_ST = OFF_V + TILE;  // stage s: Q, dO
-  static constexpr uint32_t SMEM = OFF_ST + NSTAGE * 2 * TILE + 1024;
+  static constexpr uint32_t SMEM = OFF_ST + NSTAGE * 2 * STILE + 1024;
   static_assert(SMEM <= 232448, "shared memory");
-  static_assert(OFF_VEC + NSTAGE * 2 * 128 * 4 <= OFF_K, "vector area");
-  // Half steps h (64 queries): S^T and dP^T in buffer h & 1 (B_SF[h & 1], MMA
+  static_assert(OFF_VEC + NSTAGE * 2 * SQ * 4 <= OFF_K, "vector area");
+  // Sub-steps h (HQ queries): S^T and dP^T in buffer h & 1 (B_SF[h & 1], MMA
   // commit), P^T and dS^T written over them (B_PF[h & 1], 128 arrivals).
-  static constexpr int HQ = 64;                            // queries per half step
   static constexpr int B_KV = 0, B_SFULL = 1, B_SEMPTY = 1 + NSTAGE, B_SF = 1 + 2 * NSTAGE, B_PF = B_SF + 2,
                        B_ACC = B_PF + 2, B_DONE = B_ACC + 1, NBAR = B_DONE + 1;
-  // Buffer b: S^T at 128 b, dP^T at 128 b + 64 (64 columns each; P^T, dS^T
-  // bf16 over their first 32).
-  static constexpr uint32_t COL_S = 0, COL_DP = 64, COL_DV = 256, COL_DK = 256 + D;
+  // Buffer b: S^T at BUF b, dP^T at BUF b + HQ (HQ columns each; P^T, dS^T
+  // bf16 over their first HQ / 2).
+  static constexpr uint32_t COL_S = 0, COL_DP = HQ, BUF = 2 * HQ, COL_DV = 256, COL_DK = 256 + DACC;
+  static_assert(2 * BUF <= COL_DV && COL_DK + DACC <= kTmemCols, "TMEM columns");
 };
 
 template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dkdv_sm103(const __grid_constant__ BwdParams p) {
   using C = CfgDkv<D>;
-  constexpr int KB = C::KB, NSTAGE = C::NSTAGE;
+  constexpr int KB = C::KB, NSTAGE = C::NSTAGE, SQ = C::SQ, HQ = C::HQ, NSUB = C::NSUB, DACC = C::DACC;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = sm103::smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -359,19 +389,23 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dkdv_sm103(const __gr
   auto bar = [base](int i) { return base + 8u * uint32_t(i); };
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  // Causal: key tiles seen by the most queries (the first ones) go first.
+  // Causal: key tiles seen by the most queries (the first ones) go first.  The
+  // CTAs of one key tile's column halves are adjacent.
+  const int half = C::NHALF > 1 ? int(blockIdx.x % uint32_t(C::NHALF)) : 0;
+  const uint32_t tile = blockIdx.x / uint32_t(C::NHALF);
   int kt, bh;
   if (CAUSAL) {
-    kt = int(blockIdx.x / uint32_t(p.bh));
-    bh = int(blockIdx.x % uint32_t(p.bh));
+    kt = int(tile / uint32_t(p.bh));
+    bh = int(tile % uint32_t(p.bh));
   } else {
-    kt = int(blockIdx.x % uint32_t(p.n_ktiles));
-    bh = int(blockIdx.x / uint32_t(p.n_ktiles));
+    kt = int(tile % uint32_t(p.n_ktiles));
+    bh = int(tile / uint32_t(p.n_ktiles));
   }
   const int n0 = kt * BN;
-  // Query tiles with a query that sees one of these keys (query i sees key n iff n <= i + kv_off).
-  const int it0 = CAUSAL ? max(0, n0 - p.kv_off) / BM : 0;
-  const int niter = max(0, p.n_qtiles - it0);
+  // Query blocks (SQ queries, one stage each) with a query that sees one of
+  // these keys (query i sees key n iff n <= i + kv_off).
+  const int it0 = CAUSAL ? max(0, n0 - p.kv_off) / SQ : 0;
+  const int niter = max(0, (p.Nq + SQ - 1) / SQ - it0);
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::NBAR; ++i) {
@@ -407,31 +441,32 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dkdv_sm103(const __gr
     bool ok = true;
     for (int it = 0; ok && it < niter; ++it) {
       const int st = it % NSTAGE;
-      const int i0 = (it0 + it) * BM;
-      // Per-query LSE (base 2) and D for this tile (queries past Nq get P = 0),
+      const int i0 = (it0 + it) * SQ;
+      // Per-query LSE (base 2) and D for this block (queries past Nq get P = 0),
       // read before the stage is free so the loads overlap the wait; the tile
       // copies go out first once it is free.
-      float lse4[4], d4[4];
+      constexpr int NV4 = SQ / 32;  // values per lane
+      float lse4[NV4], d4[NV4];
 #pragma unroll
-      for (int x = 0; x < 4; ++x) {
-        const int i = i0 + lane * 4 + x;
+      for (int x = 0; x < NV4; ++x) {
+        const int i = i0 + lane * NV4 + x;
         const bool live = i < p.Nq;
         lse4[x] = live ? p.lse[size_t(bh) * p.Nq + i] * 1.4426950408889634f : INFINITY;
         d4[x] = live ? p.delta[size_t(bh) * p.Nq + i] : 0.f;
       }
       if (it >= NSTAGE && !(ok = warp_wait(bar(C::B_SEMPTY + st), uint32_t(it / NSTAGE - 1) & 1u, ab))) break;
       if (lane == 0) {
-        sm103::mbar_arrive_expect_tx(bar(C::B_SFULL + st), 2u * C::TILE);
-        const uint32_t sq = sST + uint32_t(st) * 2u * C::TILE, sdo = sq + C::TILE;
+        sm103::mbar_arrive_expect_tx(bar(C::B_SFULL + st), 2u * C::STILE);
+        const uint32_t sq = sST + uint32_t(st) * 2u * C::STILE, sdo = sq + C::STILE;
         for (int kb = 0; kb < KB; ++kb) {
-          sm103::tma_load_3d(sq + kb * kSubTile, &p.tq, bar(C::B_SFULL + st), kb * 64, i0, bh);
-          sm103::tma_load_3d(sdo + kb * kSubTile, &p.tdo, bar(C::B_SFULL + st), kb * 64, i0, bh);
+          sm103::tma_load_3d(sq + kb * C::QSUB, &p.tq, bar(C::B_SFULL + st), kb * 64, i0, bh);
+          sm103::tma_load_3d(sdo + kb * C::QSUB, &p.tdo, bar(C::B_SFULL + st), kb * 64, i0, bh);
         }
       }
 #pragma unroll
-      for (int x = 0; x < 4; ++x) {
-        vec[(st * 2 + 0) * BM + lane * 4 + x] = lse4[x];
-        vec[(st * 2 + 1) * BM + lane * 4 + x] = d4[x];
+      for (int x = 0; x < NV4; ++x) {
+        vec[(st * 2 + 0) * SQ + lane * NV4 + x] = lse4[x];
+        vec[(st * 2 + 1) * SQ + lane * NV4 + x] = d4[x];
       }
       sm103::mbar_arrive(bar(C::B_SFULL + st));  // releases this lane's vector stores
       ++issued;
@@ -444,41 +479,42 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dkdv_sm103(const __gr
     __syncwarp();
   } else if (warp == kBwdMmaWarp) {
     // ------------------------------------------------------------- MMA issue
-    constexpr uint32_t kIdescS = sm103::idesc_bf16_f32(BM, C::HQ, 0, 0);  // S^T, dP^T: both K-major
-    constexpr uint32_t kIdescA = sm103::idesc_bf16_f32(BM, D, 0, 1);      // P^T / dS^T from TMEM, B MN-major
+    constexpr uint32_t kIdescS = sm103::idesc_bf16_f32(BM, HQ, 0, 0);    // S^T, dP^T: both K-major
+    constexpr uint32_t kIdescA = sm103::idesc_bf16_f32(BM, DACC, 0, 1);  // P^T / dS^T from TMEM, B MN-major
     const uint64_t dk_k = sm103::sdesc_sw128(sK, 16, 1024), dv_k = sm103::sdesc_sw128(sV, 16, 1024);
-    const uint64_t dst_k = sm103::sdesc_sw128(sST, 16, 1024), dst_mn = sm103::sdesc_sw128(sST, kSubTile, 1024);
-    constexpr uint64_t kHalf = uint64_t((C::HQ * 128u) >> 4);  // 64 rows of a 128-byte-row tile
-    // S^T and dP^T of half step h into buffer h & 1.
+    const uint64_t dst_k = sm103::sdesc_sw128(sST, 16, 1024), dst_mn = sm103::sdesc_sw128(sST, C::QSUB, 1024);
+    constexpr uint64_t kSub = uint64_t((HQ * 128u) >> 4);  // HQ rows of a stage tile
+    // This CTA's columns of dO and Q (the B operands of dV and dK).
+    const uint64_t half_off = uint64_t((uint32_t(half) * uint32_t(DACC / 64) * C::QSUB) >> 4);
+    // 16 columns kk of D: in a K or V tile and in a stage's Q or dO.
+    auto off_kv = [](int kk) { return uint64_t((uint32_t(kk >> 2) * kSubTile + uint32_t(kk & 3) * 32u) >> 4); };
+    auto off_st = [](int kk) { return uint64_t((uint32_t(kk >> 2) * C::QSUB + uint32_t(kk & 3) * 32u) >> 4); };
+    // S^T and dP^T of sub-step h into buffer h & 1.
     auto issue_s = [&](int h) {
-      const int it = h >> 1, st = it % NSTAGE;
-      const uint64_t soff = uint64_t(uint32_t(st) * 2u * (C::TILE >> 4)) + uint64_t(h & 1) * kHalf;
-      const uint64_t q_k = dst_k + soff, do_k = dst_k + soff + (C::TILE >> 4);
-      const uint32_t buf = tmem + uint32_t(h & 1) * 128u;
+      const int it = h / NSUB, st = it % NSTAGE;
+      const uint64_t soff = uint64_t(uint32_t(st) * 2u * (C::STILE >> 4)) + uint64_t(h % NSUB) * kSub;
+      const uint64_t q_k = dst_k + soff, do_k = dst_k + soff + (C::STILE >> 4);
+      const uint32_t buf = tmem + uint32_t(h & 1) * C::BUF;
 #pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {  // S^T = K Q^T
-        const uint64_t off = uint64_t((uint32_t(kk >> 2) * kSubTile + uint32_t(kk & 3) * 32u) >> 4);
-        sm103::mma_ss_warp(buf + C::COL_S, dk_k + off, q_k + off, kIdescS, kk > 0 ? 1u : 0u);
-      }
+      for (int kk = 0; kk < D / 16; ++kk)  // S^T = K Q^T
+        sm103::mma_ss_warp(buf + C::COL_S, dk_k + off_kv(kk), q_k + off_st(kk), kIdescS, kk > 0 ? 1u : 0u);
 #pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {  // dP^T = V dO^T
-        const uint64_t off = uint64_t((uint32_t(kk >> 2) * kSubTile + uint32_t(kk & 3) * 32u) >> 4);
-        sm103::mma_ss_warp(buf + C::COL_DP, dv_k + off, do_k + off, kIdescS, kk > 0 ? 1u : 0u);
-      }
+      for (int kk = 0; kk < D / 16; ++kk)  // dP^T = V dO^T
+        sm103::mma_ss_warp(buf + C::COL_DP, dv_k + off_kv(kk), do_k + off_st(kk), kIdescS, kk > 0 ? 1u : 0u);
       sm103::mma_commit_warp(bar(C::B_SF + (h & 1)));
     };
-    const int nh = 2 * niter;
+    const int nh = NSUB * niter;
     bool ok = warp_wait(bar(C::B_KV), 0u, ab) && (nh == 0 || warp_wait(bar(C::B_SFULL), 0u, ab));
     if (ok && nh > 0) {
       sm103::tc_fence_after();
       issue_s(0);
     }
     for (int h = 0; ok && h < nh; ++h) {
-      const int it = h >> 1, st = it % NSTAGE;
+      const int it = h / NSUB, st = it % NSTAGE;
       if (h + 1 < nh) {
-        // The other buffer's P^T, dS^T (half step h - 1) were read by MMAs issued before.
-        if (((h + 1) & 1) == 0) {
-          const int it1 = (h + 1) >> 1;
+        // The other buffer's P^T, dS^T (sub-step h - 1) were read by MMAs issued before.
+        if ((h + 1) % NSUB == 0) {
+          const int it1 = (h + 1) / NSUB;
           if (!(ok = warp_wait(bar(C::B_SFULL + it1 % NSTAGE), uint32_t(it1 / NSTAGE) & 1u, ab))) break;
           sm103::tc_fence_after();
         }
@@ -486,16 +522,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dkdv_sm103(const __gr
       }
       if (!(ok = warp_wait(bar(C::B_PF + (h & 1)), uint32_t(h >> 1) & 1u, ab))) break;
       sm103::tc_fence_after();
-      const uint64_t soff = uint64_t(uint32_t(st) * 2u * (C::TILE >> 4)) + uint64_t(h & 1) * kHalf;
-      const uint64_t q_mn = dst_mn + soff, do_mn = dst_mn + soff + (C::TILE >> 4);
-      const uint32_t buf = tmem + uint32_t(h & 1) * 128u;
+      const uint64_t soff = uint64_t(uint32_t(st) * 2u * (C::STILE >> 4)) + uint64_t(h % NSUB) * kSub + half_off;
+      const uint64_t q_mn = dst_mn + soff, do_mn = dst_mn + soff + (C::STILE >> 4);
+      const uint32_t buf = tmem + uint32_t(h & 1) * C::BUF;
 #pragma unroll
-      for (int kk = 0; kk < C::HQ / 16; ++kk) {  // dV += P^T dO, dK += dS^T Q: 16 queries per MMA
+      for (int kk = 0; kk < HQ / 16; ++kk) {  // dV += P^T dO, dK += dS^T Q: 16 queries per MMA
         const uint64_t off = uint64_t(kk * (2048 >> 4));
         sm103::mma_ts_warp(tmem + C::COL_DV, buf + C::COL_S + kk * 8, do_mn + off, kIdescA, (h > 0 || kk > 0) ? 1u : 0u);
         sm103::mma_ts_warp(tmem + C::COL_DK, buf + C::COL_DP + kk * 8, q_mn + off, kIdescA, (h > 0 || kk > 0) ? 1u : 0u);
       }
-      if (h & 1) sm103::mma_commit_warp(bar(C::B_SEMPTY + st));  // both halves of the stage are done with
+      if (h % NSUB == NSUB - 1) sm103::mma_commit_warp(bar(C::B_SEMPTY + st));  // the stage is done with
     }
     sm103::mma_commit_warp(bar(C::B_ACC));
     sm103::mma_commit_warp(bar(C::B_DONE));
@@ -509,25 +545,28 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dkdv_sm103(const __gr
     const uint64_t sl2x2 = sm103::f2_pack(p.scale_log2, p.scale_log2);
     const bool key_live = n < p.Nk;
     bool ok = true;
-    for (int h = 0; h < 2 * niter; ++h) {
-      const int it = h >> 1, st = it % NSTAGE, hf = h & 1;
+    for (int h = 0; h < NSUB * niter; ++h) {
+      const int it = h / NSUB, st = it % NSTAGE, hf = h & 1, sub = h % NSUB;
       if (!(ok = warp_wait(bar(C::B_SF + hf), uint32_t(h >> 1) & 1u, ab))) break;
       // The stage's LSE and D vectors were written by the producer lanes: wait on
       // their barrier directly (already complete) to acquire those stores.
       if (!(ok = warp_wait(bar(C::B_SFULL + st), uint32_t(it / NSTAGE) & 1u, ab))) break;
       sm103::tc_fence_after();
-      const int i0 = (it0 + it) * BM + hf * C::HQ;
+      const int i0 = (it0 + it) * SQ + sub * HQ;
       // query column c sees this key iff n <= i0 + c + kv_off, i.e. c >= n - kv_off - i0
-      const int cmin = key_live ? (CAUSAL ? n - p.kv_off - i0 : 0) : C::HQ;
-      const float2* lv = reinterpret_cast<const float2*>(vec + (st * 2 + 0) * BM + hf * C::HQ);
-      const float2* dv = reinterpret_cast<const float2*>(vec + (st * 2 + 1) * BM + hf * C::HQ);
-      const uint32_t tS = tmem + lane_off + uint32_t(hf) * 128u + C::COL_S, tDP = tS + (C::COL_DP - C::COL_S);
-      // S^T and dP^T are adjacent: one load of 128 columns, one wait.
-      static_assert(C::COL_DP == C::COL_S + C::HQ && 2 * C::HQ == 128, "S^T, dP^T adjacent");
-      uint32_t u[128];
-      sm103::tmem_ld128(tS, u);
+      const int cmin = key_live ? (CAUSAL ? n - p.kv_off - i0 : 0) : HQ;
+      const float2* lv = reinterpret_cast<const float2*>(vec + (st * 2 + 0) * SQ + sub * HQ);
+      const float2* dv = reinterpret_cast<const float2*>(vec + (st * 2 + 1) * SQ + sub * HQ);
+      const uint32_t tS = tmem + lane_off + uint32_t(hf) * C::BUF + C::COL_S, tDP = tS + (C::COL_DP - C::COL_S);
+      // S^T and dP^T are adjacent: one load of 2 HQ columns, one wait.
+      static_assert(C::COL_DP == C::COL_S + HQ, "S^T, dP^T adjacent");
+      uint32_t u[2 * HQ];
+      if constexpr (HQ == 64)
+        sm103::tmem_ld128(tS, u);
+      else
+        tmem_ld64(tS, u);
 #pragma unroll
-      for (int q = 0; q < C::HQ / 32; ++q) {
+      for (int q = 0; q < HQ / 32; ++q) {
         uint32_t pp[16], pd[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
@@ -540,8 +579,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dkdv_sm103(const __gr
           const float p0 = c < cmin ? 0.f : sm103::ex2_approx(t0);
           const float p1 = c + 1 < cmin ? 0.f : sm103::ex2_approx(t1);
           pp[e] = sm103::pack_bf16x2(p0, p1);
-          pd[e] = sm103::pack_bf16x2(p0 * (__uint_as_float(u[C::HQ + c]) - d2.x),
-                                     p1 * (__uint_as_float(u[C::HQ + c + 1]) - d2.y));
+          pd[e] = sm103::pack_bf16x2(p0 * (__uint_as_float(u[HQ + c]) - d2.x),
+                                     p1 * (__uint_as_float(u[HQ + c + 1]) - d2.y));
         }
         sm103::tmem_st16(tS + q * 16, pp);   // P^T over S^T (its first 32 columns)
         sm103::tmem_st16(tDP + q * 16, pd);  // dS^T over dP^T
@@ -560,7 +599,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dkdv_sm103(const __gr
         const uint32_t stage = w == 0 ? sV : sK;
         const float mul = w == 0 ? 1.f : p.scale;
 #pragma unroll
-        for (int q = 0; q < D / 32; ++q) {
+        for (int q = 0; q < DACC / 32; ++q) {
           uint32_t v[32];
           sm103::tmem_ld32(tmem + lane_off + col0 + q * 32, v);
           uint32_t pk[16];
@@ -580,9 +619,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dkdv_sm103(const __gr
     }
     ok = sm103::named_bar_and(1, BM, ok);
     if (ok && r == 0) {
-      for (int kb = 0; kb < KB; ++kb) {
-        sm103::tma_store_3d(&p.tdv, sV + kb * kSubTile, kb * 64, n0, bh);
-        sm103::tma_store_3d(&p.tdk, sK + kb * kSubTile, kb * 64, n0, bh);
+      for (int kb = 0; kb < DACC / 64; ++kb) {
+        sm103::tma_store_3d(&p.tdv, sV + kb * kSubTile, half * DACC + kb * 64, n0, bh);
+        sm103::tma_store_3d(&p.tdk, sK + kb * kSubTile, half * DACC + kb * 64, n0, bh);
       }
       sm103::bulk_commit();
       sm103::bulk_wait_read0();

@@ -38,14 +38,14 @@ EncodeTiledFn encode_fn() {
 }
 
 // [B*H, N, D] bf16 with rows ld elements apart (ld = D when contiguous) viewed
-// as a 3-D tensor {D, N, B*H}; boxes of 64 x 128 x 1 (64 bf16 = one 128-byte
+// as a 3-D tensor {D, N, B*H}; boxes of 64 x box_rows x 1 (64 bf16 = one 128-byte
 // swizzle span); columns past D and rows past N read as zero and are never written.
 bool encode_qkv_map(EncodeTiledFn enc, CUtensorMap* map, const void* ptr, int64_t D, int64_t N, int64_t BH,
-                    int64_t ld = 0) {
+                    int64_t ld = 0, uint32_t box_rows = 128) {
   if (ld == 0) ld = D;
   const cuuint64_t dims[3] = {cuuint64_t(D), cuuint64_t(N), cuuint64_t(BH)};
   const cuuint64_t strides[2] = {cuuint64_t(ld) * 2u, cuuint64_t(N) * cuuint64_t(ld) * 2u};
-  const cuuint32_t box[3] = {64u, 128u, 1u};
+  const cuuint32_t box[3] = {64u, box_rows, 1u};
   const cuuint32_t estride[3] = {1u, 1u, 1u};
   return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estride,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
