@@ -261,7 +261,10 @@ attn_status_t attn_last_status(void* stream);
  *                     rows) per unit; 2 = two tiles of one head sharing every
  *                     K/V tile; 3 = key split, one tile whose key tiles are
  *                     shared out between the CTA's two softmax warpgroups and
- *                     merged at the end (head dims up to 64; above, 3 means 1).
+ *                     merged at the end (head dims up to 64; above, 3 means 1);
+ *                     4 = one tile per unit on the short-unit kernel, two CTAs
+ *                     per SM each with half of its resources (head dims up to
+ *                     64, where it ignores `grid`; above, 4 means 1).
  *                     Head dims above 128 always run one tile per unit.
  * grid              : 1 = one CTA per unit; 2 = persistent (one CTA per SM,
  *                     each walking many units).  Head dims above 128 always

@@ -67,7 +67,8 @@ def test_unit_count_stays_in_int32(lib):
 
 
 def test_tuning_overrides_validate(lib):
-    assert pkg.attn_set_tuning(4, 0, 0, 0) == pkg.ATTN_ERR_INVALID_ARG
+    assert pkg.attn_set_tuning(5, 0, 0, 0) == pkg.ATTN_ERR_INVALID_ARG
+    assert pkg.attn_set_tuning(4, 0, 0, 0) == pkg.ATTN_OK
     assert pkg.attn_set_tuning(-1, 0, 0, 0) == pkg.ATTN_ERR_INVALID_ARG
     assert pkg.attn_set_tuning(3, 0, 0, 0) == pkg.ATTN_OK
     assert pkg.attn_set_tuning(0, 3, 0, 0) == pkg.ATTN_ERR_INVALID_ARG

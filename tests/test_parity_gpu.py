@@ -76,11 +76,12 @@ def test_full_size_every_row(name):
         del o, lse
 
 
-@pytest.fixture(params=[1, 2, 3], ids=["one_tile_per_cta", "two_tiles_per_cta", "key_split"])
+@pytest.fixture(params=[1, 2, 3, 4], ids=["one_tile_per_cta", "two_tiles_per_cta", "key_split", "short_kernel"])
 def tiles_per_cta(request):
     """Force the launcher's choice of work unit (normally picked from the grid size): one or
-    two query tiles, or one tile with its key tiles split over both softmax warpgroups
-    (D <= 64; at larger head dims the request runs as one tile per unit)."""
+    two query tiles, one tile with its key tiles split over both softmax warpgroups, or one
+    tile on the short-unit kernel that runs two CTAs per SM (the last two D <= 64; at larger
+    head dims the request runs as one tile per unit)."""
     tune(unit=request.param)
     yield request.param
     tune(unit=0)
@@ -130,6 +131,23 @@ def test_many_units_per_cta(N, D, causal, tiles_per_cta):
         full_check(q, k, v, causal, 1.0 / math.sqrt(D), f"N={N} D={D} causal={causal} T={tiles_per_cta} persistent")
     finally:
         tune(grid=0)
+
+
+@pytest.mark.parametrize("D", [8, 40, 64])
+@pytest.mark.parametrize("Nq,Nk,causal", [(1, 700, True), (200, 1000, True), (333, 333, True), (640, 200, False),
+                                          (1000, 1000, False)])
+def test_short_kernel_lengths(Nq, Nk, causal, D):
+    """The short-unit kernel (two CTAs per SM, one tile per unit) on queries and keys of
+    different lengths, head dims padded to 64, several units per CTA."""
+    tune(unit=4)
+    try:
+        q = make_qkv(3, 70, Nq, D, seed=950 + Nq + D)[0]
+        _, k, v = make_qkv(3, 70, Nk, D, seed=951 + Nk + D)
+        o, lse = run_qk(q, k, v, causal, 1.0 / math.sqrt(D))
+    finally:
+        tune(unit=0)
+    o_ref, lse_ref = oracle.attn_fwd(q, k, v, causal, 1.0 / math.sqrt(D))
+    assert_close(o, lse, o_ref, lse_ref, f"short kernel Nq={Nq} Nk={Nk} D={D} causal={causal}")
 
 
 def test_identical_keys_give_mean_of_v():

@@ -11,6 +11,7 @@
 
 #include "attn.h"
 #include "attn_fwd_kernel.cuh"
+#include "attn_fwd_short_kernel.cuh"
 #ifdef ATTN_TEST_HOOKS
 #include "attn_test_hooks.h"
 #endif
@@ -68,6 +69,9 @@ cudaError_t opt_in_smem() {
     e = cudaFuncSetAttribute(attn::attn_fwd_sm103<64, CAUSAL, true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              int(attn::Cfg<64>::SMEM));
     if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(attn::attn_fwd_short_sm103<CAUSAL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             int(attn::CfgShort::SMEM));
+    if (e != cudaSuccess) return e;
   }
   if constexpr (attn::Cfg<D>::STAGE_IN_Q) return cudaSuccess;  // one-unit grid only
   else
@@ -117,7 +121,7 @@ constexpr int64_t kPersistMaxKeyTiles = 32;
 
 // Process-wide overrides set by attn_set_tuning (0 = the launcher's own choice).
 // Read once per call with relaxed loads: a call sees either the old or the new value.
-std::atomic<int> g_tune_unit{0};          // 1 or 2 query tiles per unit, 3 key split
+std::atomic<int> g_tune_unit{0};          // 1 or 2 query tiles per unit, 3 key split, 4 short kernel
 std::atomic<int> g_tune_grid{0};          // 1 one CTA per unit, 2 persistent
 std::atomic<int> g_tune_chunks{0};        // chunks of heads in attn_fwd_from_host
 constexpr int kPipeChunksMax = 32;        // chunks at most (events held per device)
@@ -134,8 +138,14 @@ long long timeout_cycles() {
 }
 
 template <int D, bool CAUSAL>
-cudaError_t launch(const attn::FwdParams& prm, int64_t ctas, bool persist, bool split, cudaStream_t stream) {
+cudaError_t launch(const attn::FwdParams& prm, int64_t ctas, bool persist, bool split, cudaStream_t stream,
+                   bool shortk = false) {
   if constexpr (D == 64) {
+    if (shortk) {  // two CTAs per SM, each walking single-tile units
+      attn::attn_fwd_short_sm103<CAUSAL><<<dim3(unsigned(ctas)), dim3(attn::kShortThreads), attn::CfgShort::SMEM,
+                                           stream>>>(prm);
+      return cudaGetLastError();
+    }
     if (split) {  // the key-split kernel walks its units like the persistent one
       attn::attn_fwd_sm103<64, CAUSAL, true, true><<<dim3(unsigned(ctas)), dim3(attn::kThreads), attn::Cfg<64>::SMEM,
                                                      stream>>>(prm);
@@ -226,11 +236,22 @@ attn_status_t launch_fwd(const void* q, const void* k, const void* v, void* o, f
   // time is one unit's chain; b2h8n1024d64: 128 tiles on 152 SMs).  Beyond a
   // wave its extra per-unit cost (Q load, merge) loses to two tiles per unit.
   bool split = D <= 64 && n_ktiles >= 2 && n_qtiles * BH <= sms;
+  // Short-unit kernel (D <= 64, two CTAs per SM, one tile per unit): causal
+  // problems of short rows, where the two tiles of a unit differ in length
+  // and unit boundaries come every few key steps, with at least a full wave
+  // of its grid.  Measured (CUDA events, L2 flushed, mean of 150): causal
+  // b16h32n512d64 46.1 against 54.9 us, b32h32n256d64 37.7 against 44.5,
+  // b8h16n1024d64 37.6 against 40.5, b4h32n2048d64 97.9 against 99.5; it lost
+  // on full rows (b16h32n512d64 54.0 against 51.9), on a short query block
+  // against 4096 keys and below a wave (b2h8n1024d64 causal 17.3 against 16.7).
+  bool shortk = D <= 64 && causal && n_ktiles <= 16 && n_qtiles >= 2 && n_qtiles * BH >= 2 * sms;
+  if (shortk) split = false;
   if (const int u = g_tune_unit.load(std::memory_order_relaxed)) {
-    T = u == 3 ? 1 : u;
+    T = u >= 3 ? 1 : u;
     split = u == 3 && D <= 64;
+    shortk = u == 4 && D <= 64;
   }
-  if (split) T = 1;
+  if (split || shortk) T = 1;
   if (D > 128) T = 1;  // the D = 256 kernel holds one query tile (TMEM)
   prm.lse = lse;
   prm.Nq = int(Nq);
@@ -279,14 +300,19 @@ attn_status_t launch_fwd(const void* q, const void* k, const void* v, void* o, f
   bool persist = D <= 64 || n_ktiles <= kPersistMaxKeyTiles;
   if (const int g = g_tune_grid.load(std::memory_order_relaxed)) persist = g == 2;
   if (D > 128) persist = false;  // the D = 256 kernel stages O in its Q buffer
-  const int64_t ctas = persist && prm.n_work > sms ? sms : prm.n_work;
+  int64_t ctas = persist && prm.n_work > sms ? sms : prm.n_work;
+  if (shortk) {
+    ctas = prm.n_work > 2 * sms ? 2 * sms : prm.n_work;  // two CTAs per SM
+    if (!encode_qkv_map(enc, &prm.to32, o, D, Nq, BH, ld, 32)) return ATTN_ERR_CUDA;
+  }
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t err;
   // Head dims below 64, 128 or 256 run on that kernel: the tensor maps carry the true
   // D, so TMA fills the missing columns with zeros on load (they add nothing to
   // Q K^T, and P V gives zeros there) and leaves them out on store.
   if (D <= 64)
-    err = causal ? launch<64, true>(prm, ctas, persist, split, st) : launch<64, false>(prm, ctas, persist, split, st);
+    err = causal ? launch<64, true>(prm, ctas, persist, split, st, shortk)
+                 : launch<64, false>(prm, ctas, persist, split, st, shortk);
   else if (D <= 128)
     err = causal ? launch<128, true>(prm, ctas, persist, false, st) : launch<128, false>(prm, ctas, persist, false, st);
   else
@@ -332,7 +358,7 @@ attn_status_t attn_last_status(void* stream) {
 }
 
 attn_status_t attn_set_tuning(int unit, int grid, int pipe_chunks, int64_t wait_limit_cycles) {
-  if (unit < 0 || unit > 3 || grid < 0 || grid > 2 || pipe_chunks < 0 || pipe_chunks > kPipeChunksMax ||
+  if (unit < 0 || unit > 4 || grid < 0 || grid > 2 || pipe_chunks < 0 || pipe_chunks > kPipeChunksMax ||
       wait_limit_cycles < 0)
     return ATTN_ERR_INVALID_ARG;
   g_tune_unit.store(unit, std::memory_order_relaxed);

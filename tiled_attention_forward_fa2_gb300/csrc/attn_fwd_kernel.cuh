@@ -81,6 +81,7 @@ struct FwdParams {
   int lpt;                     // causal: heads per band, heaviest units first within each band (0: a head's units adjacent)
   float scale_log2;            // scale * log2(e)
   long long timeout_cycles;
+  CUtensorMap to32;            // O with 32-row boxes (the short-unit kernel's per-warp stores)
 #ifdef ATTN_TEST_HOOKS
   int withhold_kv;             // test build only: nonzero -> no K/V loads are issued, so the pipeline waits run out
 #endif
