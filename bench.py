@@ -43,7 +43,7 @@ _CSRC = "tiled_attention_forward_fa2_gb300/csrc/"
 # Sources that decide what each kernel family runs (kernel, launcher, PTX helpers);
 # an ncu summary's traffic figure is used only while these are unchanged.
 KERNEL_SOURCES = {
-    "fwd": [_CSRC + f for f in ("attn_fwd_kernel.cuh", "sm103_ptx.cuh", "attn_fwd.cu")],
+    "fwd": [_CSRC + f for f in ("attn_fwd_kernel.cuh", "attn_fwd_short_kernel.cuh", "sm103_ptx.cuh", "attn_fwd.cu")],
     "based": [_CSRC + f for f in ("based_fwd_kernel.cuh", "based_fwd_host.cuh", "sm103_ptx.cuh")],
     "bwd": [_CSRC + f for f in ("attn_bwd_kernel.cuh", "attn_bwd_host.cuh", "sm103_ptx.cuh")],
 }
@@ -666,7 +666,8 @@ def run_ours(args, w):
                          "peak_source": f"bf16_tflops (burst) of {peak_src}"})
     peak = float(peaks["bf16_tflops"])
     achieved = flops / (ms_per_step * 1e-3) / 1e12
-    traffic = ncu_traffic(w.name)
+    kernel = pkg.attn_fwd_kernel_name(w.B, w.H, w.N, w.n_keys, w.D, w.causal)
+    traffic = ncu_traffic(w.name, kernel.split("<")[0])
     # Below the ridge point (peak FLOP/s over HBM bytes/s) the kernel is bound by
     # HBM bandwidth: algorithmic bytes = Q, K, V read + O written (bf16) + LSE (fp32).
     alg_bytes = 2.0 * w.B * w.H * w.D * (2 * w.N + 2 * w.n_keys) + 4.0 * w.B * w.H * w.N
@@ -681,10 +682,7 @@ def run_ours(args, w):
     roofline["traffic"] = traffic
     roofline["algorithmic_bytes"] = alg_bytes
     roofline["flop_per_byte"] = flops / alg_bytes
-    # The launcher's grid rule: persistent at D <= 64, and up to 32 key tiles at D <= 128.
-    persist = w.D <= 64 or ((w.n_keys + 127) // 128 <= 32 and w.D <= 128)
-    dk = 64 if w.D <= 64 else (128 if w.D <= 128 else 256)
-    roofline["kernel"] = f"attn_fwd_sm103<{dk},{str(w.causal).lower()},{'persistent' if persist else 'one unit per CTA'}>"
+    roofline["kernel"] = kernel
     cpu, parity = None, None
     if not args.no_cpu_baseline:
         # The oracle on the whole workload: its wall time is the CPU baseline and

@@ -281,6 +281,17 @@ attn_status_t attn_last_status(void* stream);
  */
 attn_status_t attn_set_tuning(int unit, int grid, int pipe_chunks, int64_t wait_limit_cycles);
 
+/*
+ * attn_fwd_kernel_name -- the kernel instance attn_fwd_qk would launch for a
+ * problem of these sizes on the current device with the current tuning, e.g.
+ * "attn_fwd_sm103<128,full,persistent,2 tiles/unit>" or
+ * "attn_fwd_short_sm103<causal>" (for diagnostics, benchmarks and profiles).
+ * The string lives in thread-local storage until this thread's next call.
+ * NULL for sizes attn_fwd_qk would reject (non-positive, D > 256, too large)
+ * or when the device cannot be prepared.
+ */
+const char* attn_fwd_kernel_name(int64_t B, int64_t H, int64_t Nq, int64_t Nk, int64_t D, int causal);
+
 /* attn_status_string -- static, human-readable name of a status code. */
 const char* attn_status_string(attn_status_t status);
 

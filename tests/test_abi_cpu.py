@@ -278,3 +278,11 @@ def test_padded_rows_validation(lib):
         assert bwd(100, 104) == pkg.ATTN_ERR_CUDA
         assert bwd(4, 8) == pkg.ATTN_ERR_CUDA
         assert bwd(250, 256) == pkg.ATTN_ERR_CUDA
+
+
+def test_kernel_name_rejects_what_the_forward_rejects(lib):
+    import torch
+    for args in ((0, 1, 128, 128, 64, 0), (1, 1, 128, 128, 264, 1), (1, 1, -5, 128, 64, 0), (1, 1, 128, 0, 64, 0)):
+        assert pkg.attn_fwd_kernel_name(*args) is None, args
+    if not torch.cuda.is_available():
+        assert pkg.attn_fwd_kernel_name(1, 1, 128, 128, 64, 0) is None  # no device to plan for

@@ -150,6 +150,21 @@ def test_short_kernel_lengths(Nq, Nk, causal, D):
     assert_close(o, lse, o_ref, lse_ref, f"short kernel Nq={Nq} Nk={Nk} D={D} causal={causal}")
 
 
+def test_kernel_names_follow_the_launcher():
+    """attn_fwd_kernel_name reports the launcher's choice, tuning included."""
+    name = pkg.attn_fwd_kernel_name
+    assert name(4, 16, 4096, 4096, 128, False) == "attn_fwd_sm103<128,full,persistent,2 tiles/unit>"
+    assert name(1, 16, 16384, 16384, 128, True) == "attn_fwd_sm103<128,causal,one unit per CTA,2 tiles/unit>"
+    assert name(16, 32, 512, 512, 64, True) == "attn_fwd_short_sm103<causal>"
+    assert name(2, 8, 1024, 1024, 64, False) == "attn_fwd_sm103<64,full,persistent,key split>"
+    assert name(1, 2, 300, 300, 200, True).startswith("attn_fwd_sm103<256,causal,one unit per CTA,1 tile/unit")
+    tune(unit=1, grid=1)
+    try:
+        assert name(16, 32, 512, 512, 64, True) == "attn_fwd_sm103<64,causal,one unit per CTA,1 tile/unit>"
+    finally:
+        tune(unit=0, grid=0)
+
+
 def test_identical_keys_give_mean_of_v():
     B, H, N, D = 1, 2, 300, 128
     q, k, v = make_qkv(B, H, N, D, seed=78)

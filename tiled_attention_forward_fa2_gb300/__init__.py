@@ -24,6 +24,7 @@ from ._binding import (  # noqa: F401
     attn_fwd_flops,
     attn_fwd_from_host,
     attn_fwd_from_host_static,
+    attn_fwd_kernel_name,
     attn_fwd_ld,
     attn_fwd_qk,
     attn_fwd_qk_flops,

@@ -40,6 +40,7 @@ def load(path: str) -> ctypes.CDLL:
         "attn_bwd_qk_flops": ([I64, I64, I64, I64, I64, I], ctypes.c_double),
         "attn_fwd_from_host": ([P] * 10 + [I64, I64, I64, I64, I64, I, ctypes.c_float, P], I),
         "attn_fwd_from_host_static": ([P] * 5 + [I64, I64, I64, I64, I64, I, ctypes.c_float, P], I),
+        "attn_fwd_kernel_name": ([I64, I64, I64, I64, I64, I], ctypes.c_char_p),
         "attn_fwd_ld": ([P, P, P, P, P, I64, I64, I64, I64, I64, I64, I, ctypes.c_float, P], I),
         "attn_bwd_ld": ([P] * 10 + [I64, I64, I64, I64, I64, I64, I, ctypes.c_float, P], I),
         "attn_based_fwd": ([P, P, P, P, P, I64, I64, I64, I64, I64, ctypes.c_float, P], I),
@@ -146,6 +147,12 @@ def attn_fwd_from_host_static(q_host, k_host, v_host, o_host, lse_host, B: int, 
     a = [_addr(x) for x in (q_host, k_host, v_host, o_host, lse_host)]
     return library().attn_fwd_from_host_static(*a, int(B), int(H), int(Nq), int(Nk), int(D), int(bool(causal)),
                                                float(scale), _stream(stream))
+
+
+def attn_fwd_kernel_name(B: int, H: int, Nq: int, Nk: int, D: int, causal: bool):
+    """The kernel instance ``attn_fwd_qk`` would launch for these sizes (None if it would reject them)."""
+    name = library().attn_fwd_kernel_name(int(B), int(H), int(Nq), int(Nk), int(D), int(bool(causal)))
+    return None if name is None else name.decode()
 
 
 def attn_based_fwd(q, k, v, y, z, B: int, H: int, N: int, F: int, D: int, scale: float, stream) -> int:

@@ -7,6 +7,7 @@
 #include <atomic>
 #include <cmath>
 #include <cstdint>
+#include <cstdio>
 #include <mutex>
 
 #include "attn.h"
@@ -163,6 +164,95 @@ cudaError_t launch(const attn::FwdParams& prm, int64_t ctas, bool persist, bool 
   return cudaGetLastError();
 }
 
+// The launcher's choices for one problem: query tiles per unit, key split,
+// short-unit kernel, grid, causal order.  attn_set_tuning overrides some.
+struct FwdPlan {
+  int T = 1;              // query tiles per unit
+  bool split = false;     // key split (D <= 64)
+  bool shortk = false;    // short-unit kernel (D <= 64)
+  bool persist = false;   // persistent grid
+  int lpt = 0;            // causal: heads per longest-first band (0: a head's units adjacent)
+  int64_t n_work = 0;     // units of the whole problem
+  int64_t ctas = 0;       // grid size
+};
+
+FwdPlan plan_fwd(int64_t BH, int64_t Nq, int64_t Nk, int64_t D, bool causal, int64_t sms) {
+  FwdPlan pl;
+  const int64_t n_qtiles = (Nq + attn::BM - 1) / attn::BM;
+  const int64_t n_ktiles = (Nk + attn::BN - 1) / attn::BN;
+  // Two query tiles per CTA share every K/V tile and let two softmax warpgroups
+  // take turns on the tensor core: one key step of both tiles costs about 3100
+  // SM cycles, against about 2500 for one tile alone (no partner to overlap
+  // with).  Pick the tiling whose waves of CTAs finish first:
+  //   waves(T=2) * 3100 <= waves(T=1) * 2500, i.e. about 5 * waves2 <= 4 * waves1.
+  // attn_set_tuning overrides the choice (testing and tuning).
+  const int64_t waves2 = ((n_qtiles + 1) / 2 * BH + sms - 1) / sms;
+  const int64_t waves1 = (n_qtiles * BH + sms - 1) / sms;
+  int T = 5 * waves2 <= 4 * waves1 ? 2 : 1;
+  // Key split (D <= 64): one query tile per unit, its key tiles shared out
+  // between the two softmax warpgroups.  It halves a unit's chain of key steps
+  // at the same tensor-core throughput per CTA as two tiles per unit, so it
+  // wins when the single-tile units fit in one wave of CTAs (then every CTA's
+  // time is one unit's chain; b2h8n1024d64: 128 tiles on 152 SMs).  Beyond a
+  // wave its extra per-unit cost (Q load, merge) loses to two tiles per unit.
+  bool split = D <= 64 && n_ktiles >= 2 && n_qtiles * BH <= sms;
+  // Short-unit kernel (D <= 64, two CTAs per SM, one tile per unit): causal
+  // problems of short rows, where the two tiles of a unit differ in length
+  // and unit boundaries come every few key steps, with at least a full wave
+  // of its grid.  Measured (CUDA events, L2 flushed, mean of 150): causal
+  // b16h32n512d64 46.1 against 54.9 us, b32h32n256d64 37.7 against 44.5,
+  // b8h16n1024d64 37.6 against 40.5, b4h32n2048d64 97.9 against 99.5; it lost
+  // on full rows (b16h32n512d64 54.0 against 51.9), on a short query block
+  // against 4096 keys and below a wave (b2h8n1024d64 causal 17.3 against 16.7).
+  bool shortk = D <= 64 && causal && n_ktiles <= 16 && n_qtiles >= 2 && n_qtiles * BH >= 2 * sms;
+  if (shortk) split = false;
+  if (const int u = g_tune_unit.load(std::memory_order_relaxed)) {
+    T = u >= 3 ? 1 : u;
+    split = u == 3 && D <= 64;
+    shortk = u == 4 && D <= 64;
+  }
+  if (split || shortk) T = 1;
+  if (D > 128) T = 1;  // the D = 256 kernel holds one query tile (TMEM)
+  pl.T = T;
+  pl.split = split;
+  pl.shortk = shortk;
+  pl.n_work = (n_qtiles + T - 1) / T * BH;
+  // Causal order: longest first over all heads when the units' key ranges
+  // differ a lot (lightest below 3/4 of the heaviest: the square causal case);
+  // when they are about equal (a short query block against a long key cache)
+  // a head's units stay adjacent instead, so its K and V are read from HBM
+  // once (the longest-first order read them twice there: 976 against 553 MB).
+  if (causal) {
+    const int64_t last_row_light = (T == 2 ? 2 * attn::BM : attn::BM) - 1;  // unit 0's last query row
+    const int64_t light_row = last_row_light < Nq - 1 ? last_row_light : Nq - 1;
+    int64_t nk_light = (light_row + (Nk - Nq)) / attn::BN + 1;
+    if (nk_light > n_ktiles) nk_light = n_ktiles;
+    if (4 * nk_light < 3 * n_ktiles) {
+      // Bands of heads whose K and V together take at most half of L2 (64 MB):
+      // over all 16 heads of causal N = 16384 (8 MB each) the longest-first
+      // order read 552 MB from HBM for 201 MB of K, V and Q.
+      const int64_t kv_head = 4 * Nk * D;
+      const int64_t band = (int64_t(64) << 20) / kv_head;
+      pl.lpt = int(band < 1 ? 1 : (band > BH ? BH : band));
+    }
+  }
+  // Short key ranges: a persistent grid (one CTA per SM taking every gridDim-th
+  // unit) overlaps each unit's Q load and epilogue with the previous unit's
+  // work.  Long ones: one CTA per unit, whose key loop runs faster (see the
+  // kernel) and whose launch cost is small beside the unit.
+  // attn_set_tuning forces the choice (testing and tuning).
+  // At D <= 64 a key step costs about half as much, so the persistent grid wins
+  // at every length measured (N = 4096: +6 %, 16384: +2.5 %).
+  bool persist = D <= 64 || n_ktiles <= kPersistMaxKeyTiles;
+  if (const int g = g_tune_grid.load(std::memory_order_relaxed)) persist = g == 2;
+  if (D > 128) persist = false;  // the D = 256 kernel stages O in its Q buffer
+  int64_t ctas = persist && pl.n_work > sms ? sms : pl.n_work;
+  if (shortk) ctas = pl.n_work > 2 * sms ? 2 * sms : pl.n_work;  // two CTAs per SM
+  pl.persist = persist;
+  pl.ctas = ctas;
+  return pl;
+}
+
 // Shared launcher of attn_fwd and attn_fwd_qk: Q, O [B*H, Nq, D]; K, V [B*H, Nk, D].
 // With check_only it validates the arguments and the device and returns.
 // ld: row stride in elements of q, k, v, o (0 = contiguous, ld = D).
@@ -219,40 +309,9 @@ attn_status_t launch_fwd(const void* q, const void* k, const void* v, void* o, f
   if (!encode_qkv_map(enc, &prm.tq, q, D, Nq, BH, ld) || !encode_qkv_map(enc, &prm.tk, k, D, Nk, BH, ld) ||
       !encode_qkv_map(enc, &prm.tv, v, D, Nk, BH, ld) || !encode_qkv_map(enc, &prm.to, o, D, Nq, BH, ld))
     return ATTN_ERR_CUDA;
-  // Two query tiles per CTA share every K/V tile and let two softmax warpgroups
-  // take turns on the tensor core: one key step of both tiles costs about 3100
-  // SM cycles, against about 2500 for one tile alone (no partner to overlap
-  // with).  Pick the tiling whose waves of CTAs finish first:
-  //   waves(T=2) * 3100 <= waves(T=1) * 2500, i.e. about 5 * waves2 <= 4 * waves1.
-  // attn_set_tuning overrides the choice (testing and tuning).
   const int64_t sms = g_dev_sms[dev] > 0 ? g_dev_sms[dev] : 1;
-  const int64_t waves2 = ((n_qtiles + 1) / 2 * BH + sms - 1) / sms;
-  const int64_t waves1 = (n_qtiles * BH + sms - 1) / sms;
-  int T = 5 * waves2 <= 4 * waves1 ? 2 : 1;
-  // Key split (D <= 64): one query tile per unit, its key tiles shared out
-  // between the two softmax warpgroups.  It halves a unit's chain of key steps
-  // at the same tensor-core throughput per CTA as two tiles per unit, so it
-  // wins when the single-tile units fit in one wave of CTAs (then every CTA's
-  // time is one unit's chain; b2h8n1024d64: 128 tiles on 152 SMs).  Beyond a
-  // wave its extra per-unit cost (Q load, merge) loses to two tiles per unit.
-  bool split = D <= 64 && n_ktiles >= 2 && n_qtiles * BH <= sms;
-  // Short-unit kernel (D <= 64, two CTAs per SM, one tile per unit): causal
-  // problems of short rows, where the two tiles of a unit differ in length
-  // and unit boundaries come every few key steps, with at least a full wave
-  // of its grid.  Measured (CUDA events, L2 flushed, mean of 150): causal
-  // b16h32n512d64 46.1 against 54.9 us, b32h32n256d64 37.7 against 44.5,
-  // b8h16n1024d64 37.6 against 40.5, b4h32n2048d64 97.9 against 99.5; it lost
-  // on full rows (b16h32n512d64 54.0 against 51.9), on a short query block
-  // against 4096 keys and below a wave (b2h8n1024d64 causal 17.3 against 16.7).
-  bool shortk = D <= 64 && causal && n_ktiles <= 16 && n_qtiles >= 2 && n_qtiles * BH >= 2 * sms;
-  if (shortk) split = false;
-  if (const int u = g_tune_unit.load(std::memory_order_relaxed)) {
-    T = u >= 3 ? 1 : u;
-    split = u == 3 && D <= 64;
-    shortk = u == 4 && D <= 64;
-  }
-  if (split || shortk) T = 1;
-  if (D > 128) T = 1;  // the D = 256 kernel holds one query tile (TMEM)
+  const FwdPlan pl = plan_fwd(BH, Nq, Nk, D, causal != 0, sms);
+  const int T = pl.T;
   prm.lse = lse;
   prm.Nq = int(Nq);
   prm.Nk = int(Nk);
@@ -270,41 +329,11 @@ attn_status_t launch_fwd(const void* q, const void* k, const void* v, void* o, f
   prm.withhold_kv = g_test_withhold_kv.load(std::memory_order_relaxed);
 #endif
 
-  prm.n_work = int(int64_t(prm.n_units) * BH);
-  // Causal order: longest first over all heads when the units' key ranges
-  // differ a lot (lightest below 3/4 of the heaviest: the square causal case);
-  // when they are about equal (a short query block against a long key cache)
-  // a head's units stay adjacent instead, so its K and V are read from HBM
-  // once (the longest-first order read them twice there: 976 against 553 MB).
-  if (causal) {
-    const int64_t last_row_light = (T == 2 ? 2 * attn::BM : attn::BM) - 1;  // unit 0's last query row
-    const int64_t light_row = last_row_light < Nq - 1 ? last_row_light : Nq - 1;
-    int64_t nk_light = (light_row + (Nk - Nq)) / attn::BN + 1;
-    if (nk_light > n_ktiles) nk_light = n_ktiles;
-    if (4 * nk_light < 3 * n_ktiles) {
-      // Bands of heads whose K and V together take at most half of L2 (64 MB):
-      // over all 16 heads of causal N = 16384 (8 MB each) the longest-first
-      // order read 552 MB from HBM for 201 MB of K, V and Q.
-      const int64_t kv_head = 4 * Nk * D;
-      const int64_t band = (int64_t(64) << 20) / kv_head;
-      prm.lpt = int(band < 1 ? 1 : (band > BH ? BH : band));
-    }
-  }
-  // Short key ranges: a persistent grid (one CTA per SM taking every gridDim-th
-  // unit) overlaps each unit's Q load and epilogue with the previous unit's
-  // work.  Long ones: one CTA per unit, whose key loop runs faster (see the
-  // kernel) and whose launch cost is small beside the unit.
-  // attn_set_tuning forces the choice (testing and tuning).
-  // At D <= 64 a key step costs about half as much, so the persistent grid wins
-  // at every length measured (N = 4096: +6 %, 16384: +2.5 %).
-  bool persist = D <= 64 || n_ktiles <= kPersistMaxKeyTiles;
-  if (const int g = g_tune_grid.load(std::memory_order_relaxed)) persist = g == 2;
-  if (D > 128) persist = false;  // the D = 256 kernel stages O in its Q buffer
-  int64_t ctas = persist && prm.n_work > sms ? sms : prm.n_work;
-  if (shortk) {
-    ctas = prm.n_work > 2 * sms ? 2 * sms : prm.n_work;  // two CTAs per SM
-    if (!encode_qkv_map(enc, &prm.to32, o, D, Nq, BH, ld, 32)) return ATTN_ERR_CUDA;
-  }
+  prm.n_work = int(pl.n_work);
+  prm.lpt = pl.lpt;
+  const bool persist = pl.persist, split = pl.split, shortk = pl.shortk;
+  const int64_t ctas = pl.ctas;
+  if (shortk && !encode_qkv_map(enc, &prm.to32, o, D, Nq, BH, ld, 32)) return ATTN_ERR_CUDA;
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t err;
   // Head dims below 64, 128 or 256 run on that kernel: the tensor maps carry the true
@@ -323,6 +352,27 @@ attn_status_t launch_fwd(const void* q, const void* k, const void* v, void* o, f
 }  // namespace
 
 extern "C" {
+
+const char* attn_fwd_kernel_name(int64_t B, int64_t H, int64_t Nq, int64_t Nk, int64_t D, int causal) {
+  if (B <= 0 || H <= 0 || Nq <= 0 || Nk <= 0 || D <= 0 || D > 256) return nullptr;
+  constexpr int64_t kI32 = 2147483647;
+  if (B > kI32 || H > kI32 || B * H > kI32 || Nq > kI32 - 256 || Nk > kI32 - 256) return nullptr;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || prepare_device(dev) != ATTN_OK) return nullptr;
+  const int64_t D8 = (D + 7) & ~int64_t(7);
+  const FwdPlan pl = plan_fwd(B * H, Nq, Nk, D8, causal != 0, g_dev_sms[dev] > 0 ? g_dev_sms[dev] : 1);
+  const int dk = D8 <= 64 ? 64 : (D8 <= 128 ? 128 : 256);
+  const char* mask = causal ? "causal" : "full";
+  thread_local char name[96];
+  if (pl.shortk)
+    std::snprintf(name, sizeof(name), "attn_fwd_short_sm103<%s>", mask);
+  else if (pl.split)
+    std::snprintf(name, sizeof(name), "attn_fwd_sm103<64,%s,persistent,key split>", mask);
+  else
+    std::snprintf(name, sizeof(name), "attn_fwd_sm103<%d,%s,%s,%d tile%s/unit>", dk, mask,
+                  pl.persist ? "persistent" : "one unit per CTA", pl.T, pl.T > 1 ? "s" : "");
+  return name;
+}
 
 attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int64_t B, int64_t H,
                        int64_t N, int64_t D, int causal, float scale, void* stream) {
