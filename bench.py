@@ -191,6 +191,13 @@ def oracle_parity(w, o, lse, q, k, v):
     secs = time.perf_counter() - t0
     cpu = {"value": w.flops / secs / 1e12, "unit": "TFLOP/s", "cores": oracle.threads(), "kind": "oracle",
            "sample": f"the whole workload {w.name} (every query row, all visible keys), {secs:.1f} s wall"}
+    if w.flops <= 5e9:
+        # Small workloads: also the oracle on one core (a few seconds at most).
+        t0 = time.perf_counter()
+        oracle.attn_fwd(q, k, v, w.causal, w.scale, nthreads=1)
+        secs1 = time.perf_counter() - t0
+        cpu["single_core"] = {"value": w.flops / secs1 / 1e12, "unit": "TFLOP/s", "cores": 1,
+                              "sample": f"the whole workload {w.name}, {secs1:.2f} s wall"}
     do = np.abs(o - o_ref)
     at = np.unravel_index(int(np.argmax(do)), do.shape)
     dl = np.abs(lse - lse_ref)
@@ -587,6 +594,19 @@ def run_ours(args, w):
     elapsed_ms = max_over_ranks(elapsed_ms, pg, dev)
     if sampler:
         sampler.stop()
+    l2_warm_ms = None
+    if flush and not args.backward:
+        # The same launches back to back, without the buffer rewrite: inputs stay
+        # resident in L2 between launches (reported beside the flushed number).
+        n_warm = min(args.steps, 200)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n_warm):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        l2_warm_ms = max_over_ranks(e0.elapsed_time(e1) / n_warm, pg, dev)
 
     flops = (pkg.attn_bwd_qk_flops if args.backward else pkg.attn_fwd_qk_flops)(w.B, w.H, w.N, w.n_keys, w.D,
                                                                                 w.causal)
@@ -715,6 +735,11 @@ def run_ours(args, w):
         "kernel_source": kernel_source_hash(),
         "parity": parity,
         "backward": backward,
+        # Working sets under 2x L2: the same launches back to back after the timed
+        # region, inputs left resident in L2 (the line's value flushes L2 first).
+        "l2_resident": None if l2_warm_ms is None else {
+            "value": job_tflops(flops, world, l2_warm_ms) if w_job is w else value * ms_per_step / l2_warm_ms,
+            "unit": "TFLOP/s", "ms_per_step": l2_warm_ms, "steps": min(args.steps, 200)},
     }
     print(json.dumps(line), flush=True)
     if pg:
