@@ -151,7 +151,7 @@ __global__ void __launch_bounds__(kShortThreads, 2) attn_fwd_short_sm103(const _
       const uint32_t dS = tmem + C::COL_S, dO = tmem + C::COL_O;
       int cb = 0;   // ring index of the current unit's K_0
       int ns = 0;   // key steps so far (B_PF phases)
-      int nu = 0;   // units so far (Q buffer, B_Q / B_QE phases)
+      int nu = 0;   // units so far (Q buffer, B_Q phase, B_OF)
       bool ok = true;
       for (int k = 0; ok && more(k); ++k) {
         const int nk = unit_of<CAUSAL>(p, work(k)).nk0;
