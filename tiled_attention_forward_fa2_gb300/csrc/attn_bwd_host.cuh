@@ -31,15 +31,19 @@ attn_status_t prepare_bwd(int dev) {
 
 // prm_dq, prm_dkv: the same problem; they differ only in the box heights of
 // the load maps (D = 256: 64-key K/V boxes for dQ, 32-query Q/dO boxes for dK/dV).
+// The dK/dV kernel runs one CTA per SM walking the key tiles (D <= 128) or one
+// CTA per key tile and column half (D = 256).
 template <int D, bool CAUSAL>
-cudaError_t launch_bwd_kernels(const attn::BwdParams& prm_dq, const attn::BwdParams& prm_dkv, cudaStream_t st) {
+cudaError_t launch_bwd_kernels(const attn::BwdParams& prm_dq, const attn::BwdParams& prm_dkv, int64_t sms,
+                               cudaStream_t st) {
   attn::attn_bwd_dq_sm103<D, CAUSAL><<<dim3(unsigned(int64_t(prm_dq.n_qtiles) * prm_dq.bh)), dim3(attn::kBwdThreads),
                                        attn::CfgDq<D>::SMEM, st>>>(prm_dq);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
+  const int64_t units = int64_t(prm_dkv.n_ktiles) * prm_dkv.bh * attn::CfgDkv<D>::NHALF;
+  const int64_t ctas = attn::CfgDkv<D>::PERSIST && units > sms ? sms : units;
   attn::attn_bwd_dkdv_sm103<D, CAUSAL>
-      <<<dim3(unsigned(int64_t(prm_dkv.n_ktiles) * prm_dkv.bh * attn::CfgDkv<D>::NHALF)), dim3(attn::kBwdThreads),
-         attn::CfgDkv<D>::SMEM, st>>>(prm_dkv);
+      <<<dim3(unsigned(ctas)), dim3(attn::kBwdThreads), attn::CfgDkv<D>::SMEM, st>>>(prm_dkv);
   return cudaGetLastError();
 }
 
@@ -67,8 +71,9 @@ attn_status_t launch_bwd(const void* q, const void* k, const void* v, const void
   if (B > kI32 || H > kI32 || B * H > kI32 || Nq > kI32 - 256 || Nk > kI32 - 256) return ATTN_ERR_INVALID_ARG;
   const int64_t BH = B * H;
   const int64_t n_qtiles = (Nq + attn::BM - 1) / attn::BM, n_ktiles = (Nk + attn::BN - 1) / attn::BN;
-  // Grids: n_qtiles * BH dQ CTAs, n_ktiles * BH (two per key tile at D > 128) dK/dV CTAs.
-  if (BH > kI32 / (n_qtiles > 2 * n_ktiles ? n_qtiles : 2 * n_ktiles)) return ATTN_ERR_INVALID_ARG;
+  // Grids: n_qtiles * BH dQ CTAs; n_ktiles * BH (two per key tile at D > 128) dK/dV units, whose
+  // persistent walk runs up to two grid sizes past the last one: all in int32.
+  if (BH > (kI32 - 4096) / (n_qtiles > 2 * n_ktiles ? n_qtiles : 2 * n_ktiles)) return ATTN_ERR_INVALID_ARG;
   const int64_t Nmax = Nq > Nk ? Nq : Nk;
   if (BH > (int64_t(1) << 62) / (Nmax * ld * 2)) return ATTN_ERR_INVALID_ARG;
   const uint64_t qb = uint64_t(BH) * uint64_t(Nq) * uint64_t(ld) * 2u, kb = uint64_t(BH) * uint64_t(Nk) * uint64_t(ld) * 2u;
@@ -125,13 +130,14 @@ attn_status_t launch_bwd(const void* q, const void* k, const void* v, const void
                   !encode_qkv_map(enc, &prm_dkv.tdo, dout, D, Nq, BH, ld, attn::CfgDkv<256>::SQ)))
     return ATTN_ERR_CUDA;
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int64_t sms = g_dev_sms[dev] > 0 ? g_dev_sms[dev] : 1;
   cudaError_t err;
   if (D <= 64)  // padded to 64, 128 or 256 as in the forward
-    err = causal ? launch_bwd_kernels<64, true>(prm_dq, prm_dkv, st) : launch_bwd_kernels<64, false>(prm_dq, prm_dkv, st);
+    err = causal ? launch_bwd_kernels<64, true>(prm_dq, prm_dkv, sms, st) : launch_bwd_kernels<64, false>(prm_dq, prm_dkv, sms, st);
   else if (D <= 128)
-    err = causal ? launch_bwd_kernels<128, true>(prm_dq, prm_dkv, st) : launch_bwd_kernels<128, false>(prm_dq, prm_dkv, st);
+    err = causal ? launch_bwd_kernels<128, true>(prm_dq, prm_dkv, sms, st) : launch_bwd_kernels<128, false>(prm_dq, prm_dkv, sms, st);
   else
-    err = causal ? launch_bwd_kernels<256, true>(prm_dq, prm_dkv, st) : launch_bwd_kernels<256, false>(prm_dq, prm_dkv, st);
+    err = causal ? launch_bwd_kernels<256, true>(prm_dq, prm_dkv, sms, st) : launch_bwd_kernels<256, false>(prm_dq, prm_dkv, sms, st);
   return err == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 

@@ -15,12 +15,14 @@
 //       TMEM; dQ stored with TMA.  The elementwise warps take dP into
 //       registers first and release its columns, so the next key tile's S and
 //       dP are computed while they work on this one's dS.
-//   attn_bwd_dkdv_sm103: one CTA per 128-key tile, transposed: per half of a
-//       query tile (64 queries) S^T = K Q^T and dP^T = V dO^T into one of two
-//       TMEM buffers, P^T and dS^T (bf16) over them, then dV += P^T dO and
+//   attn_bwd_dkdv_sm103: per 128-key tile, transposed: per half of a query
+//       tile (64 queries) S^T = K Q^T and dP^T = V dO^T into one of two TMEM
+//       buffers, P^T and dS^T (bf16) over them, then dV += P^T dO and
 //       dK += dS^T Q; the next half's S^T and dP^T are computed while the
 //       elementwise warps work on this one.  The per-query LSE and D reach
-//       every thread through shared memory; dK, dV stored with TMA.
+//       every thread through shared memory; dK, dV stored with TMA.  One CTA
+//       per SM walks the key tiles (D <= 128): the next tile's K and V load,
+//       and its first S^T and dP^T run, while this tile's dK and dV are stored.
 // Warp roles as in the forward: warps 0-3 elementwise (thread = TMEM lane =
 // row), warp 4 TMA producer, warp 5 TMEM allocation and warp-uniform MMA issue.
 // Every wait is bounded (see wait_bounded in attn_fwd_kernel.cuh).
@@ -366,8 +368,17 @@ struct CfgDkv {
   static_assert(OFF_VEC + NSTAGE * 2 * SQ * 4 <= OFF_K, "vector area");
   // Sub-steps h (HQ queries): S^T and dP^T in buffer h & 1 (B_SF[h & 1], MMA
   // commit), P^T and dS^T written over them (B_PF[h & 1], 128 arrivals).
+  // B_KV: a unit's K and V landed (TMA bytes); B_KVE: its last S^T and dP^T
+  // (the products that read K and V) done (MMA commit); B_ACC: its last
+  // products done (MMA commit); B_EPI: the epilogue has read dK, dV out of
+  // TMEM (128 arrivals); B_STG: a unit's dK, dV stores have read their
+  // staging (thread 0).
   static constexpr int B_KV = 0, B_SFULL = 1, B_SEMPTY = 1 + NSTAGE, B_SF = 1 + 2 * NSTAGE, B_PF = B_SF + 2,
-                       B_ACC = B_PF + 2, B_DONE = B_ACC + 1, NBAR = B_DONE + 1;
+                       B_ACC = B_PF + 2, B_EPI = B_ACC + 1, B_STG = B_EPI + 1, B_KVE = B_STG + 1,
+                       B_DONE = B_KVE + 1, NBAR = B_DONE + 1;
+  // One CTA per SM walking key tiles (D <= 128, where a stage slot holds a
+  // unit's dK and dV for their stores), or one CTA per key tile (D = 256).
+  static constexpr bool PERSIST = 2u * STILE >= 2u * uint32_t(BM) * uint32_t(DACC) * 2u;
   // Buffer b: S^T at BUF b, dP^T at BUF b + HQ (HQ columns each; P^T, dS^T
   // bf16 over their first HQ / 2).
   static constexpr uint32_t COL_S = 0, COL_DP = HQ, BUF = 2 * HQ, COL_DV = 256, COL_DK = 256 + DACC;
@@ -378,41 +389,52 @@ template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dkdv_sm103(const __grid_constant__ BwdParams p) {
   using C = CfgDkv<D>;
   constexpr int KB = C::KB, NSTAGE = C::NSTAGE, SQ = C::SQ, HQ = C::HQ, NSUB = C::NSUB, DACC = C::DACC;
+  constexpr bool PERSIST = C::PERSIST;
+  constexpr int kRounds = PERSIST ? 0x7fffffff : 1;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = sm103::smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* const sbase = smem_raw + (base - raw);
   uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(sbase + 512);
   volatile uint32_t* const abort_flag = reinterpret_cast<volatile uint32_t*>(sbase + 516);
-  float* const vec = reinterpret_cast<float*>(sbase + C::OFF_VEC);  // [stage][0: lse2, 1: D][128]
+  float* const vec = reinterpret_cast<float*>(sbase + C::OFF_VEC);  // [stage][0: lse2, 1: D][SQ]
   const uint32_t sK = base + C::OFF_K, sV = base + C::OFF_V, sST = base + C::OFF_ST;
   auto bar = [base](int i) { return base + 8u * uint32_t(i); };
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  // Causal: key tiles seen by the most queries (the first ones) go first.  The
-  // CTAs of one key tile's column halves are adjacent.
-  const int half = C::NHALF > 1 ? int(blockIdx.x % uint32_t(C::NHALF)) : 0;
-  const uint32_t tile = blockIdx.x / uint32_t(C::NHALF);
-  int kt, bh;
-  if (CAUSAL) {
-    kt = int(tile / uint32_t(p.bh));
-    bh = int(tile % uint32_t(p.bh));
-  } else {
-    kt = int(tile % uint32_t(p.n_ktiles));
-    bh = int(tile / uint32_t(p.n_ktiles));
-  }
-  const int n0 = kt * BN;
-  // Query blocks (SQ queries, one stage each) with a query that sees one of
-  // these keys (query i sees key n iff n <= i + kv_off).
-  const int it0 = CAUSAL ? max(0, n0 - p.kv_off) / SQ : 0;
-  const int niter = max(0, (p.Nq + SQ - 1) / SQ - it0);
+  // Units: one key tile of one (b, h) (and, at D = 256, one column half of dK
+  // and dV).  Causal: key-tile major, the key tiles seen by the most queries
+  // (the first ones) first; else (b, h) major.  The CTAs of one key tile's
+  // column halves are adjacent.  PERSIST: CTA c takes units k G + c (even
+  // rounds k) and k G + G - 1 - c (odd rounds), G = grid size, as the forward.
+  const int n_units = p.n_ktiles * p.bh * C::NHALF;
+  const int w0 = int(blockIdx.x), dw = int(gridDim.x);
+  auto work = [w0, dw](int k) { return k * dw + ((k & 1) ? dw - 1 - w0 : w0); };
+  auto more = [&](int k) { return work(k) < n_units; };
+  struct UnitDkv {
+    int half, bh, n0, it0, niter;
+  };
+  auto unit_at = [&](int w) {
+    UnitDkv u;
+    u.half = C::NHALF > 1 ? w % C::NHALF : 0;
+    const int tile = w / C::NHALF;
+    const int kt = CAUSAL ? tile / p.bh : tile % p.n_ktiles;
+    u.bh = CAUSAL ? tile % p.bh : tile / p.n_ktiles;
+    u.n0 = kt * BN;
+    // Query blocks (SQ queries, one stage each) with a query that sees one of
+    // these keys (query i sees key n iff n <= i + kv_off): at least one, as
+    // causal problems have Nq <= Nk.
+    u.it0 = CAUSAL ? max(0, u.n0 - p.kv_off) / SQ : 0;
+    u.niter = max(0, (p.Nq + SQ - 1) / SQ - u.it0);
+    return u;
+  };
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::NBAR; ++i) {
       uint32_t cnt = 1;
       // the producer warp's 32 lanes (vectors written) + lane 0's expect-tx arrival
       if (i >= C::B_SFULL && i < C::B_SFULL + NSTAGE) cnt = 33;
-      if (i == C::B_PF || i == C::B_PF + 1) cnt = BM;
+      if (i == C::B_PF || i == C::B_PF + 1 || i == C::B_EPI) cnt = BM;
       sm103::mbar_init(bar(i), cnt);
     }
     *abort_flag = 0u;
@@ -428,52 +450,79 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dkdv_sm103(const __gr
   const uint32_t tmem = *tmem_slot;
   const Abort ab{abort_flag, p.timeout_cycles};
 
+  // Phase bookkeeping: every role walks the same units and counts stages (gs:
+  // B_SFULL, B_SEMPTY, the stage slot gs % NSTAGE), sub-steps (gh: the S^T /
+  // dP^T buffer gh & 1, B_SF, B_PF) and units (nu: B_KV, B_ACC, B_EPI, B_STG)
+  // across them.  With PERSIST a unit's dK, dV are staged in the slot of its
+  // last stage (free once its MMAs are done), so the next unit's K and V load
+  // while they are stored; without it (D = 256) they are staged in the K and V
+  // tiles.
   if (warp == kBwdLoadWarp) {
     // -------------------------------------------------------------- producer
-    if (lane == 0) {
-      sm103::mbar_arrive_expect_tx(bar(C::B_KV), 2u * C::TILE);
-      for (int kb = 0; kb < KB; ++kb) {
-        sm103::tma_load_3d(sK + kb * kSubTile, &p.tk, bar(C::B_KV), kb * 64, n0, bh);
-        sm103::tma_load_3d(sV + kb * kSubTile, &p.tv, bar(C::B_KV), kb * 64, n0, bh);
-      }
-    }
-    int issued = 0;
+    static_assert(NSTAGE == 2, "staging bookkeeping below is for two stage slots");
+    int gs = 0;
+    int nkv = 0;                // K, V loads issued (one per unit)
+    int stg0 = -1, stg1 = -1;   // unit whose dK, dV are staged in slot 0 / 1 (-1: none)
     bool ok = true;
-    for (int it = 0; ok && it < niter; ++it) {
-      const int st = it % NSTAGE;
-      const int i0 = (it0 + it) * SQ;
-      // Per-query LSE (base 2) and D for this block (queries past Nq get P = 0),
-      // read before the stage is free so the loads overlap the wait; the tile
-      // copies go out first once it is free.
-      constexpr int NV4 = SQ / 32;  // values per lane
-      float lse4[NV4], d4[NV4];
-#pragma unroll
-      for (int x = 0; x < NV4; ++x) {
-        const int i = i0 + lane * NV4 + x;
-        const bool live = i < p.Nq;
-        lse4[x] = live ? p.lse[size_t(bh) * p.Nq + i] * 1.4426950408889634f : INFINITY;
-        d4[x] = live ? p.delta[size_t(bh) * p.Nq + i] : 0.f;
-      }
-      if (it >= NSTAGE && !(ok = warp_wait(bar(C::B_SEMPTY + st), uint32_t(it / NSTAGE - 1) & 1u, ab))) break;
+    int nu = 0;
+    for (int k = 0; k < kRounds && ok && more(k); ++k, ++nu) {
+      const UnitDkv u = unit_at(work(k));
+      // K and V: the previous unit's S^T and dP^T must be done with the tiles.
+      if (nu > 0 && !(ok = warp_wait(bar(C::B_KVE), uint32_t(nu - 1) & 1u, ab))) break;
       if (lane == 0) {
-        sm103::mbar_arrive_expect_tx(bar(C::B_SFULL + st), 2u * C::STILE);
-        const uint32_t sq = sST + uint32_t(st) * 2u * C::STILE, sdo = sq + C::STILE;
+        sm103::mbar_arrive_expect_tx(bar(C::B_KV), 2u * C::TILE);
         for (int kb = 0; kb < KB; ++kb) {
-          sm103::tma_load_3d(sq + kb * C::QSUB, &p.tq, bar(C::B_SFULL + st), kb * 64, i0, bh);
-          sm103::tma_load_3d(sdo + kb * C::QSUB, &p.tdo, bar(C::B_SFULL + st), kb * 64, i0, bh);
+          sm103::tma_load_3d(sK + kb * kSubTile, &p.tk, bar(C::B_KV), kb * 64, u.n0, u.bh);
+          sm103::tma_load_3d(sV + kb * kSubTile, &p.tv, bar(C::B_KV), kb * 64, u.n0, u.bh);
         }
       }
+      ++nkv;
+      for (int it = 0; ok && it < u.niter; ++it, ++gs) {
+        const int st = gs % NSTAGE;
+        const int i0 = (u.it0 + it) * SQ;
+        // Per-query LSE (base 2) and D for this block (queries past Nq get P = 0),
+        // read before the stage is free so the loads overlap the wait; the tile
+        // copies go out first once it is free.
+        constexpr int NV4 = SQ / 32;  // values per lane
+        float lse4[NV4], d4[NV4];
 #pragma unroll
-      for (int x = 0; x < NV4; ++x) {
-        vec[(st * 2 + 0) * SQ + lane * NV4 + x] = lse4[x];
-        vec[(st * 2 + 1) * SQ + lane * NV4 + x] = d4[x];
+        for (int x = 0; x < NV4; ++x) {
+          const int i = i0 + lane * NV4 + x;
+          const bool live = i < p.Nq;
+          lse4[x] = live ? p.lse[size_t(u.bh) * p.Nq + i] * 1.4426950408889634f : INFINITY;
+          d4[x] = live ? p.delta[size_t(u.bh) * p.Nq + i] : 0.f;
+        }
+        if (gs >= NSTAGE && !(ok = warp_wait(bar(C::B_SEMPTY + st), uint32_t(gs / NSTAGE - 1) & 1u, ab))) break;
+        // A slot that holds a unit's staged dK, dV is refilled once its stores have read it.
+        const int stg = st == 0 ? stg0 : stg1;
+        if (PERSIST && stg >= 0) {
+          if (!(ok = warp_wait(bar(C::B_STG), uint32_t(stg) & 1u, ab))) break;
+          if (st == 0) stg0 = -1; else stg1 = -1;
+        }
+        if (lane == 0) {
+          sm103::mbar_arrive_expect_tx(bar(C::B_SFULL + st), 2u * C::STILE);
+          const uint32_t sq = sST + uint32_t(st) * 2u * C::STILE, sdo = sq + C::STILE;
+          for (int kb = 0; kb < KB; ++kb) {
+            sm103::tma_load_3d(sq + kb * C::QSUB, &p.tq, bar(C::B_SFULL + st), kb * 64, i0, u.bh);
+            sm103::tma_load_3d(sdo + kb * C::QSUB, &p.tdo, bar(C::B_SFULL + st), kb * 64, i0, u.bh);
+          }
+        }
+#pragma unroll
+        for (int x = 0; x < NV4; ++x) {
+          vec[(st * 2 + 0) * SQ + lane * NV4 + x] = lse4[x];
+          vec[(st * 2 + 1) * SQ + lane * NV4 + x] = d4[x];
+        }
+        sm103::mbar_arrive(bar(C::B_SFULL + st));  // releases this lane's vector stores
       }
-      sm103::mbar_arrive(bar(C::B_SFULL + st));  // releases this lane's vector stores
-      ++issued;
+      if (PERSIST && ok) {  // the unit's last stage will hold its dK, dV
+        if ((gs - 1) % NSTAGE == 0) stg0 = nu; else stg1 = nu;
+      }
     }
+    // No copy may land after the CTA has left.  Loads before the last NSTAGE
+    // stages, and K, V before the last unit's, were waited on by their users.
     if (lane == 0) {
-      drain_wait(bar(C::B_KV), 0u);
-      for (int t = issued > NSTAGE ? issued - NSTAGE : 0; t < issued; ++t)
+      if (nkv > 0) drain_wait(bar(C::B_KV), uint32_t(nkv - 1) & 1u);
+      for (int t = gs > NSTAGE ? gs - NSTAGE : 0; t < gs; ++t)
         drain_wait(bar(C::B_SFULL + t % NSTAGE), uint32_t(t / NSTAGE) & 1u);
     }
     __syncwarp();
@@ -484,148 +533,187 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dkdv_sm103(const __gr
     const uint64_t dk_k = sm103::sdesc_sw128(sK, 16, 1024), dv_k = sm103::sdesc_sw128(sV, 16, 1024);
     const uint64_t dst_k = sm103::sdesc_sw128(sST, 16, 1024), dst_mn = sm103::sdesc_sw128(sST, C::QSUB, 1024);
     constexpr uint64_t kSub = uint64_t((HQ * 128u) >> 4);  // HQ rows of a stage tile
-    // This CTA's columns of dO and Q (the B operands of dV and dK).
-    const uint64_t half_off = uint64_t((uint32_t(half) * uint32_t(DACC / 64) * C::QSUB) >> 4);
     // 16 columns kk of D: in a K or V tile and in a stage's Q or dO.
     auto off_kv = [](int kk) { return uint64_t((uint32_t(kk >> 2) * kSubTile + uint32_t(kk & 3) * 32u) >> 4); };
     auto off_st = [](int kk) { return uint64_t((uint32_t(kk >> 2) * C::QSUB + uint32_t(kk & 3) * 32u) >> 4); };
-    // S^T and dP^T of sub-step h into buffer h & 1.
-    auto issue_s = [&](int h) {
-      const int it = h / NSUB, st = it % NSTAGE;
-      const uint64_t soff = uint64_t(uint32_t(st) * 2u * (C::STILE >> 4)) + uint64_t(h % NSUB) * kSub;
-      const uint64_t q_k = dst_k + soff, do_k = dst_k + soff + (C::STILE >> 4);
-      const uint32_t buf = tmem + uint32_t(h & 1) * C::BUF;
+    int gs = 0, gh = 0;
+    bool ok = true;
+    int nu = 0;
+    for (int k = 0; k < kRounds && ok && more(k); ++k, ++nu) {
+      const UnitDkv u = unit_at(work(k));
+      // This unit's columns of dO and Q (the B operands of dV and dK).
+      const uint64_t half_off = uint64_t((uint32_t(u.half) * uint32_t(DACC / 64) * C::QSUB) >> 4);
+      // S^T and dP^T of the unit's sub-step h into buffer (gh + h) & 1.
+      auto issue_s = [&](int h) {
+        const int st = (gs + h / NSUB) % NSTAGE;
+        const uint64_t soff = uint64_t(uint32_t(st) * 2u * (C::STILE >> 4)) + uint64_t(h % NSUB) * kSub;
+        const uint64_t q_k = dst_k + soff, do_k = dst_k + soff + (C::STILE >> 4);
+        const uint32_t buf = tmem + uint32_t((gh + h) & 1) * C::BUF;
 #pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk)  // S^T = K Q^T
-        sm103::mma_ss_warp(buf + C::COL_S, dk_k + off_kv(kk), q_k + off_st(kk), kIdescS, kk > 0 ? 1u : 0u);
+        for (int kk = 0; kk < D / 16; ++kk)  // S^T = K Q^T
+          sm103::mma_ss_warp(buf + C::COL_S, dk_k + off_kv(kk), q_k + off_st(kk), kIdescS, kk > 0 ? 1u : 0u);
 #pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk)  // dP^T = V dO^T
-        sm103::mma_ss_warp(buf + C::COL_DP, dv_k + off_kv(kk), do_k + off_st(kk), kIdescS, kk > 0 ? 1u : 0u);
-      sm103::mma_commit_warp(bar(C::B_SF + (h & 1)));
-    };
-    const int nh = NSUB * niter;
-    bool ok = warp_wait(bar(C::B_KV), 0u, ab) && (nh == 0 || warp_wait(bar(C::B_SFULL), 0u, ab));
-    if (ok && nh > 0) {
+        for (int kk = 0; kk < D / 16; ++kk)  // dP^T = V dO^T
+          sm103::mma_ss_warp(buf + C::COL_DP, dv_k + off_kv(kk), do_k + off_st(kk), kIdescS, kk > 0 ? 1u : 0u);
+        sm103::mma_commit_warp(bar(C::B_SF + ((gh + h) & 1)));
+      };
+      const int nh = NSUB * u.niter;
+      if (!(ok = warp_wait(bar(C::B_KV), uint32_t(nu) & 1u, ab) &&
+                 warp_wait(bar(C::B_SFULL + gs % NSTAGE), uint32_t(gs / NSTAGE) & 1u, ab)))
+        break;
       sm103::tc_fence_after();
       issue_s(0);
-    }
-    for (int h = 0; ok && h < nh; ++h) {
-      const int it = h / NSUB, st = it % NSTAGE;
-      if (h + 1 < nh) {
-        // The other buffer's P^T, dS^T (sub-step h - 1) were read by MMAs issued before.
-        if ((h + 1) % NSUB == 0) {
-          const int it1 = (h + 1) / NSUB;
-          if (!(ok = warp_wait(bar(C::B_SFULL + it1 % NSTAGE), uint32_t(it1 / NSTAGE) & 1u, ab))) break;
-          sm103::tc_fence_after();
+      if (PERSIST && nh == 1) sm103::mma_commit_warp(bar(C::B_KVE));  // K and V no longer read after these
+      for (int h = 0; ok && h < nh; ++h) {
+        const int st = (gs + h / NSUB) % NSTAGE;
+        if (h + 1 < nh) {
+          // The other buffer's P^T, dS^T (sub-step h - 1) were read by MMAs issued before.
+          if ((h + 1) % NSUB == 0) {
+            const int g1 = gs + (h + 1) / NSUB;
+            if (!(ok = warp_wait(bar(C::B_SFULL + g1 % NSTAGE), uint32_t(g1 / NSTAGE) & 1u, ab))) break;
+            sm103::tc_fence_after();
+          }
+          issue_s(h + 1);
+          if (PERSIST && h + 1 == nh - 1) sm103::mma_commit_warp(bar(C::B_KVE));
         }
-        issue_s(h + 1);
-      }
-      if (!(ok = warp_wait(bar(C::B_PF + (h & 1)), uint32_t(h >> 1) & 1u, ab))) break;
-      sm103::tc_fence_after();
-      const uint64_t soff = uint64_t(uint32_t(st) * 2u * (C::STILE >> 4)) + uint64_t(h % NSUB) * kSub + half_off;
-      const uint64_t q_mn = dst_mn + soff, do_mn = dst_mn + soff + (C::STILE >> 4);
-      const uint32_t buf = tmem + uint32_t(h & 1) * C::BUF;
+        if (!(ok = warp_wait(bar(C::B_PF + ((gh + h) & 1)), uint32_t((gh + h) >> 1) & 1u, ab))) break;
+        // The first products of a unit overwrite dV and dK: the previous unit's
+        // epilogue must have read them.
+        if (h == 0 && nu > 0 && !(ok = warp_wait(bar(C::B_EPI), uint32_t(nu - 1) & 1u, ab))) break;
+        sm103::tc_fence_after();
+        const uint64_t soff = uint64_t(uint32_t(st) * 2u * (C::STILE >> 4)) + uint64_t(h % NSUB) * kSub + half_off;
+        const uint64_t q_mn = dst_mn + soff, do_mn = dst_mn + soff + (C::STILE >> 4);
+        const uint32_t buf = tmem + uint32_t((gh + h) & 1) * C::BUF;
 #pragma unroll
-      for (int kk = 0; kk < HQ / 16; ++kk) {  // dV += P^T dO, dK += dS^T Q: 16 queries per MMA
-        const uint64_t off = uint64_t(kk * (2048 >> 4));
-        sm103::mma_ts_warp(tmem + C::COL_DV, buf + C::COL_S + kk * 8, do_mn + off, kIdescA, (h > 0 || kk > 0) ? 1u : 0u);
-        sm103::mma_ts_warp(tmem + C::COL_DK, buf + C::COL_DP + kk * 8, q_mn + off, kIdescA, (h > 0 || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < HQ / 16; ++kk) {  // dV += P^T dO, dK += dS^T Q: 16 queries per MMA
+          const uint64_t off = uint64_t(kk * (2048 >> 4));
+          sm103::mma_ts_warp(tmem + C::COL_DV, buf + C::COL_S + kk * 8, do_mn + off, kIdescA,
+                             (h > 0 || kk > 0) ? 1u : 0u);
+          sm103::mma_ts_warp(tmem + C::COL_DK, buf + C::COL_DP + kk * 8, q_mn + off, kIdescA,
+                             (h > 0 || kk > 0) ? 1u : 0u);
+        }
+        if (h % NSUB == NSUB - 1) sm103::mma_commit_warp(bar(C::B_SEMPTY + st));  // the stage is done with
       }
-      if (h % NSUB == NSUB - 1) sm103::mma_commit_warp(bar(C::B_SEMPTY + st));  // the stage is done with
+      if (!ok) break;
+      sm103::mma_commit_warp(bar(C::B_ACC));
+      gs += u.niter;
+      gh += nh;
     }
-    sm103::mma_commit_warp(bar(C::B_ACC));
     sm103::mma_commit_warp(bar(C::B_DONE));
     drain_wait(bar(C::B_DONE), 0u);
     __syncwarp();
   } else {
     // ----------------------------------------------------------- elementwise
     const int r = threadIdx.x;
-    const int n = n0 + r;  // this thread's key
     const uint32_t lane_off = uint32_t(warp * 32) << 16;
     const uint64_t sl2x2 = sm103::f2_pack(p.scale_log2, p.scale_log2);
-    const bool key_live = n < p.Nk;
+    int gs = 0, gh = 0;
     bool ok = true;
-    for (int h = 0; h < NSUB * niter; ++h) {
-      const int it = h / NSUB, st = it % NSTAGE, hf = h & 1, sub = h % NSUB;
-      if (!(ok = warp_wait(bar(C::B_SF + hf), uint32_t(h >> 1) & 1u, ab))) break;
-      // The stage's LSE and D vectors were written by the producer lanes: wait on
-      // their barrier directly (already complete) to acquire those stores.
-      if (!(ok = warp_wait(bar(C::B_SFULL + st), uint32_t(it / NSTAGE) & 1u, ab))) break;
-      sm103::tc_fence_after();
-      const int i0 = (it0 + it) * SQ + sub * HQ;
-      // query column c sees this key iff n <= i0 + c + kv_off, i.e. c >= n - kv_off - i0
-      const int cmin = key_live ? (CAUSAL ? n - p.kv_off - i0 : 0) : HQ;
-      const float2* lv = reinterpret_cast<const float2*>(vec + (st * 2 + 0) * SQ + sub * HQ);
-      const float2* dv = reinterpret_cast<const float2*>(vec + (st * 2 + 1) * SQ + sub * HQ);
-      const uint32_t tS = tmem + lane_off + uint32_t(hf) * C::BUF + C::COL_S, tDP = tS + (C::COL_DP - C::COL_S);
-      // S^T and dP^T are adjacent: one load of 2 HQ columns, one wait.
-      static_assert(C::COL_DP == C::COL_S + HQ, "S^T, dP^T adjacent");
-      uint32_t u[2 * HQ];
-      if constexpr (HQ == 64)
-        sm103::tmem_ld128(tS, u);
-      else
-        tmem_ld64(tS, u);
-#pragma unroll
-      for (int q = 0; q < HQ / 32; ++q) {
-        uint32_t pp[16], pd[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const int c = q * 32 + 2 * e;
-          const float2 l2 = lv[c / 2], d2 = dv[c / 2];
-          const uint64_t t = sm103::f2_fma(sm103::f2_pack(__uint_as_float(u[c]), __uint_as_float(u[c + 1])), sl2x2,
-                                           sm103::f2_pack(-l2.x, -l2.y));
-          float t0, t1;
-          sm103::f2_unpack(t, t0, t1);
-          const float p0 = c < cmin ? 0.f : sm103::ex2_approx(t0);
-          const float p1 = c + 1 < cmin ? 0.f : sm103::ex2_approx(t1);
-          pp[e] = sm103::pack_bf16x2(p0, p1);
-          pd[e] = sm103::pack_bf16x2(p0 * (__uint_as_float(u[HQ + c]) - d2.x),
-                                     p1 * (__uint_as_float(u[HQ + c + 1]) - d2.y));
+    int nu = 0;
+    // The four warps meet at one reduction barrier per unit, whatever happened
+    // to their waits, and leave the loop together.
+    for (int k = 0; k < kRounds && more(k); ++k, ++nu) {
+      const UnitDkv u = unit_at(work(k));
+      const int n = u.n0 + r;  // this thread's key
+      const bool key_live = n < p.Nk;
+      const int nh = NSUB * u.niter;
+      for (int h = 0; ok && h < nh; ++h) {
+        const int g = gs + h / NSUB, st = g % NSTAGE, hf = (gh + h) & 1, sub = h % NSUB;
+        if (!(ok = warp_wait(bar(C::B_SF + hf), uint32_t((gh + h) >> 1) & 1u, ab))) break;
+        if (PERSIST && h == 0 && nu > 0 && r == 0) {
+          // The previous unit's dK, dV stores (issued at its end) have read their staging slot.
+          sm103::bulk_wait_read0();
+          sm103::mbar_arrive(bar(C::B_STG));
         }
-        sm103::tmem_st16(tS + q * 16, pp);   // P^T over S^T (its first 32 columns)
-        sm103::tmem_st16(tDP + q * 16, pd);  // dS^T over dP^T
+        // The stage's LSE and D vectors were written by the producer lanes: wait on
+        // their barrier directly (already complete) to acquire those stores.
+        if (!(ok = warp_wait(bar(C::B_SFULL + st), uint32_t(g / NSTAGE) & 1u, ab))) break;
+        sm103::tc_fence_after();
+        const int i0 = (u.it0 + g - gs) * SQ + sub * HQ;
+        // query column c sees this key iff n <= i0 + c + kv_off, i.e. c >= n - kv_off - i0
+        const int cmin = key_live ? (CAUSAL ? n - p.kv_off - i0 : 0) : HQ;
+        const float2* lv = reinterpret_cast<const float2*>(vec + (st * 2 + 0) * SQ + sub * HQ);
+        const float2* dv = reinterpret_cast<const float2*>(vec + (st * 2 + 1) * SQ + sub * HQ);
+        const uint32_t tS = tmem + lane_off + uint32_t(hf) * C::BUF + C::COL_S, tDP = tS + (C::COL_DP - C::COL_S);
+        // S^T and dP^T are adjacent: one load of 2 HQ columns, one wait.
+        static_assert(C::COL_DP == C::COL_S + HQ, "S^T, dP^T adjacent");
+        uint32_t uu[2 * HQ];
+        if constexpr (HQ == 64)
+          sm103::tmem_ld128(tS, uu);
+        else
+          tmem_ld64(tS, uu);
+#pragma unroll
+        for (int q = 0; q < HQ / 32; ++q) {
+          uint32_t pp[16], pd[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const int c = q * 32 + 2 * e;
+            const float2 l2 = lv[c / 2], d2 = dv[c / 2];
+            const uint64_t t = sm103::f2_fma(sm103::f2_pack(__uint_as_float(uu[c]), __uint_as_float(uu[c + 1])),
+                                             sl2x2, sm103::f2_pack(-l2.x, -l2.y));
+            float t0, t1;
+            sm103::f2_unpack(t, t0, t1);
+            const float p0 = c < cmin ? 0.f : sm103::ex2_approx(t0);
+            const float p1 = c + 1 < cmin ? 0.f : sm103::ex2_approx(t1);
+            pp[e] = sm103::pack_bf16x2(p0, p1);
+            pd[e] = sm103::pack_bf16x2(p0 * (__uint_as_float(uu[HQ + c]) - d2.x),
+                                       p1 * (__uint_as_float(uu[HQ + c + 1]) - d2.y));
+          }
+          sm103::tmem_st16(tS + q * 16, pp);   // P^T over S^T (its first 32 columns)
+          sm103::tmem_st16(tDP + q * 16, pd);  // dS^T over dP^T
+        }
+        sm103::tmem_st_wait();
+        sm103::tc_fence_before();
+        sm103::mbar_arrive(bar(C::B_PF + hf));
       }
-      sm103::tmem_st_wait();
-      sm103::tc_fence_before();
-      sm103::mbar_arrive(bar(C::B_PF + hf));
-    }
-    if (ok) ok = __all_sync(0xffffffffu, wait_bounded(bar(C::B_ACC), 0u, ab));
-    if (ok) {
-      sm103::tc_fence_after();
-      // dV -> bf16 into the idle V tile, dK * scale -> bf16 into the idle K tile.
+      if (ok) ok = warp_wait(bar(C::B_ACC), uint32_t(nu) & 1u, ab);
+      // Staging: the slot of the unit's last stage (PERSIST; its MMAs are done),
+      // else the K and V tiles.  dV into the Q half or the V tile, dK * scale
+      // into the dO half or the K tile (128-byte-swizzle layout).
+      const uint32_t slot = sST + uint32_t((gs + u.niter - 1) % NSTAGE) * 2u * C::STILE;
+      const uint32_t stg_v = PERSIST ? slot : sV, stg_k = PERSIST ? slot + C::STILE : sK;
+      if (ok) {
+        sm103::tc_fence_after();
 #pragma unroll
-      for (int w = 0; w < 2; ++w) {
-        const uint32_t col0 = w == 0 ? C::COL_DV : C::COL_DK;
-        const uint32_t stage = w == 0 ? sV : sK;
-        const float mul = w == 0 ? 1.f : p.scale;
+        for (int w = 0; w < 2; ++w) {
+          const uint32_t col0 = w == 0 ? C::COL_DV : C::COL_DK;
+          const uint32_t stage = w == 0 ? stg_v : stg_k;
+          const float mul = w == 0 ? 1.f : p.scale;
 #pragma unroll
-        for (int q = 0; q < DACC / 32; ++q) {
-          uint32_t v[32];
-          sm103::tmem_ld32(tmem + lane_off + col0 + q * 32, v);
-          uint32_t pk[16];
+          for (int q = 0; q < DACC / 32; ++q) {
+            uint32_t v[32];
+            sm103::tmem_ld32(tmem + lane_off + col0 + q * 32, v);
+            uint32_t pk[16];
 #pragma unroll
-          for (int e = 0; e < 16; ++e)
-            pk[e] = sm103::pack_bf16x2(__uint_as_float(v[2 * e]) * mul, __uint_as_float(v[2 * e + 1]) * mul);
-          const uint32_t rowbase = stage + uint32_t(q >> 1) * kSubTile + uint32_t(r) * 128u;
+            for (int e = 0; e < 16; ++e)
+              pk[e] = sm103::pack_bf16x2(__uint_as_float(v[2 * e]) * mul, __uint_as_float(v[2 * e + 1]) * mul);
+            const uint32_t rowbase = stage + uint32_t(q >> 1) * kSubTile + uint32_t(r) * 128u;
 #pragma unroll
-          for (int c4 = 0; c4 < 4; ++c4) {
-            const uint32_t chunk = uint32_t((q & 1) * 4 + c4);
-            sm103::st_shared_v4(rowbase + ((chunk ^ uint32_t(r & 7)) << 4), pk[4 * c4], pk[4 * c4 + 1], pk[4 * c4 + 2],
-                                pk[4 * c4 + 3]);
+            for (int c4 = 0; c4 < 4; ++c4) {
+              const uint32_t chunk = uint32_t((q & 1) * 4 + c4);
+              sm103::st_shared_v4(rowbase + ((chunk ^ uint32_t(r & 7)) << 4), pk[4 * c4], pk[4 * c4 + 1],
+                                  pk[4 * c4 + 2], pk[4 * c4 + 3]);
+            }
           }
         }
+        // dK, dV are in registers and shared memory: the next unit may overwrite them in TMEM.
+        sm103::tc_fence_before();
+        sm103::mbar_arrive(bar(C::B_EPI));
+        sm103::fence_proxy_async_smem();
       }
-      sm103::fence_proxy_async_smem();
-    }
-    ok = sm103::named_bar_and(1, BM, ok);
-    if (ok && r == 0) {
-      for (int kb = 0; kb < DACC / 64; ++kb) {
-        sm103::tma_store_3d(&p.tdv, sV + kb * kSubTile, half * DACC + kb * 64, n0, bh);
-        sm103::tma_store_3d(&p.tdk, sK + kb * kSubTile, half * DACC + kb * 64, n0, bh);
+      ok = sm103::named_bar_and(1, BM, ok);
+      if (!ok) break;
+      if (r == 0) {
+        for (int kb = 0; kb < DACC / 64; ++kb) {
+          sm103::tma_store_3d(&p.tdv, stg_v + kb * kSubTile, u.half * DACC + kb * 64, u.n0, u.bh);
+          sm103::tma_store_3d(&p.tdk, stg_k + kb * kSubTile, u.half * DACC + kb * 64, u.n0, u.bh);
+        }
+        sm103::bulk_commit();
       }
-      sm103::bulk_commit();
-      sm103::bulk_wait_read0();
+      gs += u.niter;
+      gh += nh;
     }
+    if (r == 0) sm103::bulk_wait_read0();  // the stores have read shared memory
   }
   sm103::tc_fence_before();
   __syncthreads();
