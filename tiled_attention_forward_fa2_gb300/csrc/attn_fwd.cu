@@ -119,6 +119,11 @@ bool ranges_overlap(const void* a, uint64_t na, const void* b, uint64_t nb) {
 // at about 38 tiles; measured on GB300, 32 tiles (N = 4096) still gains and
 // 128 (N = 16384) loses 6 %.
 constexpr int64_t kPersistMaxKeyTiles = 32;
+// Causal: up to 16.  The one-unit grid hands P over in two halves (split P),
+// which only it does: causal b4h16n4096d128 1383 against 1286 TFLOP/s
+// persistent; b8h16n2048d128 1075 against 1070; b16h16n1024d128 726 against
+// 760 (CUDA events, L2 flushed, mean of 60).
+constexpr int64_t kPersistMaxKeyTilesCausal = 16;
 
 // Process-wide overrides set by attn_set_tuning (0 = the launcher's own choice).
 // Read once per call with relaxed loads: a call sees either the old or the new value.
@@ -243,7 +248,7 @@ FwdPlan plan_fwd(int64_t BH, int64_t Nq, int64_t Nk, int64_t D, bool causal, int
   // attn_set_tuning forces the choice (testing and tuning).
   // At D <= 64 a key step costs about half as much, so the persistent grid wins
   // at every length measured (N = 4096: +6 %, 16384: +2.5 %).
-  bool persist = D <= 64 || n_ktiles <= kPersistMaxKeyTiles;
+  bool persist = D <= 64 || n_ktiles <= (causal ? kPersistMaxKeyTilesCausal : kPersistMaxKeyTiles);
   if (const int g = g_tune_grid.load(std::memory_order_relaxed)) persist = g == 2;
   if (D > 128) persist = false;  // the D = 256 kernel stages O in its Q buffer
   int64_t ctas = persist && pl.n_work > sms ? sms : pl.n_work;
