@@ -53,6 +53,7 @@ struct BwdParams {
   const float* lse;             // [B*H, Nq] natural log
   float* delta;                 // [B*H, Nq] D_i: written by the dQ kernel, read by the dK/dV kernel
   int Nq, Nk, kv_off, bh, n_qtiles, n_ktiles;
+  int lpt;                      // causal dQ order: heads per longest-first band (0: a head's tiles adjacent)
   int d;                        // true head dim (<= the kernel's D; the rest is zero padding)
   int ld;                       // row stride (elements) of every [.., N, D] tensor: a multiple of 8, >= d
   float scale;                  // softmax scale
@@ -105,11 +106,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dq_sm103(const __grid
   auto bar = [base](int i) { return base + 8u * uint32_t(i); };
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  // Causal: heaviest query tiles first; full: the tiles of one head adjacent.
+  // Causal with bands (p.lpt > 0): heaviest query tiles first within bands of
+  // p.lpt heads.  Otherwise (full, or causal tiles of about equal key ranges
+  // whose K and V exceed half of L2) the tiles of one head are adjacent, so
+  // the CTAs running at one time read its K and V from HBM once.
   int qt, bh;
-  if (CAUSAL) {
-    qt = p.n_qtiles - 1 - int(blockIdx.x / uint32_t(p.bh));
-    bh = int(blockIdx.x % uint32_t(p.bh));
+  if (CAUSAL && p.lpt) {
+    const int span = p.lpt * p.n_qtiles;
+    const int band = int(blockIdx.x) / span, idx = int(blockIdx.x) - band * span;
+    const int g = min(p.lpt, p.bh - band * p.lpt);
+    qt = p.n_qtiles - 1 - idx / g;
+    bh = band * p.lpt + idx % g;
   } else {
     qt = int(blockIdx.x % uint32_t(p.n_qtiles));
     bh = int(blockIdx.x / uint32_t(p.n_qtiles));
