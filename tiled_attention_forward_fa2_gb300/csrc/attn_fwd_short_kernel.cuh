@@ -20,13 +20,16 @@
 //   warp 4    : TMA producer (Q into one of two buffers, K/V through a ring);
 //   warp 5    : TMEM allocation and warp-uniform MMA issue;
 //   warps 6-7 : idle (they complete the second warpgroup for setmaxnreg).
-// TMEM: S/P at columns 0..127, O at 128..191.
-// Per unit and key step j: S_j = Q K_j^T -> softmax -> P_j (bf16 over S_j) ->
-// O += P_j V_j; S_{j+1} is issued right behind P_j V_j, and the next unit's
-// S_0 right behind the last P V, so it is ready when the softmax warps come
-// back from the epilogue.  The softmax warps read O for the epilogue before
-// they hand over the next unit's first P, which is what the next unit's first
-// P V (writing O afresh) waits for.  Every wait is bounded (wait_bounded).
+// TMEM: S at columns 0..127, O at 128..191, P (bf16 pairs) at 192..255.
+// Per unit and key step j: S_j = Q K_j^T -> softmax -> P_j -> O += P_j V_j.
+// P has columns of its own, so S_{j+1} is issued as soon as the softmax warps
+// have loaded S_j into registers (B_SR), and runs while they compute P_j: a
+// key step costs the softmax alone, not the softmax plus P V plus the next S.
+// The next unit's S_0 goes out the same way behind the last step's load.  The
+// softmax waits for P_{j-1} V_{j-1} (B_PVD) before it writes P_j or rescales
+// O.  The softmax warps read O for the epilogue before they hand over the
+// next unit's first P, which is what the next unit's first P V (writing O
+// afresh) waits for.  Every wait is bounded (wait_bounded).
 #pragma once
 #include "attn_fwd_kernel.cuh"
 
@@ -60,10 +63,12 @@ struct CfgShort {
   static constexpr int B_SF = 2 * NQB + 2 * NSLOT;    // S_j ready (MMA commit)
   static constexpr int B_PF = B_SF + 1;               // P_j in TMEM, O rescaled (128 arrivals)
   static constexpr int B_OF = B_PF + 1;               // the unit's last P V done (MMA commit)
-  static constexpr int B_DONE = B_OF + 1;
+  static constexpr int B_SR = B_OF + 1;               // S_j loaded by the softmax warps (128 arrivals)
+  static constexpr int B_PVD = B_SR + 1;              // P_j V_j done (MMA commit)
+  static constexpr int B_DONE = B_PVD + 1;
   static constexpr int NBAR = B_DONE + 1;
   static_assert(NBAR * 8 <= 512, "barrier area");
-  static constexpr uint32_t COL_S = 0, COL_O = 128, kCols = 256;
+  static constexpr uint32_t COL_S = 0, COL_O = 128, COL_P = 192, kCols = 256;
 };
 
 template <bool CAUSAL>
@@ -87,7 +92,8 @@ __global__ void __launch_bounds__(kShortThreads, 2) attn_fwd_short_sm103(const _
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::NBAR; ++i)
-      sm103::mbar_init(bar(i), i == C::B_PF ? uint32_t(BM) : (i >= C::B_OS && i < C::B_OS + NQB) ? 4u : 1u);
+      sm103::mbar_init(bar(i), (i == C::B_PF || i == C::B_SR) ? uint32_t(BM)
+                               : (i >= C::B_OS && i < C::B_OS + NQB) ? 4u : 1u);
     *abort_flag = 0u;
     sm103::fence_mbar_init();
   }
@@ -148,39 +154,43 @@ __global__ void __launch_bounds__(kShortThreads, 2) attn_fwd_short_sm103(const _
       auto slot_off = [](int c) { return uint32_t(c % NSLOT) * (C::TILE >> 4); };
       auto wait_full = [&](int c) { return warp_wait(bar(C::B_FULL + c % NSLOT), uint32_t(c / NSLOT) & 1u, ab); };
       auto release = [&](int c) { sm103::mma_commit_warp(bar(C::B_EMPTY + c % NSLOT)); };
-      const uint32_t dS = tmem + C::COL_S, dO = tmem + C::COL_O;
+      const uint32_t dS = tmem + C::COL_S, dO = tmem + C::COL_O, dP = tmem + C::COL_P;
       int cb = 0;   // ring index of the current unit's K_0
-      int ns = 0;   // key steps so far (B_PF phases)
+      int ns = 0;   // key steps so far (B_SF, B_SR, B_PF, B_PVD phases)
       int nu = 0;   // units so far (Q buffer, B_Q phase, B_OF)
       bool ok = true;
       for (int k = 0; ok && more(k); ++k) {
         const int nk = unit_of<CAUSAL>(p, work(k)).nk0;
         const int qi = nu % NQB;
-        auto issue_s = [&](int j) {  // S_j = Q K_j^T
+        // S_j = Q K_j^T, once the softmax warps have loaded S of the step
+        // before (global step g - 1) out of TMEM.
+        auto issue_s = [&](int j) -> bool {
+          const int g = ns + j;
+          if (g > 0 && !warp_wait(bar(C::B_SR), uint32_t(g - 1) & 1u, ab)) return false;
+          sm103::tc_fence_after();
           const uint32_t dk = desc_k + slot_off(cb + 2 * j), dq = desc_q + uint32_t(qi) * (C::TILE >> 4);
 #pragma unroll
           for (int kk = 0; kk < C::D / 16; ++kk)
             sm103::mma_ss_warp_lo(dS, dq + uint32_t(kk) * 2u, dk + uint32_t(kk) * 2u, kIdescS, kk > 0 ? 1u : 0u, hi);
           sm103::mma_commit_warp(bar(C::B_SF));
+          release(cb + 2 * j);  // K_j is done with once S_j is
+          return true;
         };
         if (!(ok = warp_wait(bar(C::B_Q + qi), uint32_t(nu / NQB) & 1u, ab) && wait_full(cb))) break;
         sm103::tc_fence_after();
-        issue_s(0);
-        release(cb);
+        if (!(ok = issue_s(0))) break;
         for (int j = 0; ok && j < nk; ++j) {
-          const bool next = j + 1 < nk;
+          if (j + 1 < nk && !(ok = wait_full(cb + 2 * j + 2) && issue_s(j + 1))) break;
           if (!(ok = wait_full(cb + 2 * j + 1))) break;
-          if (next && !(ok = wait_full(cb + 2 * j + 2))) break;
           if (!(ok = warp_wait(bar(C::B_PF), uint32_t(ns + j) & 1u, ab))) break;
           sm103::tc_fence_after();
           const uint32_t dv = desc_v + slot_off(cb + 2 * j + 1);
 #pragma unroll
           for (int kk = 0; kk < BN / 16; ++kk)  // 16 keys per MMA: 8 TMEM columns of P, 16 rows of V
-            sm103::mma_ts_warp_lo(dO, dS + uint32_t(kk) * 8u, dv + uint32_t(kk) * (2048u >> 4), kIdescO,
+            sm103::mma_ts_warp_lo(dO, dP + uint32_t(kk) * 8u, dv + uint32_t(kk) * (2048u >> 4), kIdescO,
                                   (j > 0 || kk > 0) ? 1u : 0u, hi);
-          if (next) issue_s(j + 1);
+          sm103::mma_commit_warp(bar(C::B_PVD));
           release(cb + 2 * j + 1);
-          if (next) release(cb + 2 * j + 2);
         }
         if (!ok) break;
         sm103::mma_commit_warp(bar(C::B_OF));
@@ -198,7 +208,7 @@ __global__ void __launch_bounds__(kShortThreads, 2) attn_fwd_short_sm103(const _
     sm103::regs_set<kShortRegSoftmax, kShortRegLaunch>();
     const int r = threadIdx.x;  // row of the tile = TMEM lane
     const uint32_t lane_off = uint32_t(warp * 32) << 16;
-    const uint32_t tS = tmem + lane_off + C::COL_S, tO = tmem + lane_off + C::COL_O;
+    const uint32_t tS = tmem + lane_off + C::COL_S, tO = tmem + lane_off + C::COL_O, tP = tmem + lane_off + C::COL_P;
     const float sl2 = p.scale_log2;
     const uint64_t sl2x2 = sm103::f2_pack(sl2, sl2);
     int ns = 0, nu = 0;  // key steps and units so far (B_SF, B_OF phases)
@@ -223,6 +233,9 @@ __global__ void __launch_bounds__(kShortThreads, 2) attn_fwd_short_sm103(const _
 #pragma unroll
           for (int c = 0; c < BN; ++c) s[c] = __uint_as_float(uu[c]);
         }
+        // S_j is in registers: its columns go back to the MMA warp for S_{j+1}.
+        sm103::tc_fence_before();
+        sm103::mbar_arrive(bar(C::B_SR));
         // Masks: keys past N, and keys after the query row when causal.
         int lim = min(BN - 1, p.Nk - 1 - j * BN);
         if (CAUSAL) lim = min(lim, diag - j * BN);
@@ -260,13 +273,17 @@ __global__ void __launch_bounds__(kShortThreads, 2) attn_fwd_short_sm103(const _
         // exponential unit is what a key step waits on, and the warp of the
         // other CTA on this sub-partition gets the cycles.
         const int wlim = __reduce_max_sync(0xffffffffu, lim);
+        // P_{j-1} V_{j-1} has read P and written O (at j = 0 the epilogue
+        // already waited for the previous unit's last P V).
+        if (j > 0 && !(ok = warp_wait(bar(C::B_PVD), uint32_t(ns + j - 1) & 1u, ab))) break;
+        sm103::tc_fence_after();
 #pragma unroll
         for (int q = 0; q < BN / 32; ++q) {
           uint32_t pk[16];
           if (q * 32 > wlim) {
 #pragma unroll
             for (int e = 0; e < 16; ++e) pk[e] = 0u;
-            sm103::tmem_st16(tS + q * 16, pk);
+            sm103::tmem_st16(tP + q * 16, pk);
             continue;
           }
 #pragma unroll
@@ -282,15 +299,15 @@ __global__ void __launch_bounds__(kShortThreads, 2) attn_fwd_short_sm103(const _
             else
               acc0 = sm103::f2_add(acc0, sm103::f2_pack(p0, p1));
           }
-          sm103::tmem_st16(tS + q * 16, pk);  // P over the first 64 columns of S
+          sm103::tmem_st16(tP + q * 16, pk);
         }
         float a0, a1, a2, a3;
         sm103::f2_unpack(acc0, a0, a1);
         sm103::f2_unpack(acc1, a2, a3);
         const float rowsum = (a0 + a1) + (a2 + a3);
         l_run = j == 0 ? rowsum : fmaf(alpha, l_run, rowsum);
-        // O *= alpha when a row of the warp moved its reference max.  The
-        // P V that last wrote O was issued before this step's S, so it is done.
+        // O *= alpha when a row of the warp moved its reference max (the P V
+        // that last wrote O is done: B_PVD above).
         if (__any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll 1
           for (int q = 0; q < C::D / 32; ++q) {
