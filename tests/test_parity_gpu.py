@@ -158,6 +158,8 @@ def test_kernel_names_follow_the_launcher():
     assert name(4, 16, 4096, 4096, 128, True) == "attn_fwd_sm103<128,causal,one unit per CTA,2 tiles/unit>"
     assert name(8, 16, 2048, 2048, 128, True) == "attn_fwd_sm103<128,causal,persistent,2 tiles/unit>"
     assert name(16, 32, 512, 512, 64, True) == "attn_fwd_short_sm103<causal>"
+    assert name(16, 32, 512, 512, 64, False) == "attn_fwd_short_sm103<full>"
+    assert name(4, 16, 4096, 4096, 64, False) == "attn_fwd_sm103<64,full,persistent,2 tiles/unit>"
     assert name(2, 8, 1024, 1024, 64, False) == "attn_fwd_sm103<64,full,persistent,key split>"
     assert name(1, 2, 300, 300, 200, True).startswith("attn_fwd_sm103<256,causal,one unit per CTA,1 tile/unit")
     tune(unit=1, grid=1)

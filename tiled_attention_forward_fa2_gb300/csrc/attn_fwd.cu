@@ -201,15 +201,17 @@ FwdPlan plan_fwd(int64_t BH, int64_t Nq, int64_t Nk, int64_t D, bool causal, int
   // time is one unit's chain; b2h8n1024d64: 128 tiles on 152 SMs).  Beyond a
   // wave its extra per-unit cost (Q load, merge) loses to two tiles per unit.
   bool split = D <= 64 && n_ktiles >= 2 && n_qtiles * BH <= sms;
-  // Short-unit kernel (D <= 64, two CTAs per SM, one tile per unit): causal
-  // problems of short rows, where the two tiles of a unit differ in length
-  // and unit boundaries come every few key steps, with at least a full wave
-  // of its grid.  Measured (CUDA events, L2 flushed, mean of 150): causal
-  // b16h32n512d64 46.1 against 54.9 us, b32h32n256d64 37.7 against 44.5,
-  // b8h16n1024d64 37.6 against 40.5, b4h32n2048d64 97.9 against 99.5; it lost
-  // on full rows (b16h32n512d64 54.0 against 51.9), on a short query block
-  // against 4096 keys and below a wave (b2h8n1024d64 causal 17.3 against 16.7).
-  bool shortk = D <= 64 && causal && n_ktiles <= 16 && n_qtiles >= 2 && n_qtiles * BH >= 2 * sms;
+  // Short-unit kernel (D <= 64, two CTAs per SM, one tile per unit): short
+  // rows, where unit boundaries come every few key steps (and, causal, the two
+  // tiles of a unit differ in length), with at least a full wave of its grid.
+  // Measured (CUDA events, L2 flushed, mean of 50-150): causal b16h32n512d64
+  // 43.7 against 54.9 us, b32h32n256d64 35.5 against 44.5, b8h16n1024d64
+  // 35.5 against 40.5, b4h32n2048d64 100.3 against 99.9; full rows up to 8
+  // key tiles b16h32n512d64 50.3 against 51.4, b8h16n1024d64 49.9 against
+  // 51.9.  It loses on longer full rows (b4h16n4096d64 300 against 285: the
+  // two-tile unit's shared K/V stream), on a short query block against 4096
+  // keys and below a wave (b2h8n1024d64 causal 17.3 against 16.7).
+  bool shortk = D <= 64 && n_qtiles >= 2 && n_qtiles * BH >= 2 * sms && n_ktiles <= (causal ? 16 : 8);
   if (shortk) split = false;
   if (const int u = g_tune_unit.load(std::memory_order_relaxed)) {
     T = u >= 3 ? 1 : u;
