@@ -257,7 +257,7 @@ def time_backward(pkg, w, qd, kd, vd, o, lse, stream, dev, flush, scratch, steps
     flops = pkg.attn_bwd_qk_flops(w.B, w.H, w.N, w.n_keys, w.D, w.causal)
     return {"metric": "attention bwd TFLOP/s (dQ, dK, dV; 2.5x the forward FLOPs)", "value": job_tflops(flops, world, ms),
             "unit": "TFLOP/s", "ms_per_step": ms, "steps": steps, "gpu_launches": 2 * steps,
-            "kernels": "attn_bwd_dq_sm103 + attn_bwd_dkdv_sm103"}
+            "kernels": "attn_bwd_dq_sm103 + attn_bwd_dkdv_sm103", "traffic": ncu_traffic(w.name, "attn_bwd", "bwd")}
 
 
 def based_config(w, world=1):
@@ -663,7 +663,7 @@ def run_ours(args, w):
                     "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
                     "dtype": "bf16", "data": "synthetic", "config": workload_config(w, world, {"pass": "backward"}),
                     "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                                 "frac": achieved / peak, "traffic": None,
+                                 "frac": achieved / peak, "traffic": ncu_traffic(w.name, "attn_bwd", "bwd"),
                                  "peak_source": f"bf16_tflops (burst) of {peak_src}",
                                  "kernel": "attn_bwd_dq_sm103 + attn_bwd_dkdv_sm103"},
                     "gpu_launches": 2 * args.steps, "clocks": sampler.summary() if sampler else None,

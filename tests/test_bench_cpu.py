@@ -57,7 +57,8 @@ def test_committed_profiles_carry_traffic_for_the_current_sources():
                                      ("b16h32n512d64_causal", "attn_fwd_short_sm103", "fwd"),
                                      ("b2h8n1024d64", "attn_fwd_sm103", "fwd"),
                                      ("b8h16nq512nk8192d128_causal", "attn_fwd_sm103", "fwd"),
-                                     ("based_b16h16n4096f16d64", "based_fwd_sm103", "based")):
+                                     ("based_b16h16n4096f16d64", "based_fwd_sm103", "based"),
+                                     ("b4h16n4096d128", "attn_bwd", "bwd")):
         traffic = bench.ncu_traffic(workload, kernel, family)
         assert traffic is not None and traffic > 0, (workload, kernel)
 
