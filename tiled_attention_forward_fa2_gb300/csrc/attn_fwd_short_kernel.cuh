@@ -273,17 +273,12 @@ __global__ void __launch_bounds__(kShortThreads, 2) attn_fwd_short_sm103(const _
         // exponential unit is what a key step waits on, and the warp of the
         // other CTA on this sub-partition gets the cycles.
         const int wlim = __reduce_max_sync(0xffffffffu, lim);
-        // P_{j-1} V_{j-1} has read P and written O (at j = 0 the epilogue
-        // already waited for the previous unit's last P V).
-        if (j > 0 && !(ok = warp_wait(bar(C::B_PVD), uint32_t(ns + j - 1) & 1u, ab))) break;
-        sm103::tc_fence_after();
+        uint32_t pk[BN / 32][16];
 #pragma unroll
         for (int q = 0; q < BN / 32; ++q) {
-          uint32_t pk[16];
           if (q * 32 > wlim) {
 #pragma unroll
-            for (int e = 0; e < 16; ++e) pk[e] = 0u;
-            sm103::tmem_st16(tP + q * 16, pk);
+            for (int e = 0; e < 16; ++e) pk[q][e] = 0u;
             continue;
           }
 #pragma unroll
@@ -293,14 +288,20 @@ __global__ void __launch_bounds__(kShortThreads, 2) attn_fwd_short_sm103(const _
             sm103::f2_unpack(t, t_lo, t_hi);
             const float p0 = sm103::ex2_approx(t_lo);
             const float p1 = sm103::ex2_approx(t_hi);
-            pk[e] = sm103::pack_bf16x2(p0, p1);
+            pk[q][e] = sm103::pack_bf16x2(p0, p1);
             if (e & 1)
               acc1 = sm103::f2_add(acc1, sm103::f2_pack(p0, p1));
             else
               acc0 = sm103::f2_add(acc0, sm103::f2_pack(p0, p1));
           }
-          sm103::tmem_st16(tP + q * 16, pk);
         }
+        // P_{j-1} V_{j-1} has read P and written O (at j = 0 the epilogue
+        // already waited for the previous unit's last P V): only the stores of
+        // P_j and the rescale of O wait for it, the exponentials above do not.
+        if (j > 0 && !(ok = warp_wait(bar(C::B_PVD), uint32_t(ns + j - 1) & 1u, ab))) break;
+        sm103::tc_fence_after();
+#pragma unroll
+        for (int q = 0; q < BN / 32; ++q) sm103::tmem_st16(tP + q * 16, pk[q]);
         float a0, a1, a2, a3;
         sm103::f2_unpack(acc0, a0, a1);
         sm103::f2_unpack(acc1, a2, a3);
