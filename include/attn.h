@@ -34,7 +34,7 @@ extern "C" {
 typedef enum {
   ATTN_OK = 0,
   ATTN_ERR_INVALID_ARG = 1, /* null/misaligned/overlapping pointer, bad size or scale */
-  ATTN_ERR_UNSUPPORTED = 2, /* valid request this build does not implement (head dim, lengths, device) */
+  ATTN_ERR_UNSUPPORTED = 2, /* valid request this library does not implement (head dim, lengths, device) */
   ATTN_ERR_CUDA = 3,        /* a CUDA runtime or driver call failed (launch, tensor map, ...) */
   ATTN_ERR_TIMEOUT = 4      /* a kernel pipeline wait exceeded its bound and the kernel gave up */
 } attn_status_t;
