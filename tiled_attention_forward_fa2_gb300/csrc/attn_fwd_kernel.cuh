@@ -459,18 +459,29 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_sm103(const __grid_const
         if constexpr (SPLITK) {
           // Step j: P V of key tiles 2j (slot 0) and 2j + 1 (slot 1), then S of
           // key tiles 2j + 2 and 2j + 3 for the next step.
+          // Each product waits only for its own tile: a P V for its V, an S
+          // for its K (waiting for the next K tiles before this step's P V held
+          // the P V back by a load latency whenever those K tiles were still in
+          // flight, as on short units whose ring slots refill late).
           for (int j = 0; ok && j < nk; ++j) {
             const bool has1 = j < nk1, next0 = j + 1 < nk0, next1 = j + 1 < nk1;
-            if (next0 && !(ok = wait_full(int(cb) + 2 * (2 * j + 2)))) break;
-            if (next1 && !(ok = wait_full(int(cb) + 2 * (2 * j + 3)))) break;
             if (!(ok = wait_full(int(cb) + 2 * (2 * j) + 1))) break;
-            if (has1 && !(ok = wait_full(int(cb) + 2 * (2 * j + 1) + 1))) break;
             sm103::tc_fence_after();
             if (!(ok = issue_pv(0, j))) break;
-            if (next0) issue_s(0, j + 1);
+            if (next0) {
+              if (!(ok = wait_full(int(cb) + 2 * (2 * j + 2)))) break;
+              sm103::tc_fence_after();
+              issue_s(0, j + 1);
+            }
             if (has1) {
+              if (!(ok = wait_full(int(cb) + 2 * (2 * j + 1) + 1))) break;
+              sm103::tc_fence_after();
               if (!(ok = issue_pv(1, j))) break;
-              if (next1) issue_s(1, j + 1);
+              if (next1) {
+                if (!(ok = wait_full(int(cb) + 2 * (2 * j + 3)))) break;
+                sm103::tc_fence_after();
+                issue_s(1, j + 1);
+              }
             }
             release(int(cb) + 2 * (2 * j) + 1);
             if (has1) release(int(cb) + 2 * (2 * j + 1) + 1);
@@ -481,6 +492,21 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_sm103(const __grid_const
         } else {
         for (int j = 0; ok && j < nk; ++j) {
           const bool next = j + 1 < nk;
+          if constexpr (D > 128) {
+            // One tile per unit (D = 256): its P V waits only for V_j, the next
+            // S for K_{j+1}.  Waiting for K_{j+1} first held each P V back by a
+            // load latency, the ring being two 64 KB slots (B2 H16 N4096 585 ->
+            // 499 us).  The D <= 128 instances keep K_{j+1} and V_j up front:
+            // there the split order (as a runtime branch) measured 1-5 % slower.
+            if (!(ok = wait_full(int(cb) + 2 * j + 1))) break;
+            sm103::tc_fence_after();
+            if (!(ok = issue_pv(0, j))) break;
+            if (next) {
+              if (!(ok = wait_full(int(cb) + 2 * j + 2))) break;
+              sm103::tc_fence_after();
+              issue_s(0, j + 1);
+            }
+          } else {
           if (next && !(ok = wait_full(int(cb) + 2 * j + 2))) break;
           if (!(ok = wait_full(int(cb) + 2 * j + 1))) break;
           sm103::tc_fence_after();
@@ -491,6 +517,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_sm103(const __grid_const
           if (j < nk1) {
             if (!(ok = issue_pv(1, j))) break;
             if (j + 1 < nk1) issue_s(1, j + 1);
+          }
           }
           release(int(cb) + 2 * j + 1);
           if (next) release(int(cb) + 2 * j + 2);
