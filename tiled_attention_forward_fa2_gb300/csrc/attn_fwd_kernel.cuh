@@ -49,6 +49,20 @@
 
 #include "sm103_ptx.cuh"
 
+namespace sm103 {
+// 128 rows x 256 bits of a shared-memory operand (descriptor as for an MMA
+// operand) into TMEM, 8 columns from `taddr`, in the layout an MMA reads A
+// from TMEM; one elected lane issues it.  Ordered with this thread's later
+// tcgen05.mma, and tracked by its tcgen05.commit.
+__device__ __forceinline__ void tmem_cp_128x256b_warp(uint32_t taddr, uint64_t sdesc) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t.reg .b32 r;\n\telect.sync r|e, 0xffffffff;\n\t"
+      "@e tcgen05.cp.cta_group::1.128x256b [%0], %1;\n}\n" ::"r"(taddr),
+      "l"(sdesc)
+      : "memory");
+}
+}  // namespace sm103
+
 namespace attn {
 
 constexpr int BM = 128;                     // query rows per tile (= TMEM lanes)
@@ -98,16 +112,23 @@ struct Cfg {
   // Q buffers per query tile: at D = 64 two, so a unit's Q loads while the unit
   // before still reads the other (short units would otherwise wait for it).
   static constexpr int NQB = D == 64 ? 2 : 1;
-  // K/V ring slots (one tile each): 2 at D = 256 (one key step ahead).
-  static constexpr int NSLOT = D == 256 ? 2 : (D == 128 ? 4 : 9);
-  // At D = 256 the epilogue stages O in the Q buffer (free once the unit's
-  // last S MMA has finished), so that kernel runs one unit per CTA.
+  // At D = 256 Q is read from TMEM (QT): it lands in ring slot 0 as the
+  // unit's first load, the MMA warp copies it into TMEM columns 128..255
+  // (free beside S and O there) and releases the slot, so the ring has three
+  // 64 KB slots where a separate Q buffer left room for two (K_{j+1} then
+  // loads while step j runs instead of after S_j).
+  static constexpr bool QT = D == 256;
+  // K/V ring slots (one tile each).
+  static constexpr int NSLOT = D == 256 ? 3 : (D == 128 ? 4 : 9);
+  // At D = 256 the epilogue stages O in ring slot 0 (idle once the unit's
+  // products are done), so that kernel runs one unit per CTA.
   static constexpr bool STAGE_IN_Q = D == 256;
   static constexpr uint32_t OFF_INVL = 1024;             // [2][128] fp32: 1/l of each row of tile i
   static constexpr uint32_t OFF_Q = 2048;                // Q buffer i * NQB + b of tile i
   static constexpr uint32_t OFF_STG = STAGE_IN_Q ? OFF_Q : OFF_Q + MAXT * NQB * TILE;  // O staging tile
-  static constexpr uint32_t OFF_KV = OFF_Q + MAXT * NQB * TILE + (STAGE_IN_Q ? 0u : TILE);
+  static constexpr uint32_t OFF_KV = QT ? OFF_Q : OFF_Q + MAXT * NQB * TILE + (STAGE_IN_Q ? 0u : TILE);
   static constexpr uint32_t USED = OFF_KV + NSLOT * TILE;
+  static constexpr uint32_t COL_Q = 128;   // QT: Q (bf16 pairs) in TMEM
   static constexpr uint32_t SMEM = USED + 1024;          // + slack to align the base to 1 KB
   static_assert(SMEM <= 232448, "shared memory");
   // barrier slots ([2]: one per query tile of the unit)
@@ -336,8 +357,16 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_sm103(const __grid_const
                                  (u.t0 + i) * BM, u.bh);
             return true;
           };
-          if (!(ok = load_q(0, nq0))) break;
-          ++nq0;
+          if constexpr (C::QT) {
+            // Q into ring slot 0 as the unit's load 0 (one unit per CTA at D = 256).
+            sm103::mbar_arrive_expect_tx(bar(C::B_FULL), C::TILE);
+            for (int kb = 0; kb < KB; ++kb)
+              sm103::tma_load_3d(sKV + kb * kSubTile, &p.tq, bar(C::B_FULL), kb * 64, u.t0 * BM, u.bh);
+            ++c;
+          } else {
+            if (!(ok = load_q(0, nq0))) break;
+            ++nq0;
+          }
           if (!SPLITK && u.nk1 > 0) {
             if (!(ok = load_q(1, nq1))) break;
             ++nq1;
@@ -410,9 +439,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_sm103(const __grid_const
 #pragma unroll(kUnrollS)
           for (int kk = 0; kk < D / 16; ++kk) {  // 16 of the head dim per MMA
             const uint32_t off = (uint32_t(kk >> 2) * kSubTile + uint32_t(kk & 3) * 32u) >> 4;
-            sm103::mma_ss_warp_lo(dS, dq + off, dk + off, kIdescS, kk > 0 ? 1u : 0u, hi);
+            if constexpr (C::QT)
+              sm103::mma_ts_warp_lo(dS, tmem + C::COL_Q + uint32_t(kk) * 8u, dk + off, kIdescS, kk > 0 ? 1u : 0u, hi);
+            else
+              sm103::mma_ss_warp_lo(dS, dq + off, dk + off, kIdescS, kk > 0 ? 1u : 0u, hi);
           }
           sm103::mma_commit_warp(bar(C::B_SF + i));
+          if constexpr (C::QT) return;  // Q is in TMEM: no Q buffer to free
           // Q buffer no longer read: after the unit's last S MMA on it.  With the
           // key split that is slot 0's last S when the unit has an odd number of
           // key tiles (nk0 = nk1 + 1), else slot 1's -- exactly one commit per unit.
@@ -441,8 +474,23 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_sm103(const __grid_const
           sm103::mma_commit_warp(bar(C::B_OF + i));
           return true;
         };
-        ok = warp_wait(bar(C::B_Q + nu0 % C::NQB), uint32_t(nu0 / C::NQB) & 1u, ab) && wait_full(int(cb));
-        if (!ok) break;
+        if constexpr (C::QT) {
+          // Q (ring load 0) into TMEM, 16 columns of the head dim per copy,
+          // then slot 0 goes back to the ring (the commit follows the copies).
+          if (!(ok = wait_full(0))) break;
+          sm103::tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint64_t dq = sm103::sdesc_sw128(sKV + uint32_t(kk >> 2) * kSubTile + uint32_t(kk & 3) * 32u, 16, 1024);
+            sm103::tmem_cp_128x256b_warp(tmem + C::COL_Q + uint32_t(kk) * 8u, dq);
+          }
+          release(0);
+          cb = 1;  // K_j is load 1 + 2 j, V_j load 2 + 2 j
+        } else {
+          ok = warp_wait(bar(C::B_Q + nu0 % C::NQB), uint32_t(nu0 / C::NQB) & 1u, ab);
+          if (!ok) break;
+        }
+        if (!(ok = wait_full(int(cb)))) break;
         sm103::tc_fence_after();
         issue_s(0, 0);
         if (nk1 > 0) {
