@@ -551,8 +551,9 @@ def run_ours(args, w):
         dq, dk, dv = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
         delta = torch.empty_like(lse)
 
-    # Forward steps on a working set below 2x L2 rotate over copies of the inputs
-    # and outputs (the same values), so every step reads inputs that are not in L2.
+    # Copies of the inputs and outputs (the same values) for the back-to-back leg
+    # of a working set below 2x L2: rotating over them, every launch reads inputs
+    # that are not in L2.  The timed steps use the first copy, after a flush.
     sets = [(qd, kd, vd, o, lse)]
     if flush and not args.backward:
         sets += [(qd.clone(), kd.clone(), vd.clone(), torch.empty_like(o), torch.empty_like(lse))
