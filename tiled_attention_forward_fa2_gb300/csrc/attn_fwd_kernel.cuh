@@ -20,14 +20,17 @@
 // it (long key ranges, D = 256) each CTA runs one unit.
 //   warp 12      : TMA producer.  Q tiles of each unit (into a buffer of the
 //                  tile once the last S MMA of the unit that used it before has
-//                  finished; two buffers per tile at D = 64); K_j, V_j into a
-//                  ring of 128-byte-swizzled shared-memory slots (full/empty
-//                  mbarriers).
+//                  finished; two buffers per tile at D = 64; at D = 256 into
+//                  the K/V ring's slot 0 as the unit's first load); K_j, V_j
+//                  into a ring of 128-byte-swizzled shared-memory slots
+//                  (full/empty mbarriers).
 //   warp 13      : allocates the 512 TMEM columns; one thread issues tcgen05.mma:
 //                  S_i = Q_i K_j^T into TMEM buffer i, and O_i += P_i V_j with P_i
 //                  read back from TMEM (bf16, written over S_i).  The order
 //                  PV_0(j), S_0(j+1), PV_1(j), S_1(j+1) keeps the tensor core on
-//                  one tile while the other tile's softmax runs (ping-pong).
+//                  one tile while the other tile's softmax runs (ping-pong).  At
+//                  D = 256 it first copies Q into TMEM (tcgen05.cp) and reads it
+//                  from there, which frees Q's slot for K and V.
 //   warpgroup i  : (i = 0, 1; warps 4i..4i+3) softmax of query tile i, one
 //                  thread per row (= TMEM lane).  Masks, running max in base 2,
 //                  p = 2^(s*scale*log2e - m) with packed fp32x2 math, P -> TMEM,
